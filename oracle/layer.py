@@ -1,0 +1,123 @@
+"""Oracle of one decoder-layer forward over a packed hybrid batch (test
+infrastructure only).
+
+What the hybrid iteration computes (chunked prefill, Sarathi-Serve reading
+notes section 3.1; chunked prefill knowledge page, mechanism section): chunk i
+of a prompt covers positions [(i-1)C, iC), writes their KV into the paged
+cache, and its queries attend to every key written by earlier chunks plus the
+causal part of their own chunk; a decode row attends to its full context.
+Chunking only re-partitions the work, so the result is the plain causal
+attention of every row over keys 0..pos.
+
+The layer arithmetic (absent from the pages) is the Llama/Mistral pre-norm
+block without biases:
+    xn = RMSNorm(x; g1)                y = x / sqrt(mean(x^2) + eps) * g
+    q, k, v = split(xn W_qkv^T)
+    q, k = RoPE(q, k; pos)             rotate-half, inv_freq_i = theta^(-2i/d_head)
+    k, v -> paged cache at slot        (k stored after rotation)
+    o = softmax(q k^T / sqrt(d_head)) v     per q head h on kv head h*n_kv//n_q
+    h = x + o W_o^T
+    out = h + (silu(hn W_g^T) * (hn W_u^T)) W_d^T,  hn = RMSNorm(h; g2)
+
+Everything is computed in `dtype` (float32 by default), with no intermediate
+rounding; inputs are the bf16-representable values the GPU also sees.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def rmsnorm(x, g, eps, dtype=np.float32):
+    x = np.asarray(x, dtype)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + dtype(eps)) * np.asarray(g, dtype)
+
+
+def rope_tables(max_pos, d_head, theta):
+    """cos/sin of pos * theta^(-2i/d_head), i < d_head/2, computed in float64 and
+    rounded to float32 (shape [max_pos, d_head/2])."""
+    i = np.arange(d_head // 2, dtype=np.float64)
+    inv_freq = np.power(np.float64(theta), -2.0 * i / d_head)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv_freq[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+def rope(x, pos, cos, sin, dtype=np.float32):
+    """Rotate-half RoPE. x [rows, heads, d_head], pos [rows]."""
+    x = np.asarray(x, dtype)
+    half = x.shape[-1] // 2
+    c = np.asarray(cos, dtype)[pos][:, None, :]
+    s = np.asarray(sin, dtype)[pos][:, None, :]
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def silu(x):
+    return x / (1 + np.exp(-x))
+
+
+def kv_append(k, v, slots, k_pool, v_pool, page):
+    """Write rows' K [rows, n_kv, d_head] and V into the paged pools at slots."""
+    for r, sl in enumerate(slots):
+        k_pool[sl // page, :, sl % page, :] = k[r]
+        v_pool[sl // page, :, sl % page, :] = v[r]
+
+
+def gather_keys(pool, table_row, n_keys, page):
+    """Keys 0..n_keys-1 of one sequence through its block table -> [n_keys, n_kv, d]."""
+    j = np.arange(n_keys)
+    pages = np.asarray(table_row)[j // page]
+    return pool[pages, :, j % page, :]
+
+
+def attention(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype=np.float32):
+    """q [T, n_q, d_head] -> o [T, n_q, d_head]; row r of sequence s at
+    position p attends to keys 0..p of s (its block table)."""
+    T, _, d_head = q.shape
+    scale = dtype(1.0 / np.sqrt(d_head))
+    grp = n_q // n_kv
+    o = np.zeros((T, n_q, d_head), dtype)
+    for s in range(len(plan.seq_pos0)):
+        K = gather_keys(k_pool, plan.block_table[s], plan.seq_kv_len[s], page).astype(dtype)
+        V = gather_keys(v_pool, plan.block_table[s], plan.seq_kv_len[s], page).astype(dtype)
+        for r in range(plan.seq_q_start[s], plan.seq_q_start[s + 1]):
+            n_keys = plan.row_pos[r] + 1
+            for g in range(n_kv):
+                qg = q[r, g * grp:(g + 1) * grp, :].astype(dtype)      # [grp, d]
+                sc = (qg @ K[:n_keys, g, :].T) * scale                  # [grp, n_keys]
+                sc = sc - sc.max(axis=1, keepdims=True)
+                w = np.exp(sc)
+                w = w / w.sum(axis=1, keepdims=True)
+                o[r, g * grp:(g + 1) * grp, :] = w @ V[:n_keys, g, :]
+    return o
+
+
+def layer_forward(w, dims, plan, x, k_pool, v_pool, cos, sin, dtype=np.float32,
+                  return_parts=False):
+    """One decoder layer over the packed rows of `plan`.  k_pool / v_pool are
+    updated in place with the rows' rotated K and raw V."""
+    T = len(plan.row_seq)
+    nq, nkv, dh = dims.n_q, dims.n_kv, dims.d_head
+    x = np.asarray(x, dtype)
+    xn = rmsnorm(x, w["g1"], dims.eps, dtype)
+    qkv = xn @ np.asarray(w["w_qkv"], dtype).T
+    q = qkv[:, :nq * dh].reshape(T, nq, dh)
+    k = qkv[:, nq * dh:(nq + nkv) * dh].reshape(T, nkv, dh)
+    v = qkv[:, (nq + nkv) * dh:].reshape(T, nkv, dh)
+    pos = np.asarray(plan.row_pos)
+    q = rope(q, pos, cos, sin, dtype)
+    k = rope(k, pos, cos, sin, dtype)
+    kv_append(k, v, plan.slot_mapping, k_pool, v_pool, dims.page)
+    o = attention(q, k_pool, v_pool, plan, nq, nkv, dims.page, dtype)
+    h = x + o.reshape(T, nq * dh) @ np.asarray(w["w_o"], dtype).T
+    hn = rmsnorm(h, w["g2"], dims.eps, dtype)
+    a = silu(hn @ np.asarray(w["w_g"], dtype).T) * (hn @ np.asarray(w["w_u"], dtype).T)
+    out = h + a @ np.asarray(w["w_d"], dtype).T
+    if return_parts:
+        return out, dict(xn=xn, qkv=qkv, q=q, k=k, v=v, o=o, h=h, hn=hn, a=a)
+    return out
+
+
+def lm_head(x_rows, g_f, w_lm, eps, dtype=np.float32):
+    """Final RMSNorm then the untied LM head -> logits [rows, vocab]."""
+    return rmsnorm(x_rows, g_f, eps, dtype) @ np.asarray(w_lm, dtype).T

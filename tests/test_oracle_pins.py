@@ -1,0 +1,555 @@
+"""Pins of the CPU oracle against facts the pages and the mathematics fix.
+
+Each pin is a function of the oracle module(s) so that the planted-mistake
+tests at the bottom can run it against a mutated oracle and check that it
+fails.  Nothing here touches the CUDA library.
+"""
+import json
+import math
+import os
+import types
+
+import numpy as np
+import pytest
+
+import oracle.costs as oc
+import oracle.layer as ol
+import oracle.plan as op
+import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------------------
+# helpers: tiny problems
+# ----------------------------------------------------------------------------
+def tiny_dims(**kw):
+    base = dict(d_model=32, n_q=4, n_kv=2, d_head=8, d_ff=48, theta=1e4)
+    base.update(kw)
+    return wl.Dims(**base)
+
+
+def tiny_state(rng, dims, dec_ctx, prefills, slack=64):
+    return wl.make_state(rng, dims, dec_ctx, prefills, slack_pages=slack)
+
+
+def plan_from_state(st, tau, chunk, page=16):
+    return op.plan_batch([r.done for r in st.decodes], [r.pages for r in st.decodes],
+                         [r.prompt_len for r in st.prefills], [r.done for r in st.prefills],
+                         [r.pages for r in st.prefills], st.free_pool, tau, chunk, page)
+
+
+# ----------------------------------------------------------------------------
+# planner
+# ----------------------------------------------------------------------------
+def pin_worked_example(plan_mod=op):
+    g = json.load(open(os.path.join(GOLDEN, "yi34b_worked_iteration.json")))
+    ctx = g["decode_ctx"]
+    pfs = g["prefills"]
+    dec_pages = [list(range(1000 * (i + 1), 1000 * (i + 1) + wl.pages_for(c))) for i, c in enumerate(ctx)]
+    pf_pages = [list(range(50000, 50000 + wl.pages_for(pfs[0]["done"]))), []]
+    pool = list(range(100000, 100400))
+    p = plan_mod.plan_batch(ctx, dec_pages, [r["prompt_len"] for r in pfs], [r["done"] for r in pfs],
+                            pf_pages, pool, g["tau"], g["chunk"])
+    e = g["expect"]
+    n_dec = sum(1 for k in p.seq_kind if k == 0)
+    assert n_dec == e["decode_tokens"]
+    assert g["tau"] - n_dec == e["prefill_budget"]
+    assert p.pf_take == e["take"]
+    assert e["prefill_budget"] - p.pf_take[0] == e["budget_after_R_A"]
+    assert p.n_rows == e["batch_tokens"]
+    assert g["tau"] - p.n_rows == e["budget_left"]
+    assert p.pf_finished == e["finished"]
+    rem = [r["prompt_len"] - r["done"] - t for r, t in zip(pfs, p.pf_take)]
+    assert rem == e["remaining_after"]
+    assert [p.seq_kv_len[s] for s in range(n_dec, p.n_seqs)] == e["kv_positions_attended_by_last_row"]
+
+
+def test_plan_worked_example():
+    pin_worked_example()
+
+
+def check_plan_invariants(p, dec_ctx, pf_len, pf_done, dec_pages0, pf_pages0, pool, tau, chunk, page=16):
+    b = len(dec_ctx)
+    # decodes first, one row each, at their context position
+    assert p.seq_kind[:b] == [0] * b
+    assert [p.row_pos[p.seq_q_start[s]] for s in range(b)] == list(dec_ctx)
+    # budget respected (decodes always admitted)
+    assert p.n_rows <= max(tau, b)
+    assert p.over_budget == (1 if b > tau else 0)
+    # FIFO prefix of prefills, one chunk each, chunk <= C, partial only when budget ends
+    takes = p.pf_take
+    seen_zero = False
+    for j, t in enumerate(takes):
+        full = min(chunk, pf_len[j] - pf_done[j])
+        assert 0 <= t <= full
+        if seen_zero:
+            assert t == 0
+        if t < full:
+            seen_zero = True
+            if t > 0 or full > 0:
+                assert p.n_rows == tau or b >= tau
+        assert p.pf_finished[j] == (1 if t > 0 and pf_done[j] + t == pf_len[j] else 0)
+    assert p.n_rows == b + sum(takes)
+    # rows of each sequence are consecutive positions starting at pos0
+    for s in range(p.n_seqs):
+        rows = range(p.seq_q_start[s], p.seq_q_start[s + 1])
+        assert [p.row_pos[r] for r in rows] == list(range(p.seq_pos0[s], p.seq_kv_len[s]))
+        assert all(p.row_seq[r] == s for r in rows)
+    # slots: page table lookup, unique
+    for r in range(p.n_rows):
+        s, pos = p.row_seq[r], p.row_pos[r]
+        assert p.slot_mapping[r] == p.block_table[s][pos // page] * page + pos % page
+    assert len(set(p.slot_mapping)) == p.n_rows
+    # pages popped from the front of the pool, in row order
+    new_pages = []
+    for s in range(p.n_seqs):
+        held = (dec_pages0 if p.seq_kind[s] == 0 else pf_pages0)[p.seq_req[s]]
+        for pg in p.block_table[s][len(held):]:
+            if pg >= 0:
+                new_pages.append(pg)
+    assert new_pages == list(pool[:p.pages_used])
+    assert p.free_pool == list(pool[p.pages_used:])
+
+
+def brute_force_takes(dec_n, pf_rem, tau, chunk):
+    """Enumerate every vector of takes (each 0..min(rem, C)) and keep the one
+    that the greedy rule of the pages selects: maximal lexicographically in
+    FIFO order subject to the budget (a request is only skipped when the
+    budget is gone)."""
+    import itertools
+    budget = tau - dec_n
+    best = None
+    for takes in itertools.product(*[range(min(r, chunk) + 1) for r in pf_rem]):
+        if sum(takes) > max(budget, 0):
+            continue
+        if best is None or list(takes) > list(best):
+            best = takes
+    return list(best)
+
+
+def test_plan_brute_force_tiny():
+    rng = np.random.default_rng(1)
+    for _ in range(300):
+        b = int(rng.integers(0, 5))
+        n_pf = int(rng.integers(0, 4))
+        tau = int(rng.integers(1, 40))
+        chunk = int(rng.integers(1, 20))
+        ctx = [int(v) for v in rng.integers(0, 50, b)]
+        pf_len = [int(v) for v in rng.integers(1, 30, n_pf)]
+        pf_done = [int(rng.integers(0, L)) for L in pf_len]
+        dec_pages = [list(range(100 * i, 100 * i + wl.pages_for(c))) for i, c in enumerate(ctx)]
+        pf_pages = [list(range(5000 + 100 * j, 5000 + 100 * j + wl.pages_for(d))) for j, d in enumerate(pf_done)]
+        pool = [int(v) for v in rng.permutation(np.arange(9000, 9100))]
+        p = op.plan_batch(ctx, dec_pages, pf_len, pf_done, pf_pages, pool, tau, chunk)
+        exp = brute_force_takes(b, [L - d for L, d in zip(pf_len, pf_done)], tau, chunk)
+        assert p.pf_take == exp, (b, tau, chunk, pf_len, pf_done)
+        check_plan_invariants(p, ctx, pf_len, pf_done, dec_pages, pf_pages, pool, tau, chunk)
+
+
+def test_plan_page_boundaries_and_out_of_pages():
+    # ctx = 15 (last slot of a page), 16 (needs a new page), 0 (fresh)
+    p = op.plan_batch([15, 16, 0], [[7], [8], []], [], [], [], [40, 41, 42], 8, 8)
+    assert p.slot_mapping == [7 * 16 + 15, 40 * 16 + 0, 41 * 16 + 0]
+    assert p.pages_used == 2 and p.free_pool == [42]
+    with pytest.raises(op.OutOfPages):
+        op.plan_batch([16, 32], [[1], [2, 3]], [], [], [], [9], 8, 8)
+
+
+def test_plan_configs_packing():
+    # every configuration reproduces b + c = tau with C = tau
+    for tau, b, L, off in [(512, 32, 4096, 1024), (2048, 64, 8192, 0), (1024, 128, 16384, 0)]:
+        ctx = [600] * b
+        dp = [list(range(100 * i, 100 * i + wl.pages_for(600))) for i in range(b)]
+        p = op.plan_batch(ctx, dp, [L], [off], [list(range(900000, 900000 + wl.pages_for(off)))],
+                          list(range(10**6, 10**6 + 4000)), tau, tau)
+        assert p.n_rows == tau and p.pf_take == [tau - b]
+        assert p.row_pos[b] == off and p.row_pos[-1] == off + tau - b - 1
+
+
+# ----------------------------------------------------------------------------
+# chunked attention pair counts (section 7.5b)
+# ----------------------------------------------------------------------------
+def pin_pair_identity(plan_mod=op, costs_mod=oc):
+    for L in [1, 2, 7, 64, 100, 513]:
+        for C in [1, 3, 16, 64, 512, L]:
+            done, rows, k = 0, [], 0
+            pages = []
+            pool = list(range(10**5))
+            while done < L:
+                p = plan_mod.plan_batch([], [], [L], [done], [pages], pool, C, C)
+                pages = p.pf_pages[0]
+                pool = p.free_pool
+                chunk_rows = p.row_pos
+                k += 1
+                if len(chunk_rows) == C:
+                    assert costs_mod.count_pairs(chunk_rows) == costs_mod.chunk_pairs_closed_form(k, C)
+                rows += chunk_rows
+                done += p.pf_take[0]
+            assert rows == list(range(L))
+            assert costs_mod.count_pairs(rows) == costs_mod.prompt_pairs_closed_form(L)
+            if L % C == 0:
+                K = L // C
+                assert 2 * sum(costs_mod.chunk_pairs_closed_form(i, C) for i in range(1, K + 1)) == L * L + L
+
+
+def test_pair_identity():
+    pin_pair_identity()
+
+
+def test_pair_identity_symbolic():
+    # the page's algebra: C^2 (K-1)K/2 + K C(C+1)/2 = L^2/2 + L/2 with L = KC
+    for K in range(1, 40):
+        for C in range(1, 40):
+            L = K * C
+            lhs = sum(oc.chunk_pairs_closed_form(k, C) for k in range(1, K + 1))
+            assert 2 * lhs == L * L + L
+
+
+# ----------------------------------------------------------------------------
+# arithmetic intensity I and c*
+# ----------------------------------------------------------------------------
+def pin_intensity(costs_mod=oc):
+    rng = np.random.default_rng(3)
+    dims = tiny_dims()
+    psi = dims.params_per_layer
+    for _ in range(20):
+        b = int(rng.integers(1, 6))
+        c = int(rng.integers(1, 40))
+        ctx = [int(v) for v in rng.integers(1, 90, b)]
+        dp = [list(range(100 * i, 100 * i + wl.pages_for(x))) for i, x in enumerate(ctx)]
+        p = op.plan_batch(ctx, dp, [500], [0], [[]], list(range(10**4, 10**4 + 100)), b + c, c)
+        flops, byts = costs_mod.count_iteration(p, psi, 2, 1, dims.n_kv, dims.d_head)
+        closed = costs_mod.intensity_closed_form(c, b, psi, 2, 1, dims.n_kv, dims.d_head, float(np.mean(ctx)))
+        assert math.isclose(flops / byts, closed, rel_tol=1e-12)
+        # c* brings I exactly to the target
+        i_star = closed * 1.7
+        cs = costs_mod.c_star(i_star, b, psi, 2, 1, dims.n_kv, dims.d_head, float(np.mean(ctx)))
+        i_at = costs_mod.intensity_closed_form(cs, b, psi, 2, 1, dims.n_kv, dims.d_head, float(np.mean(ctx)))
+        assert math.isclose(i_at, i_star, rel_tol=1e-12)
+    # pure decode (c = 0) has the lowest intensity; it rises monotonically with c
+    vals = [costs_mod.intensity_closed_form(c, 32, 218e6, 2, 1, 8, 128, 2300) for c in range(0, 2000, 100)]
+    assert all(a < b for a, b in zip(vals, vals[1:]))
+
+
+def test_intensity():
+    pin_intensity()
+
+
+# ----------------------------------------------------------------------------
+# RMSNorm, RoPE, SiLU
+# ----------------------------------------------------------------------------
+def pin_rmsnorm(layer=ol):
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((16, 64))
+    y = layer.rmsnorm(x, np.ones(64), 1e-6, np.float64)
+    # RMS(y) = sqrt(m / (m + eps)) with m = mean(x^2)
+    m = np.mean(x * x, axis=1)
+    assert np.allclose(np.sqrt(np.mean(y * y, axis=1)), np.sqrt(m / (m + 1e-6)), rtol=1e-12)
+    # mean square equal to eps -> RMS 1/sqrt(2)
+    z = np.full((1, 64), math.sqrt(1e-6))
+    assert np.allclose(np.sqrt(np.mean(layer.rmsnorm(z, np.ones(64), 1e-6, np.float64) ** 2)),
+                       1 / math.sqrt(2), rtol=1e-12)
+    # scale invariance (eps negligible at this scale), gain multiplies
+    g = rng.standard_normal(64)
+    assert np.allclose(layer.rmsnorm(1000 * x, g, 1e-6, np.float64), layer.rmsnorm(x, g, 0.0, np.float64),
+                       rtol=1e-9, atol=1e-12)
+
+
+def test_rmsnorm():
+    pin_rmsnorm()
+
+
+def pin_rope(layer=ol):
+    d = 16
+    cos, sin = layer.rope_tables(64, d, 1e4)
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((3, 2, d))
+    # position 0 is the identity
+    assert np.array_equal(layer.rope(x, np.zeros(3, int), cos, sin, np.float64), x)
+    # basis vector e_i at position p -> cos(p f_i) e_i + sin(p f_i) e_{i+d/2}
+    for i in range(d // 2):
+        for p in [1, 5, 63]:
+            e = np.zeros((1, 1, d))
+            e[0, 0, i] = 1
+            r = layer.rope(e, np.array([p]), cos, sin, np.float64)[0, 0]
+            ang = p * 1e4 ** (-2 * i / d)
+            assert abs(r[i] - math.cos(ang)) < 1e-6 and abs(r[i + d // 2] - math.sin(ang)) < 1e-6
+            assert np.count_nonzero(np.abs(r) > 1e-7) <= 2
+    # per-pair norm preservation
+    pos = np.array([3, 17, 40])
+    r = layer.rope(x, pos, cos, sin, np.float64)
+    h = d // 2
+    assert np.allclose(r[..., :h] ** 2 + r[..., h:] ** 2, x[..., :h] ** 2 + x[..., h:] ** 2, rtol=1e-6)
+    # relative position: <R_m q, R_n k> = <R_{m+t} q, R_{n+t} k>
+    q = rng.standard_normal((1, 1, d))
+    k = rng.standard_normal((1, 1, d))
+    dots = []
+    for t in [0, 7, 20]:
+        qm = layer.rope(q, np.array([10 + t]), cos, sin, np.float64)
+        kn = layer.rope(k, np.array([4 + t]), cos, sin, np.float64)
+        dots.append(float(np.sum(qm * kn)))
+    assert np.allclose(dots, dots[0], rtol=1e-5)
+
+
+def test_rope():
+    pin_rope()
+
+
+def test_rope_table_float64_source():
+    cos, sin = ol.rope_tables(4096, 128, 1e6)
+    assert cos.dtype == np.float32 and cos.shape == (4096, 64)
+    ang = 4095 * 1e6 ** (-2 * 3 / 128)
+    assert cos[4095, 3] == np.float32(math.cos(ang)) and sin[4095, 3] == np.float32(math.sin(ang))
+
+
+def test_silu():
+    from scipy.special import expit
+    x = np.linspace(-30, 30, 1001)
+    assert np.allclose(ol.silu(x), x * expit(x), rtol=1e-12, atol=1e-300)
+    assert ol.silu(np.array([0.0]))[0] == 0.0
+    assert abs(ol.silu(np.array([40.0]))[0] - 40.0) < 1e-12
+    assert abs(ol.silu(np.array([-40.0]))[0]) < 1e-15
+
+
+# ----------------------------------------------------------------------------
+# attention: brute-force dense masked softmax (float64)
+# ----------------------------------------------------------------------------
+def pin_attention_dense(layer=ol, plan_mod=op):
+    rng = np.random.default_rng(6)
+    for (n_q, n_kv, d) in [(4, 2, 8), (4, 4, 16), (8, 1, 8)]:
+        page = 16
+        # two decodes with contexts 5 and 37, one prompt with 21 cached + chunk of 19
+        seqs = {"d0": 5, "d1": 37, "p": 21}
+        kv = {s: (rng.standard_normal((n + 20, n_kv, d)), rng.standard_normal((n + 20, n_kv, d)))
+              for s, n in seqs.items()}
+        num_pages = 64
+        k_pool = np.zeros((num_pages, n_kv, page, d))
+        v_pool = np.zeros_like(k_pool)
+        perm = [int(v) for v in rng.permutation(num_pages)]
+        pages = {}
+        head = 0
+        for s, n in seqs.items():
+            m = wl.pages_for(n)
+            pages[s] = perm[head:head + m]
+            head += m
+            for t in range(n):
+                k_pool[pages[s][t // page], :, t % page] = kv[s][0][t]
+                v_pool[pages[s][t // page], :, t % page] = kv[s][1][t]
+        p = plan_mod.plan_batch([5, 37], [pages["d0"], pages["d1"]], [60], [21], [pages["p"]],
+                                perm[head:], 2 + 19, 19)
+        # write the new rows' K/V (positions ctx..) where the plan put them
+        names = ["d0", "d1", "p"]
+        for r in range(p.n_rows):
+            s = names[p.row_seq[r]]
+            pos = p.row_pos[r]
+            sl = p.slot_mapping[r]
+            k_pool[sl // page, :, sl % page] = kv[s][0][pos]
+            v_pool[sl // page, :, sl % page] = kv[s][1][pos]
+        q = rng.standard_normal((p.n_rows, n_q, d))
+        got = layer.attention(q, k_pool, v_pool, p, n_q, n_kv, page, np.float64)
+        # dense reference: full score matrix per sequence with an explicit mask
+        for si, s in enumerate(names):
+            rows = list(range(p.seq_q_start[si], p.seq_q_start[si + 1]))
+            nk = p.seq_kv_len[si]
+            Kd, Vd = kv[s][0][:nk], kv[s][1][:nk]
+            for h in range(n_q):
+                g = h // (n_q // n_kv)
+                S = q[rows, h, :] @ Kd[:, g, :].T / math.sqrt(d)
+                mask = np.array([[j <= p.row_pos[r] for j in range(nk)] for r in rows])
+                S = np.where(mask, S, -np.inf)
+                P = np.exp(S - S.max(axis=1, keepdims=True))
+                P /= P.sum(axis=1, keepdims=True)
+                exp = P @ Vd[:, g, :]
+                assert np.allclose(got[rows, h, :], exp, rtol=1e-10, atol=1e-12), (n_q, n_kv, s, h)
+
+
+def test_attention_dense():
+    pin_attention_dense()
+
+
+def test_attention_special_cases():
+    # one key -> the output is that key's V; identical keys -> mean of V
+    p = op.plan_batch([0], [[]], [], [], [], [3], 1, 1)
+    k_pool = np.zeros((4, 1, 16, 8))
+    v_pool = np.zeros_like(k_pool)
+    v_pool[3, 0, 0] = np.arange(8)
+    o = ol.attention(np.ones((1, 2, 8)), k_pool, v_pool, p, 2, 1, 16, np.float64)
+    assert np.array_equal(o[0, 0], np.arange(8)) and np.array_equal(o[0, 1], np.arange(8))
+    p = op.plan_batch([9], [[2]], [], [], [], [], 1, 1)
+    k_pool[2, 0, :10] = 1.0
+    v_pool[2, 0, :10] = np.arange(10)[:, None] * np.ones(8)
+    o = ol.attention(np.ones((1, 1, 8)), k_pool, v_pool, p, 1, 1, 16, np.float64)
+    assert np.allclose(o[0, 0], 4.5)
+
+
+# ----------------------------------------------------------------------------
+# layer: chunked == unchunked, decode batch independence, zero projections
+# ----------------------------------------------------------------------------
+def run_prompt_chunked(layer, dims, w, x_prompt, C, dtype, pool_pages=64, seed=0):
+    L = x_prompt.shape[0]
+    cos, sin = layer.rope_tables(L + 1, dims.d_head, dims.theta)
+    shape = (pool_pages, dims.n_kv, dims.page, dims.d_head)
+    k_pool, v_pool = np.zeros(shape, dtype), np.zeros(shape, dtype)
+    pool = [int(v) for v in np.random.default_rng(seed).permutation(pool_pages)]
+    done, pages, outs = 0, [], []
+    while done < L:
+        p = op.plan_batch([], [], [L], [done], [pages], pool, C, C, dims.page)
+        pages, pool = p.pf_pages[0], p.free_pool
+        xr = x_prompt[np.asarray(p.row_pos)]
+        outs.append(layer.layer_forward(w, dims, p, xr, k_pool, v_pool, cos, sin, dtype))
+        done += p.pf_take[0]
+    return np.concatenate(outs), k_pool, v_pool
+
+
+def pin_chunked_equals_unchunked(layer=ol, dtype=np.float32, tol=1e-5):
+    rng = np.random.default_rng(7)
+    dims = tiny_dims(d_model=64, d_ff=96)
+    w = wl.layer_weights(rng, dims, gamma_jitter=0.1)
+    L = 48
+    x = wl.bf16_round(rng.standard_normal((L, dims.d_model), dtype=np.float32))
+    ref, k_ref, v_ref = run_prompt_chunked(layer, dims, w, x, L, dtype)
+    for C in [1, 7, 16, 48]:
+        out, k, v = run_prompt_chunked(layer, dims, w, x, C, dtype)
+        assert np.max(np.abs(out - ref)) <= tol, C
+        assert np.max(np.abs(k - k_ref)) <= tol and np.max(np.abs(v - v_ref)) <= tol, C
+
+
+def test_chunked_equals_unchunked_fp32():
+    pin_chunked_equals_unchunked(dtype=np.float32, tol=1e-5)
+
+
+def test_chunked_equals_unchunked_fp64():
+    pin_chunked_equals_unchunked(dtype=np.float64, tol=1e-12)
+
+
+def pin_decode_independence(layer=ol, dtype=np.float64, tol=1e-12):
+    rng = np.random.default_rng(8)
+    dims = tiny_dims()
+    w = wl.layer_weights(rng, dims, gamma_jitter=0.1)
+    st = tiny_state(rng, dims, [3, 16, 40, 70], [(60, 20)])
+    cos, sin = layer.rope_tables(128, dims.d_head, dims.theta)
+    xdec = rng.standard_normal((4, dims.d_model)).astype(np.float32)
+    xch = rng.standard_normal((40, dims.d_model)).astype(np.float32)
+
+    def run(order, with_chunk):
+        dec = [st.decodes[i] for i in order]
+        pfs = st.prefills if with_chunk else []
+        p = op.plan_batch([r.done for r in dec], [r.pages for r in dec], [r.prompt_len for r in pfs],
+                          [r.done for r in pfs], [r.pages for r in pfs], st.free_pool, 64, 64)
+        x = np.concatenate([xdec[order], xch[:p.n_rows - len(order)]])
+        k, v = st.k_pool.astype(dtype), st.v_pool.astype(dtype)
+        out = layer.layer_forward(w, dims, p, x, k, v, cos, sin, dtype)
+        return {i: out[j] for j, i in enumerate(order)}
+
+    base = run([0, 1, 2, 3], True)
+    for order, ch in [([2], False), ([3, 2, 1, 0], True), ([2, 0], False), ([1, 2], True)]:
+        got = run(order, ch)
+        for i in order:
+            assert np.max(np.abs(got[i] - base[i])) <= tol, (order, ch, i)
+
+
+def test_decode_independence():
+    pin_decode_independence()
+
+
+def test_zero_projections_identity():
+    rng = np.random.default_rng(9)
+    dims = tiny_dims()
+    w = wl.layer_weights(rng, dims)
+    w["w_o"] = np.zeros_like(w["w_o"])
+    w["w_d"] = np.zeros_like(w["w_d"])
+    st = tiny_state(rng, dims, [5, 9], [(30, 0)])
+    p = plan_from_state(st, 20, 20)
+    cos, sin = ol.rope_tables(64, dims.d_head, dims.theta)
+    x = rng.standard_normal((p.n_rows, dims.d_model)).astype(np.float32)
+    out = ol.layer_forward(w, dims, p, x, st.k_pool, st.v_pool, cos, sin)
+    assert np.array_equal(out, x)
+
+
+# ----------------------------------------------------------------------------
+# planted mistakes: each pin must fail on a plausible wrong oracle
+# ----------------------------------------------------------------------------
+_ORIG_ATTENTION = ol.attention
+_ORIG_ROPE = ol.rope
+
+
+def _attention_variant(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype, kv_head, n_keys):
+    """The oracle's attention loop with the head map and key count as parameters."""
+    T, _, d_head = q.shape
+    o = np.zeros((T, n_q, d_head), dtype)
+    for s in range(len(plan.seq_pos0)):
+        K = ol.gather_keys(k_pool, plan.block_table[s], plan.seq_kv_len[s], page).astype(dtype)
+        V = ol.gather_keys(v_pool, plan.block_table[s], plan.seq_kv_len[s], page).astype(dtype)
+        for r in range(plan.seq_q_start[s], plan.seq_q_start[s + 1]):
+            nk = n_keys(plan, s, r)
+            for h in range(n_q):
+                g = kv_head(h, n_q, n_kv)
+                sc = K[:nk, g, :] @ q[r, h, :] / np.sqrt(d_head)
+                w = np.exp(sc - sc.max())
+                o[r, h, :] = (w / w.sum()) @ V[:nk, g, :]
+    return o
+
+
+def _attn_gqa_modulo(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype=np.float32):
+    return _attention_variant(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype,
+                              lambda h, nq, nkv: h % nkv, lambda p, s, r: p.row_pos[r] + 1)
+
+
+def _attn_excludes_self(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype=np.float32):
+    return _attention_variant(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype,
+                              lambda h, nq, nkv: h // (nq // nkv), lambda p, s, r: max(p.row_pos[r], 1))
+
+
+def _attn_noncausal_chunk(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype=np.float32):
+    return _attention_variant(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype,
+                              lambda h, nq, nkv: h // (nq // nkv), lambda p, s, r: p.seq_kv_len[s])
+
+
+def _rope_wrong_sign(x, pos, cos, sin, dtype=np.float32):
+    return _ORIG_ROPE(x, pos, cos, -np.asarray(sin), dtype)
+
+
+def _rms_eps_outside(x, g, eps, dtype=np.float32):
+    x = np.asarray(x, dtype)
+    return x / (np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + eps) * np.asarray(g, dtype)
+
+
+@pytest.mark.parametrize("pin,name,mutant", [
+    (pin_attention_dense, "attention", _attn_gqa_modulo),
+    (pin_attention_dense, "attention", _attn_excludes_self),
+    (pin_attention_dense, "attention", _attn_noncausal_chunk),
+    (pin_chunked_equals_unchunked, "attention", _attn_noncausal_chunk),
+    (pin_rope, "rope", _rope_wrong_sign),
+    (pin_rmsnorm, "rmsnorm", _rms_eps_outside),
+])
+def test_planted_mistakes_fail(monkeypatch, pin, name, mutant):
+    monkeypatch.setattr(ol, name, mutant)
+    with pytest.raises(AssertionError):
+        pin()
+
+
+def test_planted_planner_mistake_fails():
+    # the pseudo-code read literally keeps peeking the head request, taking a
+    # second chunk of R_A instead of moving on to R_B
+    m = types.ModuleType("mutant_plan")
+
+    def literal_peek(dec_ctx, dec_pages, pf_len, pf_done, pf_pages, free_pool, tau, chunk, page=16,
+                     max_pages=None):
+        return op.plan_batch(dec_ctx, dec_pages, pf_len, pf_done, pf_pages, free_pool, tau, tau, page,
+                             max_pages)
+
+    m.plan_batch = literal_peek
+    with pytest.raises(AssertionError):
+        pin_worked_example(plan_mod=m)
+
+
+def test_planted_residual_mistake_fails(monkeypatch):
+    orig = ol.layer_forward
+
+    def no_residual(w, dims, plan, x, k_pool, v_pool, cos, sin, dtype=np.float32, return_parts=False):
+        return orig(w, dims, plan, x, k_pool, v_pool, cos, sin, dtype) - 0.5 * np.asarray(x, dtype)
+
+    monkeypatch.setattr(ol, "layer_forward", no_residual)
+    with pytest.raises(AssertionError):
+        test_zero_projections_identity()
