@@ -1,0 +1,408 @@
+// Packed-token projections on the 5th-generation tensor cores:
+//   C = epilogue(A B^T),  A [M][K] bf16 (activations), B [N][K] bf16 (weights).
+//
+// These are the linear layers whose cost model the pages use (Sarathi-Serve
+// reading notes, section 1.6: T = max(T_math, T_mem) with
+// T_math = 2 n d_in d_out / FLOPS and T_mem = (d_in d_out bytes_w + ...) / BW).
+//
+// Design (sm_103a):
+//   * persistent grid (<= one CTA per SM), 128 x BN output tiles walked with
+//     the M index fastest, so the CTAs that share a weight tile run together
+//     and the weights stream from HBM once;
+//   * warp 0: TMA producer.  128-byte swizzled 128x64 (A) and BNx64 (B) boxes
+//     into a STAGES-deep shared-memory ring, completion via mbarrier tx bytes;
+//   * warp 1: one elected thread issues tcgen05.mma (kind::f16, M=128,
+//     N=BN, K=16) into a TMEM accumulator; tcgen05.commit frees a ring slot
+//     and, after the last K block, signals the epilogue;
+//   * warps 2-5: epilogue.  tcgen05.ld 32x32b (warp w reads TMEM lanes
+//     32*(w%4)..), fused STORE / RESIDUAL / SWIGLU / F32 epilogue, then the
+//     accumulator buffer is handed back.  Two accumulator buffers let the
+//     epilogue of one tile overlap the main loop of the next.
+//   * every wait is bounded (device.cuh); on expiry the kernel unwinds.
+#include <cuda_bf16.h>
+
+#include "device.cuh"
+#include "runtime.h"
+
+namespace hb {
+namespace {
+
+using namespace dev;
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+
+template <int BN>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = BN == 256 ? 4 : (BN == 192 ? 5 : 6);
+  static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+};
+
+struct Params {
+  int M, N, K;
+  void* C;
+  const void* R;
+  int ldc;
+  int* status;
+};
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+
+template <int EPI>
+__device__ __forceinline__ void store_chunk(const Params& p, int row, int col, const uint32_t (&r)[32]) {
+  if (EPI == HB_EPI_F32) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.C) + static_cast<size_t>(row) * p.ldc + col);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]), __uint_as_float(r[4 * i + 2]),
+                           __uint_as_float(r[4 * i + 3]));
+    return;
+  }
+  uint32_t w[16];
+  if (EPI == HB_EPI_RESIDUAL) {
+    const uint4* res =
+        reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.R) + static_cast<size_t>(row) * p.ldc + col);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint4 rv = res[i];
+      uint32_t rr[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float2 f = unpack_bf16x2(rr[j]);
+        const int e = 8 * i + 2 * j;
+        w[4 * i + j] = pack_bf16x2(f.x + __uint_as_float(r[e]), f.y + __uint_as_float(r[e + 1]));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+  }
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) + static_cast<size_t>(row) * p.ldc + col);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m_tiles = (p.M + BM - 1) / BM;
+  const int n_tiles = (p.N + BN - 1) / BN;
+  const int tiles = m_tiles * n_tiles;
+  const int kblocks = p.K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      uint32_t pending = 0;  // stages armed and not yet seen consumed (bit mask)
+      uint32_t armed_parity = 0;
+      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+        const int m0 = (tile % m_tiles) * BM;
+        const int n0 = (tile / m_tiles) * BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * C::STAGE_BYTES;
+          pending |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
+          tma_load_2d(sa + C::A_BYTES, &tmB, &full[stage], kb * BK, n0);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // let copies already in flight land before the CTA exits; a stage
+        // whose empty wait succeeded later was consumed, so only the last
+        // STAGES arms can be outstanding
+        for (int s = 0; s < C::STAGES; ++s)
+          if (pending & (1u << s)) mbar_drain(&full[s], (armed_parity >> s) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int t = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++t) {
+        const int acc = t & 1;
+        const uint32_t acc_phase = (t >> 1) & 1;
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + C::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            mma_bf16(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), kIdesc,
+                     (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) mma_commit(&acc_full[acc]);
+      }
+      if (!ok) {
+        // make sure no MMA is still reading shared memory or writing TMEM
+        mma_commit(drain);
+        mbar_drain(drain, 0);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    int t = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++t) {
+      const int acc = t & 1;
+      const uint32_t acc_phase = (t >> 1) & 1;
+      bool ok = mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const int m0 = (tile % m_tiles) * BM;
+      const int n_blk = tile / m_tiles;
+      const int row = m0 + quarter * 32 + lane;
+      const bool row_ok = row < p.M;
+      const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+      if (EPI == HB_EPI_SWIGLU) {
+#pragma unroll 1
+        for (int j = 0; j < BN / 128; ++j) {
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            uint32_t g[32], u[32];
+            tmem_ld_32x32b_x32(t_base + j * 128 + h * 32, g);
+            tmem_ld_32x32b_x32(t_base + j * 128 + 64 + h * 32, u);
+            tmem_ld_wait();
+            const int col = n_blk * (BN / 2) + j * 64 + h * 32;
+            if (row_ok && col < p.ldc) {
+              uint32_t w[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float a0 = silu(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+                const float a1 = silu(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+                w[i] = pack_bf16x2(a0, a1);
+              }
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) +
+                                                    static_cast<size_t>(row) * p.ldc + col);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_base + c * 32, r);
+          tmem_ld_wait();
+          const int col = n_blk * BN + c * 32;
+          if (row_ok && col < p.N) store_chunk<EPI>(p, row, col, r);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int BN, int EPI>
+hb_status launch(const DeviceCtx& ctx, const void* A, const void* B, void* Cp, const void* R, int M, int N, int K,
+                 cudaStream_t stream) {
+  using C = Cfg<BN>;
+  CUtensorMap tmA, tmB;
+  hb_status st = encode_tmap_2d(&tmA, A, K, M, static_cast<uint64_t>(K) * 2, BK, BM, true);
+  if (st != HB_OK) return st;
+  st = encode_tmap_2d(&tmB, B, K, N, static_cast<uint64_t>(K) * 2, BK, BN, true);
+  if (st != HB_OK) return st;
+  static bool attr_set[64] = {};
+  if (!attr_set[ctx.device]) {
+    st = cuda_status(cudaFuncSetAttribute(gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM),
+                     "cudaFuncSetAttribute(gemm)");
+    if (st != HB_OK) return st;
+    attr_set[ctx.device] = true;
+  }
+  Params p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.C = Cp;
+  p.R = R;
+  p.ldc = EPI == HB_EPI_SWIGLU ? N / 2 : N;
+  p.status = ctx.status;
+  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
+  gemm_kernel<BN, EPI><<<grid, kThreads, C::SMEM, stream>>>(tmA, tmB, p);
+  return launch_status("gemm_kernel launch");
+}
+
+// Tile width: fewest waves of tiles over the SMs, weighted by a per-tile
+// cost that grows with BN (plus a fixed per-tile overhead).
+int choose_bn(int M, int N, int epi, int num_sms) {
+  const int cands_swiglu[2] = {256, 128};
+  const int cands[3] = {256, 192, 128};
+  const int* c = epi == HB_EPI_SWIGLU ? cands_swiglu : cands;
+  const int nc = epi == HB_EPI_SWIGLU ? 2 : 3;
+  const int m_tiles = (M + BM - 1) / BM;
+  int best = 128;
+  double best_cost = 1e30;
+  for (int i = 0; i < nc; ++i) {
+    const int bn = c[i];
+    if (N % bn != 0 && !(epi != HB_EPI_SWIGLU && bn == 128)) continue;
+    const int tiles = m_tiles * ((N + bn - 1) / bn);
+    const int waves = (tiles + num_sms - 1) / num_sms;
+    const double cost = waves * (bn + 32.0);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+}  // namespace
+
+hb_status gemm_launch(const DeviceCtx& ctx, const void* A, const void* B, void* C, const void* R, int M, int N, int K,
+                      int epi, cudaStream_t stream) {
+  const int bn = choose_bn(M, N, epi, ctx.num_sms);
+#define HB_GEMM_CASE(BN_, EPI_) \
+  if (bn == BN_ && epi == EPI_) return launch<BN_, EPI_>(ctx, A, B, C, R, M, N, K, stream);
+  HB_GEMM_CASE(256, HB_EPI_STORE)
+  HB_GEMM_CASE(192, HB_EPI_STORE)
+  HB_GEMM_CASE(128, HB_EPI_STORE)
+  HB_GEMM_CASE(256, HB_EPI_RESIDUAL)
+  HB_GEMM_CASE(192, HB_EPI_RESIDUAL)
+  HB_GEMM_CASE(128, HB_EPI_RESIDUAL)
+  HB_GEMM_CASE(256, HB_EPI_SWIGLU)
+  HB_GEMM_CASE(128, HB_EPI_SWIGLU)
+  HB_GEMM_CASE(256, HB_EPI_F32)
+  HB_GEMM_CASE(192, HB_EPI_F32)
+  HB_GEMM_CASE(128, HB_EPI_F32)
+#undef HB_GEMM_CASE
+  set_error("hb_gemm: no kernel for BN=%d epilogue=%d", bn, epi);
+  return HB_ERR_UNSUPPORTED;
+}
+
+hb_status gemm_check(const void* A, const void* B, void* C, const void* R, int M, int N, int K, int epi) {
+  HB_REQUIRE(A && B && C, "hb_gemm: null operand");
+  HB_REQUIRE(M >= 1 && N >= 64 && K >= 64, "hb_gemm: bad shape M=%d N=%d K=%d", M, N, K);
+  HB_REQUIRE(K % 64 == 0 && N % 64 == 0, "hb_gemm: K and N must be multiples of 64 (K=%d N=%d)", K, N);
+  HB_REQUIRE(epi >= HB_EPI_STORE && epi <= HB_EPI_F32, "hb_gemm: unknown epilogue %d", epi);
+  HB_REQUIRE(epi != HB_EPI_SWIGLU || N % 128 == 0, "hb_gemm: SWIGLU needs N %% 128 == 0");
+  HB_REQUIRE(epi != HB_EPI_RESIDUAL || R != nullptr, "hb_gemm: RESIDUAL needs R");
+  HB_REQUIRE(aligned16(A) && aligned16(B) && aligned16(C) && (R == nullptr || aligned16(R)),
+             "hb_gemm: operands must be 16-byte aligned");
+  return HB_OK;
+}
+
+// ---------------------------------------------------------------- weight prep
+__global__ void interleave_gate_up_kernel(const uint4* __restrict__ wg, const uint4* __restrict__ wu,
+                                          uint4* __restrict__ out, int F, int d8) {
+  const size_t total = static_cast<size_t>(2 * F) * d8;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int row = static_cast<int>(i / d8);
+    const int c = static_cast<int>(i % d8);
+    const int blk = row / 128, e = row % 128;
+    const int src = blk * 64 + (e & 63);
+    out[i] = (e < 64 ? wg : wu)[static_cast<size_t>(src) * d8 + c];
+  }
+}
+
+}  // namespace hb
+
+extern "C" hb_status hb_gemm(const void* A, const void* B, void* C, const void* R, int32_t M, int32_t N, int32_t K,
+                             int32_t epilogue, void* stream) {
+  hb::clear_error();
+  hb_status st = hb::gemm_check(A, B, C, R, M, N, K, epilogue);
+  if (st != HB_OK) return st;
+  hb::DeviceCtx ctx;
+  st = hb::device_context(&ctx);
+  if (st != HB_OK) return st;
+  return hb::gemm_launch(ctx, A, B, C, R, M, N, K, epilogue, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" hb_status hb_interleave_gate_up(const void* w_gate, const void* w_up, void* w_gu, int32_t F, int32_t d,
+                                           void* stream) {
+  hb::clear_error();
+  HB_REQUIRE(w_gate && w_up && w_gu, "hb_interleave_gate_up: null pointer");
+  HB_REQUIRE(F > 0 && F % 64 == 0 && d > 0 && d % 8 == 0, "hb_interleave_gate_up: F %% 64 and d %% 8 required");
+  HB_REQUIRE(hb::aligned16(w_gate) && hb::aligned16(w_up) && hb::aligned16(w_gu),
+             "hb_interleave_gate_up: pointers must be 16-byte aligned");
+  hb::DeviceCtx ctx;
+  hb_status st = hb::device_context(&ctx);
+  if (st != HB_OK) return st;
+  hb::interleave_gate_up_kernel<<<ctx.num_sms * 8, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(w_gate), static_cast<const uint4*>(w_up), static_cast<uint4*>(w_gu), F, d / 8);
+  return hb::launch_status("interleave_gate_up_kernel launch");
+}

@@ -1,0 +1,133 @@
+// One decoder layer over a packed hybrid batch, and the final norm + LM head.
+//
+// The forward of a hybrid iteration ("run_iteration(B)" of the scheduling
+// loop, Sarathi-Serve reading notes section 3.4) for one pre-norm layer:
+//   rmsnorm1 -> qkv projection -> RoPE + paged KV append -> hybrid attention
+//   -> o projection + residual -> rmsnorm2 -> gate/up projection + SwiGLU
+//   -> down projection + residual.
+// Every stage is one kernel launch on the caller's stream; the workspace is
+// carved into 256-byte aligned regions.
+#include <cuda_runtime.h>
+
+#include "runtime.h"
+
+namespace hb {
+namespace {
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct LayerWs {
+  size_t xn, qkv, q, o, h, a, attn, total;
+};
+
+LayerWs layer_ws(const hb_layer_dims& dm, int T, int S, int max_kv_len) {
+  LayerWs w;
+  const size_t t = static_cast<size_t>(T);
+  size_t off = 0;
+  w.xn = off;   off += align256(t * dm.d_model * 2);
+  w.qkv = off;  off += align256(t * (dm.n_q + 2 * dm.n_kv) * dm.d_head * 2);
+  w.q = off;    off += align256(t * dm.n_q * dm.d_head * 2);
+  w.o = off;    off += align256(t * dm.n_q * dm.d_head * 2);
+  w.h = off;    off += align256(t * dm.d_model * 2);
+  w.a = off;    off += align256(t * dm.d_ff * 2);
+  w.attn = off; off += align256(attention_workspace_bytes(dm, S, max_kv_len));
+  w.total = off;
+  return w;
+}
+
+}  // namespace
+}  // namespace hb
+
+extern "C" size_t hb_layer_workspace_bytes(const hb_layer_dims* dims, int32_t max_rows, int32_t max_seqs,
+                                           int32_t max_kv_len) {
+  if (!dims || max_rows < 0 || max_seqs < 0 || max_kv_len < 0) return 0;
+  return hb::layer_ws(*dims, max_rows, max_seqs, max_kv_len).total;
+}
+
+extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_dims* dims, const hb_device_plan* plan,
+                                      const void* rope, int32_t max_pos, const void* x_in, void* x_out, void* k_cache,
+                                      void* v_cache, int32_t num_pages, int32_t max_kv_len, void* workspace,
+                                      size_t ws_bytes, void* stream, const hb_profile* prof) {
+  using namespace hb;
+  clear_error();
+  hb_status st = check_dims(dims);
+  if (st != HB_OK) return st;
+  HB_REQUIRE(w && plan, "hb_layer_forward: null weights or plan");
+  HB_REQUIRE(w->w_qkv && w->w_o && w->w_gu && w->w_d && w->g1 && w->g2, "hb_layer_forward: null weight");
+  HB_REQUIRE(x_in && x_out && k_cache && v_cache && rope, "hb_layer_forward: null pointer");
+  HB_REQUIRE(plan->n_rows >= 0 && plan->n_seqs >= 0, "hb_layer_forward: bad plan sizes");
+  HB_REQUIRE(plan->n_rows == 0 || (plan->row_pos && plan->slot_mapping && plan->seq_q_start && plan->seq_kv_len &&
+                                   plan->block_table),
+             "hb_layer_forward: null plan array");
+  HB_REQUIRE(num_pages > 0 && max_pos > 0 && max_kv_len > 0, "hb_layer_forward: bad sizes");
+  HB_REQUIRE(prof == nullptr || (prof->events && prof->n_events >= HB_LAYER_STAGES + 1),
+             "hb_layer_forward: profile needs %d events", HB_LAYER_STAGES + 1);
+  HB_REQUIRE(aligned16(x_in) && aligned16(x_out) && aligned16(rope), "hb_layer_forward: 16-byte alignment");
+  const int T = plan->n_rows;
+  if (T == 0) return HB_OK;
+  const hb_layer_dims& dm = *dims;
+  const LayerWs lw = layer_ws(dm, T, plan->n_seqs, max_kv_len);
+  HB_REQUIRE(workspace && ws_bytes >= lw.total, "hb_layer_forward: workspace of %zu bytes needed, %zu given",
+             lw.total, ws_bytes);
+  HB_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, "hb_layer_forward: workspace 256-byte alignment");
+  DeviceCtx ctx;
+  st = device_context(&ctx);
+  if (st != HB_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* xn = ws + lw.xn;
+  void* qkv = ws + lw.qkv;
+  void* q = ws + lw.q;
+  void* o = ws + lw.o;
+  void* h = ws + lw.h;
+  void* a = ws + lw.a;
+  void* aws = ws + lw.attn;
+  const int d = dm.d_model, hd = dm.n_q * dm.d_head, qkv_cols = (dm.n_q + 2 * dm.n_kv) * dm.d_head;
+
+  auto mark = [&](int k) -> hb_status {
+    if (!prof) return HB_OK;
+    return cuda_status(cudaEventRecord(static_cast<cudaEvent_t>(prof->events[k]), s), "cudaEventRecord");
+  };
+#define HB_STEP(k, call)         \
+  do {                           \
+    st = mark(k);                \
+    if (st != HB_OK) return st;  \
+    st = (call);                 \
+    if (st != HB_OK) return st;  \
+  } while (0)
+
+  HB_STEP(0, rmsnorm_launch(ctx, x_in, nullptr, w->g1, xn, T, d, dm.rms_eps, T, s));
+  HB_STEP(1, gemm_launch(ctx, xn, w->w_qkv, qkv, nullptr, T, qkv_cols, d, HB_EPI_STORE, s));
+  HB_STEP(2, kv_append_launch(ctx, qkv, T, plan->row_pos, plan->slot_mapping, rope, max_pos, dm, q, k_cache, v_cache,
+                              num_pages, s));
+  HB_STEP(3, attention_launch(ctx, q, k_cache, v_cache, num_pages, *plan, dm, max_kv_len, o, aws,
+                              lw.total - lw.attn, s));
+  HB_STEP(4, gemm_launch(ctx, o, w->w_o, h, x_in, T, d, hd, HB_EPI_RESIDUAL, s));
+  HB_STEP(5, rmsnorm_launch(ctx, h, nullptr, w->g2, xn, T, d, dm.rms_eps, T, s));
+  HB_STEP(6, gemm_launch(ctx, xn, w->w_gu, a, nullptr, T, 2 * dm.d_ff, d, HB_EPI_SWIGLU, s));
+  HB_STEP(7, gemm_launch(ctx, a, w->w_d, x_out, h, T, d, dm.d_ff, HB_EPI_RESIDUAL, s));
+#undef HB_STEP
+  return mark(HB_LAYER_STAGES);
+}
+
+extern "C" hb_status hb_final_logits(const void* x, int32_t T, const int32_t* rows, int32_t n_sel, const void* g_f,
+                                     const void* w_lm, int32_t vocab, int32_t d, float eps, void* logits,
+                                     void* workspace, size_t ws_bytes, void* stream) {
+  using namespace hb;
+  clear_error();
+  HB_REQUIRE(x && rows && g_f && w_lm && logits && workspace, "hb_final_logits: null pointer");
+  HB_REQUIRE(T >= 0 && n_sel >= 0 && vocab > 0 && vocab % 64 == 0 && d > 0 && d % 64 == 0,
+             "hb_final_logits: vocab and d must be multiples of 64");
+  HB_REQUIRE(ws_bytes >= static_cast<size_t>(n_sel) * d * 2, "hb_final_logits: workspace too small");
+  HB_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, "hb_final_logits: workspace 256-byte alignment");
+  if (n_sel == 0) return HB_OK;
+  hb_status st = gemm_check(workspace, w_lm, logits, nullptr, n_sel, vocab, d, HB_EPI_F32);
+  if (st != HB_OK) return st;
+  DeviceCtx ctx;
+  st = device_context(&ctx);
+  if (st != HB_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = rmsnorm_launch(ctx, x, rows, g_f, workspace, n_sel, d, eps, T, s);
+  if (st != HB_OK) return st;
+  return gemm_launch(ctx, workspace, w_lm, logits, nullptr, n_sel, vocab, d, HB_EPI_F32, s);
+}

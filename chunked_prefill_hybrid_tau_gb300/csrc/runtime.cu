@@ -1,0 +1,141 @@
+// Host runtime pieces: device status word, device properties, TMA tensor-map
+// encoding through the driver entry point (no link-time libcuda dependency,
+// so the library also loads on machines without a GPU driver).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "runtime.h"
+
+// Device status word: 0 = ok, else the first error a kernel recorded.
+__device__ int g_hb_status_word;
+
+namespace hb {
+
+namespace {
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices];
+int g_num_sms[kMaxDevices];
+int g_cc[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+}  // namespace
+
+hb_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return HB_OK;
+  set_error("%s: %s", what, cudaGetErrorString(e));
+  return HB_ERR_CUDA;
+}
+
+static hb_status init_device(int dev) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_status_ptr[dev] != nullptr) return HB_OK;
+  void* p = nullptr;
+  hb_status st = cuda_status(cudaGetSymbolAddress(&p, g_hb_status_word), "cudaGetSymbolAddress(status word)");
+  if (st != HB_OK) return st;
+  cudaDeviceProp prop;
+  st = cuda_status(cudaGetDeviceProperties(&prop, dev), "cudaGetDeviceProperties");
+  if (st != HB_OK) return st;
+  g_num_sms[dev] = prop.multiProcessorCount;
+  g_cc[dev] = prop.major * 10 + prop.minor;
+  g_status_ptr[dev] = static_cast<int*>(p);
+  return HB_OK;
+}
+
+hb_status device_context(DeviceCtx* ctx) {
+  int dev = 0;
+  hb_status st = cuda_status(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != HB_OK) return st;
+  if (dev < 0 || dev >= kMaxDevices) {
+    set_error("device ordinal %d out of range", dev);
+    return HB_ERR_UNSUPPORTED;
+  }
+  if (g_status_ptr[dev] == nullptr) {
+    st = init_device(dev);
+    if (st != HB_OK) return st;
+  }
+  if (g_cc[dev] != 103) {
+    set_error("the library is built for sm_103a; device %d is sm_%d", dev, g_cc[dev]);
+    return HB_ERR_UNSUPPORTED;
+  }
+  ctx->device = dev;
+  ctx->num_sms = g_num_sms[dev];
+  ctx->status = g_status_ptr[dev];
+  return HB_OK;
+}
+
+hb_status encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
+  if (g_encode == nullptr) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      hb_status st = cuda_status(
+          cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q),
+          "cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)");
+      if (st != HB_OK) return st;
+      if (q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        set_error("cuTensorMapEncodeTiled is not available from the driver");
+        return HB_ERR_UNSUPPORTED;
+      }
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (%d): dims %llu x %llu, box %u x %u", static_cast<int>(r),
+              static_cast<unsigned long long>(inner), static_cast<unsigned long long>(outer), box_inner, box_outer);
+    return HB_ERR_INVALID_ARG;
+  }
+  return HB_OK;
+}
+
+hb_status launch_status(const char* what) { return cuda_status(cudaGetLastError(), what); }
+
+}  // namespace hb
+
+extern "C" hb_status hb_check_status(void* stream) {
+  hb::clear_error();
+  hb::DeviceCtx ctx;
+  hb_status st = hb::device_context(&ctx);
+  if (st != HB_OK) return st;
+  st = hb::cuda_status(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "cudaStreamSynchronize");
+  if (st != HB_OK) return st;
+  int word = 0;
+  st = hb::cuda_status(cudaMemcpy(&word, ctx.status, sizeof(int), cudaMemcpyDeviceToHost), "read status word");
+  if (st != HB_OK) return st;
+  if (word == 0) return HB_OK;
+  const int zero = 0;
+  st = hb::cuda_status(cudaMemcpy(ctx.status, &zero, sizeof(int), cudaMemcpyHostToDevice), "clear status word");
+  if (st != HB_OK) return st;
+  if (word == hb::kDevTimeout) {
+    hb::set_error("a bounded device-side wait expired");
+    return HB_ERR_TIMEOUT;
+  }
+  hb::set_error("a device-side index check failed (code %d)", word);
+  return HB_ERR_DEVICE;
+}
+
+extern "C" hb_status hb_device_info(int32_t* num_sms, int32_t* is_sm103) {
+  hb::clear_error();
+  HB_REQUIRE(num_sms && is_sm103, "hb_device_info: null output");
+  int dev = 0;
+  hb_status st = hb::cuda_status(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != HB_OK) return st;
+  cudaDeviceProp prop;
+  st = hb::cuda_status(cudaGetDeviceProperties(&prop, dev), "cudaGetDeviceProperties");
+  if (st != HB_OK) return st;
+  *num_sms = prop.multiProcessorCount;
+  *is_sm103 = (prop.major == 10 && prop.minor == 3) ? 1 : 0;
+  return HB_OK;
+}

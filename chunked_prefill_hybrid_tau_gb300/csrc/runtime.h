@@ -1,0 +1,46 @@
+// Host-side runtime helpers shared by the CUDA translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.h"
+
+namespace hb {
+
+struct DeviceCtx {
+  int device;
+  int num_sms;
+  int* status;  // device address of the status word of this device
+};
+
+// Current device, checked to be sm_103; status-word address cached per device.
+hb_status device_context(DeviceCtx* ctx);
+
+hb_status cuda_status(cudaError_t e, const char* what);
+hb_status launch_status(const char* what);
+
+// 2D bf16 tensor map: `outer` rows of `inner` elements, rows `row_stride_bytes`
+// apart; box of box_inner x box_outer elements.
+hb_status encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks shared by the layer entry points.
+hb_status check_dims(const hb_layer_dims* dims);
+
+// Launchers (arguments already checked; asynchronous on `stream`).
+hb_status rmsnorm_launch(const DeviceCtx& ctx, const void* x, const int* rows, const void* gamma, void* y,
+                         int n_rows, int d, float eps, int n_src, cudaStream_t stream);
+hb_status kv_append_launch(const DeviceCtx& ctx, const void* qkv, int T, const int* row_pos, const int* slots,
+                           const void* rope, int max_pos, const hb_layer_dims& dims, void* q_out, void* k_cache,
+                           void* v_cache, int num_pages, cudaStream_t stream);
+hb_status gemm_check(const void* A, const void* B, void* C, const void* R, int M, int N, int K, int epi);
+hb_status gemm_launch(const DeviceCtx& ctx, const void* A, const void* B, void* C, const void* R, int M, int N, int K,
+                      int epi, cudaStream_t stream);
+size_t attention_workspace_bytes(const hb_layer_dims& dims, int max_seqs, int max_kv_len);
+hb_status attention_launch(const DeviceCtx& ctx, const void* q, const void* k_cache, const void* v_cache,
+                           int num_pages, const hb_device_plan& plan, const hb_layer_dims& dims, int max_kv_len,
+                           void* out, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+}  // namespace hb

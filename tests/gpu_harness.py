@@ -1,0 +1,75 @@
+"""Shared helpers of the GPU parity tests: tolerance checks and layer runs
+through the C ABI with the oracle beside them."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle.layer as ol
+import oracle.plan as op
+import workloads as wl
+from workloads import device as wd
+
+# Tolerance for bf16 activations and outputs: |gpu - ref| <= ATOL + RTOL*|ref|
+# elementwise (a bf16 value of magnitude >= 4 is itself rounded by up to
+# 2^-7 * |v| / 2, so a purely absolute 2e-2 bound cannot hold for it), and a
+# relative L2 error <= 1e-2 over the tensor.
+ATOL = 2e-2
+RTOL = 2e-2
+REL_L2 = 1e-2
+
+
+def assert_close(gpu, ref, what, atol=ATOL, rtol=RTOL, rel_l2=REL_L2):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert gpu.shape == ref.shape, (what, gpu.shape, ref.shape)
+    assert np.all(np.isfinite(gpu)), f"{what}: non-finite GPU values"
+    err = np.abs(gpu - ref)
+    bound = atol + rtol * np.abs(ref)
+    worst = int(np.argmax(err - bound))
+    assert np.all(err <= bound), (f"{what}: max excess at {np.unravel_index(worst, err.shape)}: "
+                                  f"gpu {gpu.flat[worst]} ref {ref.flat[worst]} (max abs err {err.max():.4g})")
+    denom = np.linalg.norm(ref)
+    if denom > 0:
+        rl2 = np.linalg.norm(gpu - ref) / denom
+        assert rl2 <= rel_l2, f"{what}: relative L2 {rl2:.4g} > {rel_l2}"
+    return float(err.max())
+
+
+def plan_both(st: wl.State, tau: int, chunk: int, max_pages=None):
+    """The C++ plan (through the ABI) and the oracle plan of the same state."""
+    import chunked_prefill_hybrid_tau_gb300 as hb
+    args = ([r.done for r in st.decodes], [r.pages for r in st.decodes], [r.prompt_len for r in st.prefills],
+            [r.done for r in st.prefills], [r.pages for r in st.prefills], st.free_pool, tau, chunk, st.dims.page)
+    hp = hb.hb_plan_batch(*args, max_pages=max_pages)
+    o = op.plan_batch(*args, max_pages=hp.max_pages)
+    assert list(hp.slot_mapping) == o.slot_mapping and hp.block_table.tolist() == o.block_table
+    return hp, o
+
+
+class GpuLayer:
+    """One layer's weights, caches and RoPE table on the device."""
+
+    def __init__(self, w: dict, dims, k_pool: np.ndarray, v_pool: np.ndarray, max_pos: int, device="cuda"):
+        self.dims = dims
+        self.w = wd.layer_weights_device(w, dims, device)
+        self.k = wd.bf16_tensor(k_pool, device)
+        self.v = wd.bf16_tensor(v_pool, device)
+        self.max_pos = max_pos
+        self.rope = wd.rope_table_device(max_pos, dims, device)
+        self.device = device
+
+    def forward(self, hp, x: np.ndarray, max_kv_len: int):
+        import torch
+        import chunked_prefill_hybrid_tau_gb300 as hb
+        dp = hb.DevicePlan(hp, self.device)
+        xin = wd.bf16_tensor(x, self.device)
+        xout = torch.empty_like(xin)
+        ws = wd.workspace(hb.hb_layer_workspace_bytes(self.dims, hp.n_rows, hp.n_seqs, max_kv_len), self.device)
+        hb.hb_layer_forward(self.w, self.dims, dp, self.rope, self.max_pos, xin, xout, self.k, self.v, max_kv_len, ws)
+        hb.hb_check_status()
+        return wd.to_numpy(xout)
+
+
+def oracle_layer(w, dims, plan, x, k_pool, v_pool, max_pos):
+    cos, sin = ol.rope_tables(max_pos, dims.d_head, dims.theta)
+    return ol.layer_forward(w, dims, plan, x, k_pool, v_pool, cos, sin)
