@@ -1,0 +1,485 @@
+#!/usr/bin/env python3
+"""Hybrid-iteration benchmark: tokens/s, ms/iter and roofline fraction.
+
+One step = one pass of the whole hot path over the Mistral-7B-shaped layer
+at tau = 512 (one 480-token chunk at offset 1024 of a 4096-token prompt + 32
+decodes with contexts uniform in [512, 4096]): the C planner packs the batch
+and maps slots, the plan is copied to the device (one pinned copy), and
+hb_layer_forward runs RMSNorm, the QKV projection, RoPE + paged KV append,
+the hybrid attention, the O projection + residual, RMSNorm, gate/up + SwiGLU
+and the down projection + residual.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) each rank runs an independent replica on its own GPU
+(the iteration has no exchange step); value = all ranks' tokens / max time.
+--impl reference times the CPU oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes as C
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "hybrid-iteration tokens/s and ms/iter vs token budget; % of per-iteration roofline"
+WORKLOAD = "mistral7b_layer_tau512"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="hb", choices=["hb", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tau", type=int, default=512)
+    ap.add_argument("--decodes", type=int, default=32)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- workload
+def make_workload(tau: int, n_dec: int):
+    import workloads as wl
+    if tau == 512 and n_dec == 32:
+        return wl.mistral_layer(seed=0)
+    return wl.mistral_layer(seed=0, tau=tau, n_dec=n_dec, ctx_lo=512, ctx_hi=8192, prompt_len=8192, offset=0)
+
+
+class PlanRunner:
+    """Per-step planning through the C ABI into pinned staging buffers and one
+    host-to-device copy of the kernel-facing plan arrays."""
+
+    def __init__(self, lib, st, tau, chunk, device):
+        import torch
+        from chunked_prefill_hybrid_tau_gb300 import _lib as L
+        self.lib, self.L, self.tau, self.chunk = lib, L, tau, chunk
+        self.n_dec, self.n_pf = len(st.decodes), len(st.prefills)
+        self.page_bufs = []
+        self.dec = (L.hb_request * max(self.n_dec, 1))()
+        self.pf = (L.hb_request * max(self.n_pf, 1))()
+        grow = tau // 16 + 2
+        self.n_pages0 = []
+        for arr, reqs in ((self.dec, st.decodes), (self.pf, st.prefills)):
+            for i, r in enumerate(reqs):
+                b = np.zeros(len(r.pages) + grow, np.int32)
+                b[:len(r.pages)] = r.pages
+                self.page_bufs.append(b)
+                arr[i] = L.hb_request(r.prompt_len, r.done, len(r.pages), b.size, b.ctypes.data_as(L.p_i32))
+                self.n_pages0.append(len(r.pages))
+        self.pool_arr = np.asarray(st.free_pool, np.int32)
+        self.row_cap = max(tau, self.n_dec)
+        self.seq_cap = self.n_dec + self.n_pf
+        spans = [r.done + 1 for r in st.decodes] + [r.done + min(chunk, tau) for r in st.prefills]
+        self.max_pages = max((s + 15) // 16 for s in spans)
+        rc, sc, mp = self.row_cap, self.seq_cap, self.max_pages
+        self.off = np.cumsum([0, rc, rc, sc + 1, sc, sc * mp])  # row_pos, slots, q_start, kv_len, table
+        self.dev_ints = int(self.off[-1])
+        self.host_only = {k: np.zeros(n, np.int32) for k, n in
+                          (("row_seq", rc), ("seq_pos0", sc), ("seq_kind", sc), ("seq_req", sc),
+                           ("pf_take", max(self.n_pf, 1)), ("pf_finished", max(self.n_pf, 1)))}
+        self.pinned = [torch.zeros(self.dev_ints, dtype=torch.int32).pin_memory() for _ in range(2)]
+        self.copied = [torch.cuda.Event(), torch.cuda.Event()]
+        self.dev = torch.zeros(self.dev_ints, dtype=torch.int32, device=device)
+        self.k = 0
+        self.h2d_bytes = 0
+
+    def step(self, stream):
+        """Plan the iteration on the host and enqueue its upload on `stream`.
+        Returns the hb_device_plan struct."""
+        L = self.L
+        b = self.k & 1
+        self.copied[b].synchronize()  # the copy that last read this staging buffer is done
+        stage = self.pinned[b].numpy()
+        for i in range(self.n_dec):
+            self.dec[i].n_pages = self.n_pages0[i]
+        for j in range(self.n_pf):
+            self.pf[j].n_pages = self.n_pages0[self.n_dec + j]
+        P = L.hb_plan()
+        P.row_cap, P.seq_cap, P.max_pages, P.pf_cap = self.row_cap, self.seq_cap, self.max_pages, self.n_pf
+        base = stage.ctypes.data
+
+        def at(i):
+            return C.cast(base + 4 * int(self.off[i]), L.p_i32)
+
+        P.row_pos, P.slot_mapping, P.seq_q_start, P.seq_kv_len, P.block_table = at(0), at(1), at(2), at(3), at(4)
+        for k, a in self.host_only.items():
+            setattr(P, k, a.ctypes.data_as(L.p_i32))
+        pool = L.hb_page_pool(self.pool_arr.ctypes.data_as(L.p_i32), int(self.pool_arr.size), 0)
+        st = self.lib.hb_plan_batch(self.dec, self.n_dec, self.pf, self.n_pf, C.byref(pool), self.tau, self.chunk, 16,
+                                    C.byref(P))
+        if st != 0:
+            raise RuntimeError(f"hb_plan_batch failed: {self.lib.hb_last_error().decode()}")
+        import torch
+        with torch.cuda.stream(stream):
+            self.dev.copy_(self.pinned[b], non_blocking=True)
+            self.copied[b].record(stream)
+        self.h2d_bytes = self.dev_ints * 4
+        self.k += 1
+        self.n_rows, self.n_seqs = P.n_rows, P.n_seqs
+        d = self.dev.data_ptr()
+        return L.hb_device_plan(P.n_rows, P.n_seqs, self.max_pages, *[d + 4 * int(self.off[i]) for i in range(5)])
+
+    def host_plan_arrays(self):
+        s = self.pinned[(self.k - 1) & 1].numpy()
+        T, S = self.n_rows, self.n_seqs
+        return (s[self.off[0]:self.off[0] + T].copy(), s[self.off[2]:self.off[2] + S + 1].copy(),
+                s[self.off[3]:self.off[3] + S].copy())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={self.QUERY}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_iteration_rate(w, budget_s: float, min_iters: int = 1):
+    """Time the oracle's full layer iteration on the same workload until
+    `budget_s` seconds (at least `min_iters` iterations)."""
+    import oracle.layer as ol
+    import oracle.plan as op
+    st = w.state
+    args = ([r.done for r in st.decodes], [r.pages for r in st.decodes], [r.prompt_len for r in st.prefills],
+            [r.done for r in st.prefills], [r.pages for r in st.prefills], st.free_pool, w.tau, w.chunk)
+    max_pos = max(r.done for r in st.decodes + st.prefills) + w.tau + 1
+    cos, sin = ol.rope_tables(max_pos, w.dims.d_head, w.dims.theta)
+    k, v = st.k_pool, st.v_pool  # the append writes the same slots each iteration
+    n, rows = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        p = op.plan_batch(*args)
+        ol.layer_forward(w.weights[0], w.dims, p, w.x, k, v, cos, sin)
+        n += 1
+        rows += p.n_rows
+        if n >= min_iters and time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return rows / dt, n, dt
+
+
+def oracle_decode_sample_rate(w, n_rows: int):
+    """Oracle on a sub-batch of the workload's first n_rows decodes."""
+    import oracle.layer as ol
+    import oracle.plan as op
+    st = w.state
+    dec = st.decodes[:n_rows]
+    p = op.plan_batch([r.done for r in dec], [r.pages for r in dec], [], [], [], st.free_pool, w.tau, w.chunk)
+    max_pos = max(r.done for r in dec) + 2
+    cos, sin = ol.rope_tables(max_pos, w.dims.d_head, w.dims.theta)
+    t0 = time.perf_counter()
+    ol.layer_forward(w.weights[0], w.dims, p, w.x[:p.n_rows], st.k_pool, st.v_pool, cos, sin)
+    return p.n_rows, time.perf_counter() - t0
+
+
+def cores():
+    return len(os.sched_getaffinity(0))
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    w = make_workload(args.tau, args.decodes)
+    n_steps = args.steps + args.warmup
+    budget = max(0.05, 150.0 / n_steps)  # whole run within a few minutes
+    rows_cal, t_cal = oracle_decode_sample_rate(w, 4)
+    per_row = t_cal / rows_cal
+    T = args.tau
+    full = per_row * T <= budget
+    n_rows = T if full else max(1, min(len(w.state.decodes), int(budget / per_row)))
+    import oracle.layer as ol
+    import oracle.plan as op
+    st = w.state
+    if full:
+        args_p = ([r.done for r in st.decodes], [r.pages for r in st.decodes], [r.prompt_len for r in st.prefills],
+                  [r.done for r in st.prefills], [r.pages for r in st.prefills], st.free_pool, w.tau, w.chunk)
+        sample = f"full iteration of {T} rows per step"
+    else:
+        dec = st.decodes[:n_rows]
+        args_p = ([r.done for r in dec], [r.pages for r in dec], [], [], [], st.free_pool, w.tau, w.chunk)
+        sample = f"{n_rows} decode rows of the iteration per step (full context each)"
+    max_pos = max(r.done for r in st.decodes + st.prefills) + w.tau + 1
+    cos, sin = ol.rope_tables(max_pos, w.dims.d_head, w.dims.theta)
+
+    def step():
+        p = op.plan_batch(*args_p)
+        ol.layer_forward(w.weights[0], w.dims, p, w.x[:p.n_rows], st.k_pool, st.v_pool, cos, sin)
+        return p.n_rows
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    rows = sum(step() for _ in range(args.steps))
+    dt = time.perf_counter() - t0
+    value = rows / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tau": w.tau, "rows_per_step": n_rows},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_hb(args, world, rank, local):
+    import torch
+    import chunked_prefill_hybrid_tau_gb300 as hb
+    from chunked_prefill_hybrid_tau_gb300 import costs
+    from workloads import device as wd
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = hb.lib()
+    w = make_workload(args.tau, args.decodes)
+    st, dims = w.state, w.dims
+    max_pos = max(r.done for r in st.decodes + st.prefills) + w.tau + 1
+    gw = wd.layer_weights_device(w.weights[0], dims, dev)
+    kc, vc = wd.bf16_tensor(st.k_pool, dev), wd.bf16_tensor(st.v_pool, dev)
+    rope = wd.rope_table_device(max_pos, dims, dev)
+    x_dev = wd.bf16_tensor(w.x, dev)
+    out_dev = torch.empty_like(x_dev)
+    stream = torch.cuda.Stream(device=dev)
+    runner = PlanRunner(lib, st, w.tau, w.chunk, dev)
+    max_kv = max_pos
+    ws = wd.workspace(hb.hb_layer_workspace_bytes(dims, runner.row_cap, runner.seq_cap, max_kv), dev)
+    ds = hb.dims_struct(dims)
+    wstruct = gw.struct()
+    n_events = 9
+    prof_steps = min(args.steps, 200)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_events)] for _ in range(prof_steps)]
+    for row in ev:  # torch creates the CUDA event on first record
+        for e in row:
+            e.record(stream)
+    stream.synchronize()
+    ev_arrays = [(C.c_void_p * n_events)(*[e.cuda_event for e in row]) for row in ev]
+    from chunked_prefill_hybrid_tau_gb300 import _lib as L
+    profs = [L.hb_profile(a, n_events) for a in ev_arrays]
+    sptr = C.c_void_p(stream.cuda_stream)
+
+    def layer(dplan, xin, xout, prof=None):
+        rc = lib.hb_layer_forward(C.byref(wstruct), C.byref(ds), C.byref(dplan), C.c_void_p(rope.data_ptr()),
+                                  max_pos, C.c_void_p(xin.data_ptr()), C.c_void_p(xout.data_ptr()),
+                                  C.c_void_p(kc.data_ptr()), C.c_void_p(vc.data_ptr()), int(kc.shape[0]), max_kv,
+                                  C.c_void_p(ws.data_ptr()), ws.numel(), sptr, C.byref(prof) if prof else None)
+        if rc != 0:
+            raise RuntimeError(f"hb_layer_forward: {lib.hb_last_error().decode()}")
+
+    # ---- device-resident timing ------------------------------------------
+    for _ in range(args.warmup):
+        layer(runner.step(stream), x_dev, out_dev)
+    stream.synchronize()
+    hb.hb_check_status(stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for k in range(args.steps):
+        j = k - (args.steps - prof_steps)
+        layer(runner.step(stream), x_dev, out_dev, profs[j] if j >= 0 else None)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    hb.hb_check_status(stream)
+    t_dev = max_over_ranks(start.elapsed_time(end) / 1e3, world)
+    T = runner.n_rows
+    value = world * T * args.steps / t_dev
+
+    stage_ms = np.zeros(8)
+    for row in ev:
+        for s in range(8):
+            stage_ms[s] += row[s].elapsed_time(row[s + 1])
+    stage_ms /= len(ev)
+
+    # ---- end to end through the C ABI with host buffers ------------------
+    x_host = torch.from_numpy(wd.to_numpy(x_dev).astype(np.float32)).to(torch.bfloat16).pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    x_in2 = torch.empty_like(x_dev)
+    e_steps = max(1, min(args.steps, 1000))
+    for _ in range(min(args.warmup, 5)):
+        with torch.cuda.stream(stream):
+            x_in2.copy_(x_host, non_blocking=True)
+        layer(runner.step(stream), x_in2, out_dev)
+        with torch.cuda.stream(stream):
+            out_host.copy_(out_dev, non_blocking=True)
+    stream.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        with torch.cuda.stream(stream):
+            x_in2.copy_(x_host, non_blocking=True)
+        layer(runner.step(stream), x_in2, out_dev)
+        with torch.cuda.stream(stream):
+            out_host.copy_(out_dev, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    hb.hb_check_status(stream)
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    e2e = {"value": world * T * e_steps / t_e2e, "unit": "tokens/s",
+           "h2d_bytes_per_step": int(x_host.numel() * 2 + runner.h2d_bytes),
+           "d2h_bytes_per_step": int(out_host.numel() * 2)}
+
+    # ---- roofline --------------------------------------------------------
+    peaks = load_peaks()
+    row_pos, q_start, kv_len = runner.host_plan_arrays()
+    sc = costs.stage_costs(dims, row_pos, q_start, kv_len)
+    flops, byts = costs.iteration_totals(sc)
+    t_step = t_dev / args.steps
+    t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
+    dom = int(np.argmax(stage_ms))
+    name = costs.STAGES[dom]
+    f_dom, b_dom, bound = sc[name]
+    dur = stage_ms[dom] / 1e3
+    if bound == "tensor":
+        achieved, peak, unit = f_dom / dur / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = b_dom / dur / 1e9, peaks["hbm_gbs"], "GB/s"
+    traffic = None
+    prof_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof_path):
+        tr = json.load(open(prof_path))
+        if tr.get("workload") == WORKLOAD and name in tr.get("kernels", {}):
+            traffic = tr["kernels"][name]
+
+    n_dec = sum(1 for r in st.decodes)
+    c = T - n_dec
+    s_bar = float(np.mean([r.done for r in st.decodes])) if n_dec else 0.0
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * t_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tau": w.tau, "chunk_tokens": c, "decodes": n_dec, "rows": T,
+                   "d_model": dims.d_model, "heads": f"{dims.n_q}q/{dims.n_kv}kv", "d_head": dims.d_head,
+                   "d_ff": dims.d_ff, "page": 16, "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (436 MB weights + 308 MB KV per step), no flush"},
+        "roofline": {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peaks["source"] + " burst",
+                     "launch_ms": stage_ms[dom]},
+        "iteration_roofline": {"flops": flops, "bytes": byts, "t_roof_ms": 1e3 * t_roof,
+                               "frac": t_roof / t_step, "intensity_flop_per_byte": flops / byts,
+                               "intensity_page": costs.page_intensity(c, n_dec, dims.params_per_layer, 2, 1,
+                                                                      dims.n_kv, dims.d_head, s_bar)},
+        "stages_ms": {k: round(float(v), 5) for k, v in zip(costs.STAGES, stage_ms)},
+        "e2e": e2e,
+        "gpu_launches": 8 * args.steps,
+        "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, n, dt = oracle_iteration_rate(w, budget_s=10.0)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+                                "sample": f"{n} full oracle iterations ({n * T} rows) in {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        rc = run_reference(args, world, rank)
+    else:
+        rc = run_hb(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -266,6 +266,9 @@ def hb_layer_forward(w: LayerWeights, dims, dplan: DevicePlan, rope, max_pos, x_
     ps = dplan.struct()
     prof = None
     if events is not None:
+        for e in events:  # torch creates the CUDA event lazily, on first record
+            if e.cuda_event == 0:
+                e.record()
         arr = (C.c_void_p * len(events))(*[e.cuda_event for e in events])
         prof = L.hb_profile(arr, len(events))
     _check(lib().hb_layer_forward(C.byref(ws), C.byref(ds), C.byref(ps), _p(rope), int(max_pos), _p(x_in), _p(x_out),

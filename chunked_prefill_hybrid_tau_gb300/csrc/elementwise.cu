@@ -172,7 +172,7 @@ hb_status check_dims(const hb_layer_dims* dm) {
   HB_REQUIRE(dm->n_q > 0 && dm->n_kv > 0 && dm->n_q % dm->n_kv == 0, "n_q must be a multiple of n_kv");
   HB_REQUIRE(dm->n_q / dm->n_kv <= 16, "at most 16 query heads per kv head");
   HB_REQUIRE(dm->d_head == 64 || dm->d_head == 128, "d_head must be 64 or 128");
-  HB_REQUIRE(dm->d_ff > 0 && dm->d_ff % 64 == 0, "d_ff must be a positive multiple of 64");
+  HB_REQUIRE(dm->d_ff > 0 && dm->d_ff % 8 == 0, "d_ff must be a positive multiple of 8");
   HB_REQUIRE(dm->page_size == 16, "page_size must be 16");
   HB_REQUIRE(dm->rms_eps >= 0.f, "rms_eps must be >= 0");
   return HB_OK;

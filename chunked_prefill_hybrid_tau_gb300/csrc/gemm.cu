@@ -50,33 +50,38 @@ struct Params {
   int M, N, K;
   void* C;
   const void* R;
-  int ldc;
+  int ldc;       // row stride of C and R (elements)
+  int out_cols;  // valid output columns (N, or N/2 for SWIGLU)
   int* status;
 };
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
 
+// Store 32 accumulator columns [col, col+32) of one row, 16-byte segments
+// past the last valid column skipped.
 template <int EPI>
 __device__ __forceinline__ void store_chunk(const Params& p, int row, int col, const uint32_t (&r)[32]) {
+  const int ncols = p.out_cols;
   if (EPI == HB_EPI_F32) {
     float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.C) + static_cast<size_t>(row) * p.ldc + col);
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]), __uint_as_float(r[4 * i + 2]),
-                           __uint_as_float(r[4 * i + 3]));
+      if (col + 4 * i < ncols)
+        dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                             __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
     return;
   }
   uint32_t w[16];
   if (EPI == HB_EPI_RESIDUAL) {
-    const uint4* res =
-        reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.R) + static_cast<size_t>(row) * p.ldc + col);
+    const uint4* res = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.R) +
+                                                      static_cast<size_t>(row) * p.ldc + col);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      uint4 rv = res[i];
-      uint32_t rr[4] = {rv.x, rv.y, rv.z, rv.w};
+      const uint4 rv = col + 8 * i < ncols ? res[i] : make_uint4(0, 0, 0, 0);
+      const uint32_t rr[4] = {rv.x, rv.y, rv.z, rv.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        float2 f = unpack_bf16x2(rr[j]);
+        const float2 f = unpack_bf16x2(rr[j]);
         const int e = 8 * i + 2 * j;
         w[4 * i + j] = pack_bf16x2(f.x + __uint_as_float(r[e]), f.y + __uint_as_float(r[e + 1]));
       }
@@ -87,7 +92,8 @@ __device__ __forceinline__ void store_chunk(const Params& p, int row, int col, c
   }
   uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) + static_cast<size_t>(row) * p.ldc + col);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  for (int i = 0; i < 4; ++i)
+    if (col + 8 * i < ncols) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
 }
 
 template <int BN, int EPI>
@@ -109,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int m_tiles = (p.M + BM - 1) / BM;
   const int n_tiles = (p.N + BN - 1) / BN;
   const int tiles = m_tiles * n_tiles;
-  const int kblocks = p.K / BK;
+  const int kblocks = (p.K + BK - 1) / BK;  // TMA zero-fills columns past K
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -237,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_32x32b_x32(t_base + j * 128 + 64 + h * 32, u);
             tmem_ld_wait();
             const int col = n_blk * (BN / 2) + j * 64 + h * 32;
-            if (row_ok && col < p.ldc) {
+            if (row_ok && col < p.out_cols) {
               uint32_t w[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
@@ -248,7 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) +
                                                     static_cast<size_t>(row) * p.ldc + col);
 #pragma unroll
-              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+              for (int i = 0; i < 4; ++i)
+                if (col + 8 * i < p.out_cols) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
             }
           }
         }
@@ -259,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_32x32b_x32(t_base + c * 32, r);
           tmem_ld_wait();
           const int col = n_blk * BN + c * 32;
-          if (row_ok && col < p.N) store_chunk<EPI>(p, row, col, r);
+          if (row_ok && col < p.out_cols) store_chunk<EPI>(p, row, col, r);
         }
       }
       tc_fence_before();
@@ -277,11 +284,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int BN, int EPI>
-hb_status launch(const DeviceCtx& ctx, const void* A, const void* B, void* Cp, const void* R, int M, int N, int K,
-                 cudaStream_t stream) {
+hb_status launch(const DeviceCtx& ctx, const void* A, int lda, const void* B, void* Cp, int ldc, const void* R, int M,
+                 int N, int K, cudaStream_t stream) {
   using C = Cfg<BN>;
   CUtensorMap tmA, tmB;
-  hb_status st = encode_tmap_2d(&tmA, A, K, M, static_cast<uint64_t>(K) * 2, BK, BM, true);
+  hb_status st = encode_tmap_2d(&tmA, A, K, M, static_cast<uint64_t>(lda) * 2, BK, BM, true);
   if (st != HB_OK) return st;
   st = encode_tmap_2d(&tmB, B, K, N, static_cast<uint64_t>(K) * 2, BK, BN, true);
   if (st != HB_OK) return st;
@@ -298,7 +305,8 @@ hb_status launch(const DeviceCtx& ctx, const void* A, const void* B, void* Cp, c
   p.K = K;
   p.C = Cp;
   p.R = R;
-  p.ldc = EPI == HB_EPI_SWIGLU ? N / 2 : N;
+  p.ldc = ldc;
+  p.out_cols = EPI == HB_EPI_SWIGLU ? N / 2 : N;
   p.status = ctx.status;
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
@@ -318,7 +326,7 @@ int choose_bn(int M, int N, int epi, int num_sms) {
   double best_cost = 1e30;
   for (int i = 0; i < nc; ++i) {
     const int bn = c[i];
-    if (N % bn != 0 && !(epi != HB_EPI_SWIGLU && bn == 128)) continue;
+    if (epi == HB_EPI_SWIGLU ? N % bn != 0 : (N % bn != 0 && bn != 128)) continue;
     const int tiles = m_tiles * ((N + bn - 1) / bn);
     const int waves = (tiles + num_sms - 1) / num_sms;
     const double cost = waves * (bn + 32.0);
@@ -332,11 +340,11 @@ int choose_bn(int M, int N, int epi, int num_sms) {
 
 }  // namespace
 
-hb_status gemm_launch(const DeviceCtx& ctx, const void* A, const void* B, void* C, const void* R, int M, int N, int K,
-                      int epi, cudaStream_t stream) {
+hb_status gemm_launch(const DeviceCtx& ctx, const void* A, int lda, const void* B, void* C, int ldc, const void* R,
+                      int M, int N, int K, int epi, cudaStream_t stream) {
   const int bn = choose_bn(M, N, epi, ctx.num_sms);
 #define HB_GEMM_CASE(BN_, EPI_) \
-  if (bn == BN_ && epi == EPI_) return launch<BN_, EPI_>(ctx, A, B, C, R, M, N, K, stream);
+  if (bn == BN_ && epi == EPI_) return launch<BN_, EPI_>(ctx, A, lda, B, C, ldc, R, M, N, K, stream);
   HB_GEMM_CASE(256, HB_EPI_STORE)
   HB_GEMM_CASE(192, HB_EPI_STORE)
   HB_GEMM_CASE(128, HB_EPI_STORE)
@@ -355,8 +363,8 @@ hb_status gemm_launch(const DeviceCtx& ctx, const void* A, const void* B, void* 
 
 hb_status gemm_check(const void* A, const void* B, void* C, const void* R, int M, int N, int K, int epi) {
   HB_REQUIRE(A && B && C, "hb_gemm: null operand");
-  HB_REQUIRE(M >= 1 && N >= 64 && K >= 64, "hb_gemm: bad shape M=%d N=%d K=%d", M, N, K);
-  HB_REQUIRE(K % 64 == 0 && N % 64 == 0, "hb_gemm: K and N must be multiples of 64 (K=%d N=%d)", K, N);
+  HB_REQUIRE(M >= 1 && N >= 8 && K >= 8, "hb_gemm: bad shape M=%d N=%d K=%d", M, N, K);
+  HB_REQUIRE(K % 8 == 0 && N % 8 == 0, "hb_gemm: K and N must be multiples of 8 (K=%d N=%d)", K, N);
   HB_REQUIRE(epi >= HB_EPI_STORE && epi <= HB_EPI_F32, "hb_gemm: unknown epilogue %d", epi);
   HB_REQUIRE(epi != HB_EPI_SWIGLU || N % 128 == 0, "hb_gemm: SWIGLU needs N %% 128 == 0");
   HB_REQUIRE(epi != HB_EPI_RESIDUAL || R != nullptr, "hb_gemm: RESIDUAL needs R");
@@ -366,16 +374,18 @@ hb_status gemm_check(const void* A, const void* B, void* C, const void* R, int M
 }
 
 // ---------------------------------------------------------------- weight prep
+// w_gu row 128*b + e holds gate row 64*b + e (e < 64) or up row 64*b + e - 64;
+// rows past F (when F % 64 != 0) are zero.
 __global__ void interleave_gate_up_kernel(const uint4* __restrict__ wg, const uint4* __restrict__ wu,
-                                          uint4* __restrict__ out, int F, int d8) {
-  const size_t total = static_cast<size_t>(2 * F) * d8;
+                                          uint4* __restrict__ out, int F, int F_pad, int d8) {
+  const size_t total = static_cast<size_t>(2 * F_pad) * d8;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const int row = static_cast<int>(i / d8);
     const int c = static_cast<int>(i % d8);
     const int blk = row / 128, e = row % 128;
     const int src = blk * 64 + (e & 63);
-    out[i] = (e < 64 ? wg : wu)[static_cast<size_t>(src) * d8 + c];
+    out[i] = src < F ? (e < 64 ? wg : wu)[static_cast<size_t>(src) * d8 + c] : make_uint4(0, 0, 0, 0);
   }
 }
 
@@ -389,20 +399,22 @@ extern "C" hb_status hb_gemm(const void* A, const void* B, void* C, const void* 
   hb::DeviceCtx ctx;
   st = hb::device_context(&ctx);
   if (st != HB_OK) return st;
-  return hb::gemm_launch(ctx, A, B, C, R, M, N, K, epilogue, static_cast<cudaStream_t>(stream));
+  const int ldc = epilogue == HB_EPI_SWIGLU ? N / 2 : N;
+  return hb::gemm_launch(ctx, A, K, B, C, ldc, R, M, N, K, epilogue, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" hb_status hb_interleave_gate_up(const void* w_gate, const void* w_up, void* w_gu, int32_t F, int32_t d,
                                            void* stream) {
   hb::clear_error();
   HB_REQUIRE(w_gate && w_up && w_gu, "hb_interleave_gate_up: null pointer");
-  HB_REQUIRE(F > 0 && F % 64 == 0 && d > 0 && d % 8 == 0, "hb_interleave_gate_up: F %% 64 and d %% 8 required");
+  HB_REQUIRE(F > 0 && F % 8 == 0 && d > 0 && d % 8 == 0, "hb_interleave_gate_up: F %% 8 and d %% 8 required");
   HB_REQUIRE(hb::aligned16(w_gate) && hb::aligned16(w_up) && hb::aligned16(w_gu),
              "hb_interleave_gate_up: pointers must be 16-byte aligned");
   hb::DeviceCtx ctx;
   hb_status st = hb::device_context(&ctx);
   if (st != HB_OK) return st;
   hb::interleave_gate_up_kernel<<<ctx.num_sms * 8, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(w_gate), static_cast<const uint4*>(w_up), static_cast<uint4*>(w_gu), F, d / 8);
+      static_cast<const uint4*>(w_gate), static_cast<const uint4*>(w_up), static_cast<uint4*>(w_gu), F,
+      (F + 63) / 64 * 64, d / 8);
   return hb::launch_status("interleave_gate_up_kernel launch");
 }

@@ -16,6 +16,9 @@ namespace {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// SwiGLU width rounded up to the 64-row interleave blocks of w_gu.
+inline int ffn_pad(const hb_layer_dims& dm) { return (dm.d_ff + 63) / 64 * 64; }
+
 struct LayerWs {
   size_t xn, qkv, q, o, h, a, attn, total;
 };
@@ -29,7 +32,7 @@ LayerWs layer_ws(const hb_layer_dims& dm, int T, int S, int max_kv_len) {
   w.q = off;    off += align256(t * dm.n_q * dm.d_head * 2);
   w.o = off;    off += align256(t * dm.n_q * dm.d_head * 2);
   w.h = off;    off += align256(t * dm.d_model * 2);
-  w.a = off;    off += align256(t * dm.d_ff * 2);
+  w.a = off;    off += align256(t * ffn_pad(dm) * 2);
   w.attn = off; off += align256(attention_workspace_bytes(dm, S, max_kv_len));
   w.total = off;
   return w;
@@ -83,6 +86,7 @@ extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_
   void* a = ws + lw.a;
   void* aws = ws + lw.attn;
   const int d = dm.d_model, hd = dm.n_q * dm.d_head, qkv_cols = (dm.n_q + 2 * dm.n_kv) * dm.d_head;
+  const int fp = ffn_pad(dm);
 
   auto mark = [&](int k) -> hb_status {
     if (!prof) return HB_OK;
@@ -97,15 +101,15 @@ extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_
   } while (0)
 
   HB_STEP(0, rmsnorm_launch(ctx, x_in, nullptr, w->g1, xn, T, d, dm.rms_eps, T, s));
-  HB_STEP(1, gemm_launch(ctx, xn, w->w_qkv, qkv, nullptr, T, qkv_cols, d, HB_EPI_STORE, s));
+  HB_STEP(1, gemm_launch(ctx, xn, d, w->w_qkv, qkv, qkv_cols, nullptr, T, qkv_cols, d, HB_EPI_STORE, s));
   HB_STEP(2, kv_append_launch(ctx, qkv, T, plan->row_pos, plan->slot_mapping, rope, max_pos, dm, q, k_cache, v_cache,
                               num_pages, s));
   HB_STEP(3, attention_launch(ctx, q, k_cache, v_cache, num_pages, *plan, dm, max_kv_len, o, aws,
                               lw.total - lw.attn, s));
-  HB_STEP(4, gemm_launch(ctx, o, w->w_o, h, x_in, T, d, hd, HB_EPI_RESIDUAL, s));
+  HB_STEP(4, gemm_launch(ctx, o, hd, w->w_o, h, d, x_in, T, d, hd, HB_EPI_RESIDUAL, s));
   HB_STEP(5, rmsnorm_launch(ctx, h, nullptr, w->g2, xn, T, d, dm.rms_eps, T, s));
-  HB_STEP(6, gemm_launch(ctx, xn, w->w_gu, a, nullptr, T, 2 * dm.d_ff, d, HB_EPI_SWIGLU, s));
-  HB_STEP(7, gemm_launch(ctx, a, w->w_d, x_out, h, T, d, dm.d_ff, HB_EPI_RESIDUAL, s));
+  HB_STEP(6, gemm_launch(ctx, xn, d, w->w_gu, a, fp, nullptr, T, 2 * fp, d, HB_EPI_SWIGLU, s));
+  HB_STEP(7, gemm_launch(ctx, a, fp, w->w_d, x_out, d, h, T, d, dm.d_ff, HB_EPI_RESIDUAL, s));
 #undef HB_STEP
   return mark(HB_LAYER_STAGES);
 }
@@ -129,5 +133,5 @@ extern "C" hb_status hb_final_logits(const void* x, int32_t T, const int32_t* ro
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = rmsnorm_launch(ctx, x, rows, g_f, workspace, n_sel, d, eps, T, s);
   if (st != HB_OK) return st;
-  return gemm_launch(ctx, workspace, w_lm, logits, nullptr, n_sel, vocab, d, HB_EPI_F32, s);
+  return gemm_launch(ctx, workspace, d, w_lm, logits, vocab, nullptr, n_sel, vocab, d, HB_EPI_F32, s);
 }

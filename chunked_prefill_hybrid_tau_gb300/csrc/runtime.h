@@ -36,8 +36,9 @@ hb_status kv_append_launch(const DeviceCtx& ctx, const void* qkv, int T, const i
                            const void* rope, int max_pos, const hb_layer_dims& dims, void* q_out, void* k_cache,
                            void* v_cache, int num_pages, cudaStream_t stream);
 hb_status gemm_check(const void* A, const void* B, void* C, const void* R, int M, int N, int K, int epi);
-hb_status gemm_launch(const DeviceCtx& ctx, const void* A, const void* B, void* C, const void* R, int M, int N, int K,
-                      int epi, cudaStream_t stream);
+// A [M][K] with row stride lda, B [N][K], C/R with row stride ldc (elements).
+hb_status gemm_launch(const DeviceCtx& ctx, const void* A, int lda, const void* B, void* C, int ldc, const void* R,
+                      int M, int N, int K, int epi, cudaStream_t stream);
 size_t attention_workspace_bytes(const hb_layer_dims& dims, int max_seqs, int max_kv_len);
 hb_status attention_launch(const DeviceCtx& ctx, const void* q, const void* k_cache, const void* v_cache,
                            int num_pages, const hb_device_plan& plan, const hb_layer_dims& dims, int max_kv_len,

@@ -63,7 +63,7 @@ typedef struct hb_layer_dims {
   int32_t n_q;         /* query heads */
   int32_t n_kv;        /* key/value heads; n_q % n_kv == 0 (GQA: q head h reads kv head h / (n_q / n_kv)) */
   int32_t d_head;      /* head dimension; 64 or 128 */
-  int32_t d_ff;        /* SwiGLU inner size (multiple of 64) */
+  int32_t d_ff;        /* SwiGLU inner size (multiple of 8) */
   int32_t page_size;   /* tokens per KV page; must be 16 */
   float rms_eps;       /* RMSNorm epsilon, inside the square root */
   float rope_theta;    /* RoPE base, used by hb_rope_table */
@@ -225,7 +225,7 @@ hb_status hb_attention(const void* q, const void* k_cache, const void* v_cache, 
  *                    (hb_interleave_gate_up); C bf16 [M][N/2] =
  *                    silu(A Bg^T) * (A Bu^T)
  *   HB_EPI_F32     : C fp32 [M][N] = AB^T
- * Requires K % 64 == 0, N % 64 == 0 (N % 128 for SWIGLU), 16-byte aligned
+ * Requires K % 8 == 0 and N % 8 == 0 (N % 128 for SWIGLU), 16-byte aligned
  * pointers.
  * ---------------------------------------------------------------------- */
 typedef enum hb_epilogue {
@@ -238,9 +238,10 @@ typedef enum hb_epilogue {
 hb_status hb_gemm(const void* A, const void* B, void* C, const void* R, int32_t M, int32_t N, int32_t K,
                   int32_t epilogue, void* stream);
 
-/* Weight preparation: w_gu[2F][d] from w_gate[F][d], w_up[F][d] (device bf16),
- * rows interleaved in blocks of 64: [gate 0..63, up 0..63, gate 64..127, ...].
- * F % 64 == 0. */
+/* Weight preparation: w_gu[2 Fp][d], Fp = F rounded up to a multiple of 64,
+ * from w_gate[F][d] and w_up[F][d] (device bf16): rows interleaved in blocks
+ * of 64 ([gate 0..63, up 0..63, gate 64..127, ...]); rows of the padding
+ * (gate/up index >= F) are zero.  F % 8 == 0, d % 8 == 0. */
 hb_status hb_interleave_gate_up(const void* w_gate, const void* w_up, void* w_gu, int32_t F, int32_t d,
                                 void* stream);
 
@@ -264,7 +265,7 @@ hb_status hb_interleave_gate_up(const void* w_gate, const void* w_up, void* w_gu
 typedef struct hb_layer_weights {
   const void* w_qkv;  /* bf16 [(n_q + 2 n_kv) d_head][d_model] */
   const void* w_o;    /* bf16 [d_model][n_q d_head] */
-  const void* w_gu;   /* bf16 [2 d_ff][d_model], interleaved in blocks of 64 rows */
+  const void* w_gu;   /* bf16 [2 Fp][d_model] from hb_interleave_gate_up (Fp = d_ff rounded up to 64) */
   const void* w_d;    /* bf16 [d_model][d_ff] */
   const void* g1;     /* bf16 [d_model] */
   const void* g2;     /* bf16 [d_model] */

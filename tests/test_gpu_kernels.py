@@ -34,6 +34,25 @@ def test_rope_table_matches_oracle():
         assert np.mean(t[..., 0] == cos) > 0.999 and np.mean(t[..., 1] == sin) > 0.999
 
 
+def test_gemm_swiglu_padded_ffn():
+    """F = 688 (not a multiple of 64): the interleave pads gate/up to 704 rows
+    of zeros and the padded output columns are silu(0) * 0 = 0."""
+    rng = np.random.default_rng(688)
+    M, K, F = 68, 256, 688
+    Fp = 704
+    A = wl.bf16_round(rng.standard_normal((M, K), dtype=np.float32))
+    Wg = wl.bf16_round(rng.standard_normal((F, K), dtype=np.float32) * np.float32(0.02))
+    Wu = wl.bf16_round(rng.standard_normal((F, K), dtype=np.float32) * np.float32(0.02))
+    Wgu = torch.full((2 * Fp, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    hb.hb_interleave_gate_up(wd.bf16_tensor(Wg), wd.bf16_tensor(Wu), Wgu)
+    out = torch.empty((M, Fp), dtype=torch.bfloat16, device="cuda")
+    hb.hb_gemm(wd.bf16_tensor(A), Wgu, out, None, L.HB_EPI_SWIGLU)
+    hb.hb_check_status()
+    got = wd.to_numpy(out)
+    assert_close(got[:, :F], ol.silu(A @ Wg.T) * (A @ Wu.T), "swiglu padded")
+    assert np.all(got[:, F:] == 0)
+
+
 @pytest.mark.parametrize("rows,d", [(1, 256), (77, 4096), (300, 7168)])
 def test_rmsnorm(rows, d):
     rng = np.random.default_rng(rows)
@@ -60,6 +79,9 @@ GEMM_CASES = [
     (512, 28672, 4096, L.HB_EPI_SWIGLU),
     (65, 32000, 4096, L.HB_EPI_F32),
     (3, 640, 128, L.HB_EPI_F32),
+    (68, 200, 688, L.HB_EPI_STORE),          # K and N not multiples of 64 / 32
+    (68, 256, 688, L.HB_EPI_RESIDUAL),
+    (5, 1000, 72, L.HB_EPI_F32),
 ]
 
 

@@ -45,7 +45,39 @@ def from_bf16_bits(b: np.ndarray) -> np.ndarray:
 
 def bf16_round(x: np.ndarray) -> np.ndarray:
     """Round float32 values to the nearest bf16-representable float32."""
-    return from_bf16_bits(to_bf16_bits(x))
+    out = np.array(x, dtype=np.float32, copy=True)
+    bf16_round_(out)
+    return out
+
+
+_CHUNK = 1 << 22
+
+
+def bf16_round_(x: np.ndarray) -> np.ndarray:
+    """In-place round-to-nearest-even of a contiguous float32 array to bf16 values."""
+    u = x.reshape(-1).view(np.uint32)
+    tmp = np.empty(min(u.size, _CHUNK), np.uint32)
+    for i in range(0, u.size, _CHUNK):
+        c = u[i:i + _CHUNK]
+        t = tmp[:c.size]
+        np.right_shift(c, 16, out=t)
+        np.bitwise_and(t, 1, out=t)
+        t += np.uint32(0x7FFF)
+        c += t
+        c &= np.uint32(0xFFFF0000)
+    return x
+
+
+def normal_bf16(rng: np.random.Generator, shape, scale: float = 1.0) -> np.ndarray:
+    """N(0, scale^2) samples rounded to bf16, generated in place chunk by chunk."""
+    out = np.empty(shape, np.float32)
+    flat = out.reshape(-1)
+    for i in range(0, flat.size, _CHUNK):
+        c = flat[i:i + _CHUNK]
+        rng.standard_normal(out=c, dtype=np.float32)
+        if scale != 1.0:
+            c *= np.float32(scale)
+    return bf16_round_(out)
 
 
 # ----------------------------------------------------------------------------
@@ -94,7 +126,7 @@ def layer_weights(rng: np.random.Generator, dims: Dims, gamma_jitter: float = 0.
     d, f = dims.d_model, dims.d_ff
 
     def normal(*shape):
-        return bf16_round(rng.standard_normal(shape, dtype=np.float32) * np.float32(0.02))
+        return normal_bf16(rng, shape, 0.02)
 
     def gain():
         g = np.ones(d, np.float32)
@@ -114,7 +146,7 @@ def layer_weights(rng: np.random.Generator, dims: Dims, gamma_jitter: float = 0.
 
 
 def activations(rng: np.random.Generator, rows: int, d: int) -> np.ndarray:
-    return bf16_round(rng.standard_normal((rows, d), dtype=np.float32))
+    return normal_bf16(rng, (rows, d))
 
 
 # ----------------------------------------------------------------------------
@@ -178,17 +210,11 @@ def make_state(rng: np.random.Generator, dims: Dims, dec_ctx, prefills, slack_pa
     v_pool = np.zeros(shape, np.float32)
 
     def fill(req):
-        for t in range(req.done):
-            pg, off = req.pages[t // dims.page], t % dims.page
-            k_pool[pg, :, off, :] = rng.standard_normal((dims.n_kv, dims.d_head), dtype=np.float32)
-            v_pool[pg, :, off, :] = rng.standard_normal((dims.n_kv, dims.d_head), dtype=np.float32)
-
-    def fill_fast(req):
         n = req.done
         if n == 0:
             return
-        k = rng.standard_normal((n, dims.n_kv, dims.d_head), dtype=np.float32)
-        v = rng.standard_normal((n, dims.n_kv, dims.d_head), dtype=np.float32)
+        k = normal_bf16(rng, (n, dims.n_kv, dims.d_head))
+        v = normal_bf16(rng, (n, dims.n_kv, dims.d_head))
         t = np.arange(n)
         pg = np.asarray(req.pages)[t // dims.page]
         off = t % dims.page
@@ -196,12 +222,10 @@ def make_state(rng: np.random.Generator, dims: Dims, dec_ctx, prefills, slack_pa
         v_pool[pg, :, off, :] = v
 
     for r in decodes:
-        fill_fast(r)
+        fill(r)
     if random_prefix:
         for r in pfs:
-            fill_fast(r)
-    k_pool = bf16_round(k_pool)
-    v_pool = bf16_round(v_pool)
+            fill(r)
     return State(dims, decodes, pfs, perm[head:], num_pages, k_pool, v_pool)
 
 

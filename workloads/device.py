@@ -30,7 +30,8 @@ def layer_weights_device(w: dict, dims, device="cuda"):
     import chunked_prefill_hybrid_tau_gb300 as hb
     wg = bf16_tensor(w["w_g"], device)
     wu = bf16_tensor(w["w_u"], device)
-    w_gu = torch.empty((2 * dims.d_ff, dims.d_model), dtype=torch.bfloat16, device=device)
+    f_pad = (dims.d_ff + 63) // 64 * 64
+    w_gu = torch.empty((2 * f_pad, dims.d_model), dtype=torch.bfloat16, device=device)
     hb.hb_interleave_gate_up(wg, wu, w_gu)
     del wg, wu
     return hb.LayerWeights(w_qkv=bf16_tensor(w["w_qkv"], device), w_o=bf16_tensor(w["w_o"], device), w_gu=w_gu,
