@@ -66,6 +66,8 @@ PROTOTYPES = {
     "hb_attention_workspace_bytes": (C.c_size_t, [C.POINTER(hb_layer_dims), i32, i32, i32]),
     "hb_attention": (C.c_int, [vp, vp, vp, i32, C.POINTER(hb_device_plan), C.POINTER(hb_layer_dims), i32, vp, vp,
                                C.c_size_t, vp]),
+    "hb_attention_noalloc": (C.c_int, [vp, vp, vp, i32, C.POINTER(hb_device_plan), C.POINTER(hb_layer_dims), i32,
+                                       vp, vp]),
     "hb_gemm": (C.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, vp]),
     "hb_interleave_gate_up": (C.c_int, [vp, vp, vp, i32, i32, vp]),
     "hb_layer_workspace_bytes": (C.c_size_t, [C.POINTER(hb_layer_dims), i32, i32, i32]),

@@ -215,6 +215,32 @@ hb_status hb_attention(const void* q, const void* k_cache, const void* v_cache, 
                        void* out, void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * hb_attention_noalloc - hb_attention for callers that cannot allocate
+ * device memory (no counterpart on the pages: an interface addition).
+ *
+ * Some callers cannot pass a workspace: a plug-in running inside another
+ * engine's execution step, where that engine owns every device allocation
+ * and cudaMalloc is not allowed (it can also synchronise the device), or a
+ * host runtime with no spare device buffer.  This call takes only the inputs
+ * and the output (same meaning and layout as hb_attention) and uses a fixed
+ * 32 MiB scratch array that the library places in device memory of every GPU
+ * that loads it, held until the process exits.  It allocates nothing.
+ *   - Its first call on a device looks up that array's device address (once
+ *     per device, with the device current); make that first call before any
+ *     stream capture.
+ *   - Plans needing more scratch than 32 MiB (hb_attention_workspace_bytes
+ *     of n_seqs and max_kv_len above 32 MiB) are rejected with
+ *     HB_ERR_CAPACITY and a message; use hb_attention with a workspace then.
+ *   - Every call on a device shares the one array; the counters that must
+ *     start at zero are cleared by each call on `stream`.  Calls that can
+ *     overlap on the GPU (different streams, no ordering between them) race
+ *     on the array and give wrong results: order them.
+ * ---------------------------------------------------------------------- */
+hb_status hb_attention_noalloc(const void* q, const void* k_cache, const void* v_cache, int32_t num_pages,
+                               const hb_device_plan* plan, const hb_layer_dims* dims, int32_t max_kv_len,
+                               void* out, void* stream);
+
+/* ------------------------------------------------------------------------
  * hb_gemm - C = epilogue(A B^T) on the tensor cores (bf16 in, fp32
  * accumulate): the packed-token projections whose roofline the pages use
  * (Sarathi-Serve reading notes, section 1.6: T = max(T_math, T_mem)).
