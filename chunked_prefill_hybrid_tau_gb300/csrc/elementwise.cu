@@ -11,11 +11,14 @@ namespace {
 using namespace dev;
 
 // ---------------------------------------------------------------- RMSNorm
-// One warp per row: 16-byte loads, fp32 sum of squares, shuffle reduction,
-// y = x * rsqrt(mean(x^2) + eps) * gamma rounded once to bf16.  `rows`
-// (optional) gathers source rows (final norm of selected rows).
-constexpr int kNormWarps = 8;
+// One warp per row, four rows per CTA.  The row is held in registers (NV
+// 16-byte vectors per lane, all loads issued before the reduction), fp32
+// sum of squares, shuffle reduction, y = x * rsqrt(mean(x^2) + eps) * gamma
+// rounded once to bf16.  `rows` (optional) gathers source rows (final norm
+// of selected rows).
+constexpr int kNormWarps = 4;
 
+template <int NV>
 __global__ void __launch_bounds__(kNormWarps * 32)
     rmsnorm_kernel(const uint4* __restrict__ x, const int* __restrict__ rows, const uint4* __restrict__ gamma,
                    uint4* __restrict__ y, int n_rows, int d8, float inv_d, float eps, int n_src, int* status) {
@@ -31,13 +34,19 @@ __global__ void __launch_bounds__(kNormWarps * 32)
     }
   }
   const uint4* xr = x + static_cast<size_t>(src) * d8;
+  uint4 v[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int i = lane + 32 * k;
+    v[k] = i < d8 ? xr[i] : make_uint4(0, 0, 0, 0);
+  }
   float ss = 0.f;
-  for (int i = lane; i < d8; i += 32) {
-    uint4 v = xr[i];
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      float2 f = unpack_bf16x2(w[j]);
+      const float2 f = unpack_bf16x2(w[j]);
       ss += f.x * f.x + f.y * f.y;
     }
   }
@@ -45,12 +54,16 @@ __global__ void __launch_bounds__(kNormWarps * 32)
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   const float inv = rsqrtf(ss * inv_d + eps);
   uint4* yr = y + static_cast<size_t>(r) * d8;
-  for (int i = lane; i < d8; i += 32) {
-    uint4 v = xr[i], g = gamma[i];
-    uint32_t w[4] = {v.x, v.y, v.z, v.w}, gw[4] = {g.x, g.y, g.z, g.w}, o[4];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int i = lane + 32 * k;
+    if (i >= d8) break;
+    const uint4 g = gamma[i];
+    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w}, gw[4] = {g.x, g.y, g.z, g.w};
+    uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      float2 f = unpack_bf16x2(w[j]), gg = unpack_bf16x2(gw[j]);
+      const float2 f = unpack_bf16x2(w[j]), gg = unpack_bf16x2(gw[j]);
       o[j] = pack_bf16x2(f.x * inv * gg.x, f.y * inv * gg.y);
     }
     yr[i] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -139,10 +152,26 @@ hb_status rmsnorm_launch(const DeviceCtx& ctx, const void* x, const int* rows, c
                          int n_rows, int d, float eps, int n_src, cudaStream_t stream) {
   if (n_rows == 0) return HB_OK;
   const int blocks = (n_rows + kNormWarps - 1) / kNormWarps;
-  rmsnorm_kernel<<<blocks, kNormWarps * 32, 0, stream>>>(static_cast<const uint4*>(x), rows,
-                                                         static_cast<const uint4*>(gamma), static_cast<uint4*>(y),
-                                                         n_rows, d / 8, 1.0f / d, eps, n_src, ctx.status);
-  return launch_status("rmsnorm_kernel launch");
+  const int d8 = d / 8;
+  const int nv = (d8 + 31) / 32;
+  auto* xp = static_cast<const uint4*>(x);
+  auto* gp = static_cast<const uint4*>(gamma);
+  auto* yp = static_cast<uint4*>(y);
+#define HB_NORM(NV_)                                                                                           \
+  if (nv <= NV_) {                                                                                             \
+    rmsnorm_kernel<NV_><<<blocks, kNormWarps * 32, 0, stream>>>(xp, rows, gp, yp, n_rows, d8, 1.0f / d, eps,   \
+                                                                n_src, ctx.status);                            \
+    return launch_status("rmsnorm_kernel launch");                                                            \
+  }
+  HB_NORM(1)
+  HB_NORM(2)
+  HB_NORM(4)
+  HB_NORM(8)
+  HB_NORM(16)
+  HB_NORM(32)
+#undef HB_NORM
+  set_error("rmsnorm: d = %d above the supported 8192", d);
+  return HB_ERR_UNSUPPORTED;
 }
 
 hb_status kv_append_launch(const DeviceCtx& ctx, const void* qkv, int T, const int* row_pos, const int* slots,
