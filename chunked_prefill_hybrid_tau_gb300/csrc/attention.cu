@@ -12,7 +12,7 @@
 //     own 16 rows each and sweep all key blocks 0..pos_last (tensor path:
 //     mma.sync m16n8k16, fp32 online softmax, causal mask by position);
 //   * decode unit: one decode row x one kv head (its n_q/n_kv q heads as MMA
-//     rows) x one 512-key split at fixed absolute positions, so the result
+//     rows) x one 1024-key split at fixed absolute positions, so the result
 //     of a row never depends on its batch companions.  Warp w takes page w
 //     of every 64-key block; the four warps merge in shared memory; splits
 //     are combined in a fixed order by the last CTA to finish (HBM path).
@@ -31,7 +31,7 @@ using namespace dev;
 
 constexpr int KB = 64;                      // keys per block (4 pages)
 constexpr int STAGES = 4;
-constexpr int SPLIT = 512;                  // keys per decode split
+constexpr int SPLIT = 1024;                 // keys per decode split
 constexpr int QTILE = 64;                   // query rows per chunk tile
 constexpr int kConsumers = 128;             // 4 consumer warps
 constexpr int kThreads = kConsumers + 32;   // + producer warp
@@ -56,6 +56,7 @@ struct Params {
   const int* kv_len;
   const int* block_table;
   int S, T, max_pages, num_pages, n_q, n_kv, grp, max_kv_len;
+  int chunk_only;  // 1: schedule chunk tiles only (decode rows go to decode_kernel)
   float scale_log2;
   int* work_counter;
   int* combine_counters;
@@ -278,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
       flag_error(p.status, kStatusIndex);
     } else if (qlen > 1) {
       c = p.n_q * ((qlen + QTILE - 1) / QTILE);
-    } else if (qlen == 1) {
+    } else if (qlen == 1 && !p.chunk_only) {
       d = p.n_kv * ((kvl + SPLIT - 1) / SPLIT);
     }
     cpre[s + 1] = c;
@@ -557,8 +558,253 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
   }
 }
 
+
+// ---------------------------------------------------------------- decode rows
+// HBM path.  Each warp owns whole units -- one decode row x one kv head (its
+// q-head group as MMA rows) x one SPLIT-key range at fixed absolute
+// positions -- and streams the unit's 16-token pages through its own
+// DR-deep ring of TMA boxes, refilling a slot as soon as it has consumed it.
+// No cross-warp synchronisation: partial results go straight from registers
+// to the split records, and the last warp to finish a (row, kv head)
+// combines the splits in split order.
+constexpr int kDecWarps = 8;
+
 template <int D>
-hb_status attention_launch_d(const DeviceCtx& ctx, const CUtensorMap& tmK, const CUtensorMap& tmV, const Params& p,
+struct DC {
+  static constexpr int PAGE_BYTES = (D / 64) * HALF_BYTES;  // one page of one kv head, K or V
+  static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;        // K page then V page
+  static constexpr int DR = D == 128 ? 3 : 6;               // ring depth per warp
+  static constexpr int REC_FLOATS = 16 * D + 32;
+  static constexpr int RING_BYTES = kDecWarps * DR * STAGE_BYTES;  // multiple of 1024
+  static constexpr int BAR_BYTES = kDecWarps * DR * 8;               // mbarriers: 8-byte aligned after the rings
+  static constexpr int BT_BYTES = kDecWarps * (SPLIT / 16) * 4;    // per-warp copy of a unit's page ids
+  static constexpr int SMEM = RING_BYTES + BAR_BYTES + BT_BYTES + (MAX_SEQS + 1) * 4 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kDecWarps * 32, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, Params p) {
+  using C = DC<D>;
+  constexpr int DR = C::DR, STAGE_BYTES = C::STAGE_BYTES, PAGE_BYTES = C::PAGE_BYTES, REC_FLOATS = C::REC_FLOATS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::RING_BYTES);
+  int* btc_all = reinterpret_cast<int*>(smem + C::RING_BYTES + C::BAR_BYTES);
+  int* dpre = btc_all + kDecWarps * (SPLIT / 16);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ga = lane >> 2, t4 = lane & 3;
+
+  for (int s = tid; s < p.S; s += blockDim.x) {
+    const int q0 = p.q_start[s], q1 = p.q_start[s + 1];
+    const int kvl = p.kv_len[s];
+    int d = 0;
+    if (q1 - q0 == 1) {
+      if (q0 < 0 || q1 > p.T || kvl < 1 || kvl > p.max_kv_len || (kvl + 15) / 16 > p.max_pages)
+        flag_error(p.status, kStatusIndex);
+      else
+        d = p.n_kv * ((kvl + SPLIT - 1) / SPLIT);
+    }
+    dpre[s + 1] = d;
+  }
+  if (tid < kDecWarps * DR) mbar_init(&bars[tid], 1);
+  if (tid == 0) fence_barrier_init();
+  __syncthreads();
+  if (tid == 0) {
+    dpre[0] = 0;
+    for (int s = 1; s <= p.S; ++s) dpre[s] += dpre[s - 1];
+  }
+  __syncthreads();
+  const int total = dpre[p.S];
+  if (tid == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+
+  uint8_t* ring = smem + warp * DR * STAGE_BYTES;
+  uint64_t* full = bars + warp * DR;
+  int* btc = btc_all + warp * (SPLIT / 16);
+  uint32_t phases = 0;  // bit s: parity to wait for on slot s
+  while (true) {
+    int u = 0;
+    if (lane == 0) u = atomicAdd(p.work_counter + 1, 1);
+    u = __shfl_sync(0xffffffffu, u, 0);
+    if (u >= total) break;
+    const int s = upper_index(dpre, p.S, u);
+    const int local = u - dpre[s];
+    const int kvl = p.kv_len[s];
+    const int g = local % p.n_kv;
+    const int split = local / p.n_kv;
+    const int key_begin = split * SPLIT;
+    const int key_end = min(kvl, key_begin + SPLIT);
+    const int nsplit = (kvl + SPLIT - 1) / SPLIT;
+    const int npages = (key_end - key_begin + 15) / 16;
+    const int page0 = key_begin / 16;
+    const int* bt = p.block_table + static_cast<size_t>(s) * p.max_pages;
+    const int row = p.q_start[s];
+    // the unit's page ids, validated once, into this warp's shared copy
+    for (int b = lane; b < npages; b += 32) {
+      int page = bt[page0 + b];
+      if (page < 0 || page >= p.num_pages) {
+        flag_error(p.status, kStatusIndex);
+        page = 0;
+      }
+      btc[b] = page;
+    }
+    __syncwarp();
+
+    auto issue = [&](int b) {  // lane 0: page b of this unit into slot b % DR
+      const int slot = b % DR;
+      const int page = btc[b];
+      const int y = (page * p.n_kv + g) * 16;
+      uint8_t* dst = ring + slot * STAGE_BYTES;
+      mbar_arrive_expect_tx(&full[slot], STAGE_BYTES);
+#pragma unroll
+      for (int hf = 0; hf < D / 64; ++hf) {
+        tma_load_2d(dst + hf * HALF_BYTES, &tmK, &full[slot], hf * 64, y);
+        tma_load_2d(dst + PAGE_BYTES + hf * HALF_BYTES, &tmV, &full[slot], hf * 64, y);
+      }
+    };
+    if (lane == 0)
+      for (int b = 0; b < min(DR, npages); ++b) issue(b);
+
+    // q rows of this kv head's group (rows >= grp are zero padding)
+    const bool oka = ga < p.grp, okb = ga + 8 < p.grp;
+    const size_t qbase = static_cast<size_t>(row) * p.n_q + g * p.grp;
+    const __nv_bfloat16* qra = p.q + (qbase + (oka ? ga : 0)) * D;
+    const __nv_bfloat16* qrb = p.q + (qbase + (okb ? ga + 8 : 0)) * D;
+    uint32_t qa[D / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      qa[kk][0] = ld_q2(qra, 16 * kk + 2 * t4, oka);
+      qa[kk][1] = ld_q2(qrb, 16 * kk + 2 * t4, okb);
+      qa[kk][2] = ld_q2(qra, 16 * kk + 8 + 2 * t4, oka);
+      qa[kk][3] = ld_q2(qrb, 16 * kk + 8 + 2 * t4, okb);
+    }
+    float o[D / 8][4];
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    const int lim = key_end - 1;
+
+    bool ok = true;
+    for (int b = 0; b < npages; ++b) {
+      const int slot = b % DR;
+      bool fok = mbar_wait(&full[slot], (phases >> slot) & 1u, nullptr, p.status);
+      phases ^= 1u << slot;
+      if (!__all_sync(0xffffffffu, fok)) {
+        ok = false;
+        break;
+      }
+      uint8_t* st = ring + slot * STAGE_BYTES;
+      const int key0 = key_begin + 16 * b;
+      const bool tail = key0 + 16 > key_end;
+      if (tail) {
+        // keys past key_end may hold uninitialised memory: zero their V rows
+        uint4* vb = reinterpret_cast<uint4*>(st + PAGE_BYTES);
+        const int first = key_end - key0;
+        for (int i = lane; i < (16 - first) * (D / 8); i += 32) {
+          const int key = first + i / (D / 8), c = i % (D / 8);
+          vb[blk_off<D>(key, c) / 16] = make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
+      const uint32_t kb = smem_u32(st);
+      warp_block<D, 1>(kb, kb + PAGE_BYTES, 0, key0, qa, o, m, l, lim, lim, p.scale_log2, lane);
+      // slot consumed.  Reads are complete (their results fed the MMAs); the
+      // zeroing writes of a tail page must be ordered before the next TMA write.
+      if (tail) fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && b + DR < npages) issue(b + DR);
+    }
+    if (!ok) {
+      // unwind: let this warp's copies in flight land (bounded) before exiting
+      if (lane == 0)
+        for (int sl = 0; sl < DR; ++sl) mbar_drain(&full[sl], (phases >> sl) & 1u);
+      break;
+    }
+
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
+      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
+    }
+    __nv_bfloat16* orow = p.out + static_cast<size_t>(row) * p.n_q * D + g * p.grp * D;
+    if (nsplit == 1) {
+      const float ia = l[0] > 0.f ? 1.f / l[0] : 0.f, ib = l[1] > 0.f ? 1.f / l[1] : 0.f;
+#pragma unroll
+      for (int j = 0; j < D / 8; ++j) {
+        const int col = 8 * j + 2 * t4;
+        if (oka) *reinterpret_cast<uint32_t*>(orow + ga * D + col) = pack_bf16x2(o[j][0] * ia, o[j][1] * ia);
+        if (okb) *reinterpret_cast<uint32_t*>(orow + (ga + 8) * D + col) = pack_bf16x2(o[j][2] * ib, o[j][3] * ib);
+      }
+      continue;
+    }
+    // split record (unnormalised O, running max in log2 units, row sum)
+    float* rec = p.partials + static_cast<size_t>(u) * REC_FLOATS;
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) {
+      const int col = 8 * j + 2 * t4;
+      if (oka) *reinterpret_cast<float2*>(rec + ga * D + col) = make_float2(o[j][0], o[j][1]);
+      if (okb) *reinterpret_cast<float2*>(rec + (ga + 8) * D + col) = make_float2(o[j][2], o[j][3]);
+    }
+    if (t4 == 0) {
+      rec[16 * D + ga] = m[0];
+      rec[16 * D + ga + 8] = m[1];
+      rec[16 * D + 16 + ga] = l[0];
+      rec[16 * D + 16 + ga + 8] = l[1];
+    }
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      int* cnt = p.combine_counters + s * p.n_kv + g;
+      const int old = atomicAdd(cnt, 1);
+      last = old == nsplit - 1;
+      if (last) *cnt = 0;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) continue;
+    __threadfence();
+    // combine the splits of this (row, kv head) in split order: lane r < grp
+    // finds row r's max and sum over splits, then each lane owns 4 columns of
+    // every row and issues all its split loads before accumulating
+    const float* rec0 = p.partials + static_cast<size_t>(u - split * p.n_kv) * REC_FLOATS;
+    const size_t rstride = static_cast<size_t>(p.n_kv) * REC_FLOATS;
+    float Mr = -INFINITY, Lr = 0.f;
+    if (lane < p.grp) {
+#pragma unroll 4
+      for (int sp = 0; sp < nsplit; ++sp) Mr = fmaxf(Mr, __ldcg(rec0 + sp * rstride + 16 * D + lane));
+#pragma unroll 4
+      for (int sp = 0; sp < nsplit; ++sp) {
+        const float* rs = rec0 + sp * rstride;
+        Lr += __ldcg(rs + 16 * D + 16 + lane) * exp2f(__ldcg(rs + 16 * D + lane) - Mr);
+      }
+    }
+    for (int r = 0; r < p.grp; ++r) {
+      const float M = __shfl_sync(0xffffffffu, Mr, r);
+      const float L = __shfl_sync(0xffffffffu, Lr, r);
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      for (int c4 = lane; c4 < D / 4; c4 += 32) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int sp = 0; sp < nsplit; ++sp) {
+          const float* rs = rec0 + sp * rstride;
+          const float wgt = exp2f(__ldcg(rs + 16 * D + r) - M);
+          const float4 ov = __ldcg(reinterpret_cast<const float4*>(rs + r * D) + c4);
+          acc.x += wgt * ov.x;
+          acc.y += wgt * ov.y;
+          acc.z += wgt * ov.z;
+          acc.w += wgt * ov.w;
+        }
+        *reinterpret_cast<uint2*>(orow + r * D + 4 * c4) =
+            make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+      }
+    }
+  }
+}
+
+template <int D>
+hb_status attention_launch_d(const DeviceCtx& ctx, const CUtensorMap& tmK, const CUtensorMap& tmV, Params p,
                              cudaStream_t stream) {
   static bool attr_set[64] = {};
   if (!attr_set[ctx.device]) {
@@ -566,10 +812,18 @@ hb_status attention_launch_d(const DeviceCtx& ctx, const CUtensorMap& tmK, const
         cudaFuncSetAttribute(attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, AC<D>::SMEM),
         "cudaFuncSetAttribute(attention)");
     if (st != HB_OK) return st;
+    st = cuda_status(cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DC<D>::SMEM),
+                     "cudaFuncSetAttribute(decode)");
+    if (st != HB_OK) return st;
     attr_set[ctx.device] = true;
   }
+  // chunk tiles (tensor path), then decode rows (HBM path), both persistent
+  p.chunk_only = 1;
   attention_kernel<D><<<ctx.num_sms, kThreads, AC<D>::SMEM, stream>>>(tmK, tmV, p);
-  return launch_status("attention_kernel launch");
+  hb_status st = launch_status("attention_kernel launch");
+  if (st != HB_OK) return st;
+  decode_kernel<D><<<ctx.num_sms, kDecWarps * 32, DC<D>::SMEM, stream>>>(tmK, tmV, p);
+  return launch_status("decode_kernel launch");
 }
 
 }  // namespace
@@ -622,7 +876,7 @@ hb_status attention_launch(const DeviceCtx& ctx, const void* q, const void* k_ca
   p.grp = dm.n_q / dm.n_kv;
   p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(dm.d_head)));
   uint8_t* w8 = static_cast<uint8_t*>(ws);
-  p.work_counter = reinterpret_cast<int*>(w8);
+  p.work_counter = reinterpret_cast<int*>(w8);  // [0] chunk tiles, [1] decode units
   p.combine_counters = reinterpret_cast<int*>(w8 + 256);
   p.partials = reinterpret_cast<float*>(w8 + counters);
   p.status = ctx.status;
