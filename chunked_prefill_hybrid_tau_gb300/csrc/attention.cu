@@ -804,8 +804,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
 }
 
 template <int D>
-hb_status attention_launch_d(const DeviceCtx& ctx, const CUtensorMap& tmK, const CUtensorMap& tmV, Params p,
-                             cudaStream_t stream) {
+hb_status attention_launch_d(const DeviceCtx& ctx, const void* q, const hb_device_plan& plan, const hb_layer_dims& dm,
+                             const CUtensorMap& tmK, const CUtensorMap& tmV, Params p, cudaStream_t stream) {
   static bool attr_set[64] = {};
   if (!attr_set[ctx.device]) {
     hb_status st = cuda_status(
@@ -817,10 +817,8 @@ hb_status attention_launch_d(const DeviceCtx& ctx, const CUtensorMap& tmK, const
     if (st != HB_OK) return st;
     attr_set[ctx.device] = true;
   }
-  // chunk tiles (tensor path), then decode rows (HBM path), both persistent
-  p.chunk_only = 1;
-  attention_kernel<D><<<ctx.num_sms, kThreads, AC<D>::SMEM, stream>>>(tmK, tmV, p);
-  hb_status st = launch_status("attention_kernel launch");
+  // chunk tiles (tcgen05 path), then decode rows (HBM path), both persistent
+  hb_status st = chunk_tc_launch(ctx, q, tmK, tmV, plan, dm, p.num_pages, p.max_kv_len, p.out, p.work_counter, stream);
   if (st != HB_OK) return st;
   decode_kernel<D><<<ctx.num_sms, kDecWarps * 32, DC<D>::SMEM, stream>>>(tmK, tmV, p);
   return launch_status("decode_kernel launch");
@@ -880,8 +878,8 @@ hb_status attention_launch(const DeviceCtx& ctx, const void* q, const void* k_ca
   p.combine_counters = reinterpret_cast<int*>(w8 + 256);
   p.partials = reinterpret_cast<float*>(w8 + counters);
   p.status = ctx.status;
-  return dm.d_head == 128 ? attention_launch_d<128>(ctx, tmK, tmV, p, stream)
-                          : attention_launch_d<64>(ctx, tmK, tmV, p, stream);
+  return dm.d_head == 128 ? attention_launch_d<128>(ctx, q, plan, dm, tmK, tmV, p, stream)
+                          : attention_launch_d<64>(ctx, q, plan, dm, tmK, tmV, p, stream);
 }
 
 }  // namespace hb

@@ -1,0 +1,566 @@
+// Chunk-row attention on the 5th-generation tensor cores.
+//
+// A prompt chunk's query at position p attends to keys 0..p of its request:
+// the prefix cached by earlier chunks plus the causal part of its own chunk
+// (Sarathi-Serve reading notes, sections 3.1 and 7.5b).  This is the dense,
+// tensor-bound half of the hybrid attention; decode rows go to the HBM path.
+//
+// Work unit: 128 consecutive query rows of one sequence x one q head (GQA: the
+// unit's kv head is head / (n_q / n_kv)), keys 0 .. pos_last in 128-key blocks
+// read through the block table.  Persistent CTAs take units from a global
+// counter, heaviest (latest) tiles first.
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0   TMA producer: the unit's Q tile (3-D box over [T][n_q][D]) and,
+//            per block, 8 pages of K and of V (16 keys x 64 dims per box, 128-
+//            byte swizzle) into a 2-stage ring;
+//   warp 1   MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM S
+//            buffers (K-major operands), then O += P_j V_j with P from shared
+//            memory (K-major) and V as an MN-major operand;
+//   warps 2-5 softmax, one query row per thread: tcgen05.ld of the S row,
+//            causal mask, online softmax in base 2 with a lazily updated
+//            maximum (O in TMEM is rescaled only when a row's maximum grows by
+//            more than 2^8), P written as bf16 into shared memory; finally
+//            O / l from TMEM to global memory.
+// Every wait is bounded; an expired wait sets the status word and unwinds.
+#include <cuda_bf16.h>
+
+#include "device.cuh"
+#include "runtime.h"
+
+namespace hb {
+namespace {
+
+using namespace dev;
+
+constexpr int TQ = 128;           // query rows per unit (MMA M)
+constexpr int TK = 128;           // keys per block (MMA N of S, K of PV)
+constexpr int NSTAGE = 2;
+constexpr int MAX_SEQS = 1024;
+constexpr int kThreads = 192;
+constexpr float kRescale = 8.0f;  // log2 growth of a row maximum that forces an O rescale
+
+template <int D>
+struct TC {
+  static constexpr int HALVES = D / 64;
+  static constexpr int HALF_TILE = 128 * 128;            // 128 rows x 128 bytes
+  static constexpr int Q_BYTES = HALVES * HALF_TILE;     // Q tile
+  static constexpr int KV_BYTES = HALVES * HALF_TILE;    // K (or V) block of 128 keys
+  static constexpr int STAGE_BYTES = 2 * KV_BYTES;
+  static constexpr int P_BYTES = 2 * HALF_TILE;          // 128 rows x 128 keys bf16
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = Q_BYTES;
+  static constexpr int OFF_P = OFF_KV + NSTAGE * STAGE_BYTES;
+  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int OFF_PRE = OFF_BAR + BAR_BYTES;
+  static constexpr int SMEM = OFF_PRE + (MAX_SEQS + 1) * 4 + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;             // S0 | S1 | O
+  static constexpr uint32_t COL_O = 256;
+};
+
+struct TcParams {
+  __nv_bfloat16* out;
+  const int* q_start;
+  const int* kv_len;
+  const int* block_table;
+  int S, T, max_pages, num_pages, n_q, n_kv, grp, max_kv_len;
+  float scale_log2;
+  int* work_counter;
+  int* status;
+};
+
+struct TcUnit {
+  int seq, head, row0, nrows, pos0, nblk, valid;
+};
+
+__device__ __forceinline__ int upper_index(const int* pre, int n, int u) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ TcUnit tc_unit(const TcParams& p, const int* pre, int u) {
+  TcUnit w;
+  w.valid = u < pre[p.S];
+  if (!w.valid) return w;
+  const int s = upper_index(pre, p.S, u);
+  const int local = u - pre[s];
+  const int q0 = p.q_start[s], qlen = p.q_start[s + 1] - q0;
+  const int ntiles = (qlen + TQ - 1) / TQ;
+  const int t = ntiles - 1 - local / p.n_q;  // heaviest tiles first
+  w.seq = s;
+  w.head = local % p.n_q;
+  w.row0 = q0 + t * TQ;
+  w.nrows = min(TQ, qlen - t * TQ);
+  w.pos0 = p.kv_len[s] - qlen + t * TQ;
+  w.nblk = (w.pos0 + w.nrows + TK - 1) / TK;
+  return w;
+}
+
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
+                                            int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Shared-memory descriptor of an MN-major operand with the 128-byte swizzle:
+// rows of 64 contiguous MN elements (128 B) along K, 8-row groups `sbo` bytes
+// apart (K direction), 64-element MN atoms `lbo` bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, TcParams p) {
+  using C = TC<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sKV = smem + C::OFF_KV;
+  uint8_t* sP = smem + C::OFF_P;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* kv_full = bar;                  // [NSTAGE]
+  uint64_t* kv_empty = bar + 2;             // [NSTAGE]
+  uint64_t* q_full = bar + 4;
+  uint64_t* q_empty = bar + 5;
+  uint64_t* s_full = bar + 6;               // [2]
+  uint64_t* s_empty = bar + 8;              // [2]
+  uint64_t* p_full = bar + 10;
+  uint64_t* pv_done = bar + 11;             // one completion per PV block
+  uint64_t* o_empty = bar + 12;
+  uint64_t* uq_full = bar + 13;             // [2]
+  uint64_t* uq_empty = bar + 15;            // [2]
+  uint64_t* drain = bar + 17;
+  int* uq = reinterpret_cast<int*>(bar + 18);  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(uq + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* pre = reinterpret_cast<int*>(smem + C::OFF_PRE);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- per-sequence unit counts (chunk sequences: more than one row)
+  for (int s = tid; s < p.S; s += kThreads) {
+    const int q0 = p.q_start[s], q1 = p.q_start[s + 1];
+    const int qlen = q1 - q0, kvl = p.kv_len[s];
+    int c = 0;
+    if (q0 < 0 || q1 > p.T || qlen < 0 || kvl < qlen || kvl > p.max_kv_len || (kvl + 15) / 16 > p.max_pages)
+      flag_error(p.status, kStatusIndex);
+    else if (qlen > 1)
+      c = p.n_q * ((qlen + TQ - 1) / TQ);
+    pre[s + 1] = c;
+  }
+  if (tid == 0) {
+    for (int i = 0; i < NSTAGE; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 4);
+      mbar_init(&uq_full[i], 1);
+      mbar_init(&uq_empty[i], 5);
+    }
+    mbar_init(p_full, 4);
+    mbar_init(pv_done, 1);
+    mbar_init(o_empty, 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0) {
+    pre[0] = 0;
+    for (int s = 1; s <= p.S; ++s) pre[s] += pre[s - 1];
+  }
+  __syncthreads();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      int qs = 0, stage = 0, nunit = 0;
+      uint32_t qph = 0, kph = 0;
+      uint32_t pending = 0, armed = 0;
+      bool ok = true;
+      while (ok) {
+        if (!mbar_wait(&uq_empty[qs], qph ^ 1u, abort_flag, p.status)) break;
+        const int u = atomicAdd(p.work_counter, 1);
+        uq[qs] = u;
+        mbar_arrive(&uq_full[qs]);
+        if (++qs == 2) {
+          qs = 0;
+          qph ^= 1u;
+        }
+        const TcUnit w = tc_unit(p, pre, u);
+        if (!w.valid) break;
+        // Q tile (the MMA of the previous unit's last S block has read it)
+        if (!mbar_wait(q_empty, (nunit & 1) ^ 1u, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+#pragma unroll
+        for (int hf = 0; hf < C::HALVES; ++hf) tma_load_3d(sQ + hf * C::HALF_TILE, &tmQ, q_full, hf * 64, w.head, w.row0);
+        ++nunit;
+        const int g = w.head / p.grp;
+        const int* bt = p.block_table + static_cast<size_t>(w.seq) * p.max_pages;
+        const int key_end = w.pos0 + w.nrows;
+        for (int j = 0; j < w.nblk; ++j) {
+          if (!mbar_wait(&kv_empty[stage], kph ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const int npg = min(8, (key_end - j * TK + 15) / 16);
+          pending |= 1u << stage;
+          armed = (armed & ~(1u << stage)) | (kph << stage);
+          mbar_arrive_expect_tx(&kv_full[stage], npg * 2 * C::HALVES * 2048);
+          uint8_t* sk = sKV + stage * C::STAGE_BYTES;
+          for (int pg = 0; pg < npg; ++pg) {
+            int page = bt[j * 8 + pg];
+            if (page < 0 || page >= p.num_pages) {
+              flag_error(p.status, kStatusIndex);
+              page = 0;
+            }
+            const int y = (page * p.n_kv + g) * 16;
+#pragma unroll
+            for (int hf = 0; hf < C::HALVES; ++hf) {
+              tma_load_2d(sk + hf * C::HALF_TILE + pg * 2048, &tmK, &kv_full[stage], hf * 64, y);
+              tma_load_2d(sk + C::KV_BYTES + hf * C::HALF_TILE + pg * 2048, &tmV, &kv_full[stage], hf * 64, y);
+            }
+          }
+          if (++stage == NSTAGE) {
+            stage = 0;
+            kph ^= 1u;
+          }
+        }
+      }
+      if (!ok)
+        for (int s = 0; s < NSTAGE; ++s)
+          if (pending & (1u << s)) mbar_drain(&kv_full[s], (armed >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    const bool leader = lane == 0;
+    constexpr uint32_t idS = idesc_bf16_f32(TQ, TK);
+    constexpr uint32_t idPV = idesc_bf16_f32(TQ, D) | (1u << 16);  // B (V) is MN-major
+    int qs = 0, stage = 0, J = 0, nunit = 0;
+    uint32_t qph = 0, kph = 0;
+    bool ok = true;
+    while (ok) {
+      bool got = mbar_wait(&uq_full[qs], qph, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, got)) break;
+      const int u = uq[qs];
+      __syncwarp();
+      if (leader) mbar_arrive(&uq_empty[qs]);
+      if (++qs == 2) {
+        qs = 0;
+        qph ^= 1u;
+      }
+      const TcUnit w = tc_unit(p, pre, u);
+      if (!w.valid) break;
+      if (leader) {
+        ok = mbar_wait(q_full, nunit & 1, abort_flag, p.status);
+        // O of the previous unit has been read by the epilogue
+        ok = ok && mbar_wait(o_empty, (nunit & 1) ^ 1u, abort_flag, p.status);
+        tc_fence_after();
+        const uint32_t q_addr = smem_u32(sQ);
+        int pst = 0;  // stage of block j - 1
+        for (int j = 0; j <= w.nblk && ok; ++j) {
+          if (j < w.nblk) {
+            const int b = (J + j) & 1;
+            ok = mbar_wait(&kv_full[stage], kph, abort_flag, p.status) &&
+                 mbar_wait(&s_empty[b], (((J + j) >> 1) & 1) ^ 1u, abort_flag, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t k_addr = smem_u32(sKV + stage * C::STAGE_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::HALF_TILE + (kk & 3) * 32;
+              mma_bf16(tmem + b * TK, smem_desc_sw128(q_addr + off), smem_desc_sw128(k_addr + off), idS,
+                       kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&s_full[b]);
+            if (j == w.nblk - 1) mma_commit(q_empty);
+          }
+          if (j > 0) {
+            // O += P_{j-1} V_{j-1} once the softmax has written P_{j-1}
+            ok = mbar_wait(p_full, (J + j - 1) & 1, abort_flag, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t p_addr = smem_u32(sP);
+            const uint32_t v_addr = smem_u32(sKV + pst * C::STAGE_BYTES + C::KV_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < TK / 16; ++kk) {
+              const uint64_t a = smem_desc_sw128(p_addr + (kk >> 2) * C::HALF_TILE + (kk & 3) * 32);
+              const uint64_t bdesc = smem_desc_sw128_mn(v_addr + kk * 2048, C::HALF_TILE, 1024);
+              mma_bf16(tmem + C::COL_O, a, bdesc, idPV, (j > 1 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&kv_empty[pst]);
+            mma_commit(pv_done);
+          }
+          if (j < w.nblk) {
+            pst = stage;
+            if (++stage == NSTAGE) {
+              stage = 0;
+              kph ^= 1u;
+            }
+          }
+        }
+        J += w.nblk;
+        ++nunit;
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      J = __shfl_sync(0xffffffffu, J, 0);
+      nunit = __shfl_sync(0xffffffffu, nunit, 0);
+      stage = __shfl_sync(0xffffffffu, stage, 0);
+      kph = __shfl_sync(0xffffffffu, kph, 0);
+    }
+    if (leader && !ok) {
+      mma_commit(drain);
+      mbar_drain(drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // query row of this thread within the tile
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    int qs = 0, J = 0, nunit = 0;
+    uint32_t qph = 0;
+    while (true) {
+      bool got = mbar_wait(&uq_full[qs], qph, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, got)) break;
+      const int u = uq[qs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&uq_empty[qs]);
+      if (++qs == 2) {
+        qs = 0;
+        qph ^= 1u;
+      }
+      const TcUnit w = tc_unit(p, pre, u);
+      if (!w.valid) break;
+      const int key_end = w.pos0 + w.nrows;
+      const int lim = r < w.nrows ? w.pos0 + r : key_end - 1;  // last key this row sees
+      float m_used = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < w.nblk; ++j) {
+        const int b = (J + j) & 1;
+        bool sok = mbar_wait(&s_full[b], ((J + j) >> 1) & 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, sok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sv[TK];
+#pragma unroll
+        for (int c = 0; c < TK / 32; ++c) tmem_ld_32x32b_x32(tmem + lane_base + b * TK + c * 32,
+                                                            *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[b]);
+        // mask and scale (base 2), row maximum
+        const int key0 = j * TK;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < TK; ++c) {
+          const float v = key0 + c <= lim ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
+          sv[c] = __float_as_uint(v);
+          mx = fmaxf(mx, v);
+        }
+        // lazily raise the maximum; rescale O (in TMEM) and l when it moves
+        const bool raise = mx > m_used + kRescale;
+        const float m_new = raise ? mx : m_used;
+        const float alpha = raise ? exp2f(m_used - m_new) : 1.f;
+        if (j > 0 && __any_sync(0xffffffffu, raise)) {
+          // the previous PV block must be complete before O is touched
+          bool pok = mbar_wait(pv_done, (J + j - 1) & 1, abort_flag, p.status);
+          if (!__all_sync(0xffffffffu, pok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld_32x32b_x32(tmem + lane_base + C::COL_O + c * 32, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st_32x32b_x32(tmem + lane_base + C::COL_O + c * 32, ov);
+          }
+          tmem_st_wait();
+        }
+        m_used = m_new;
+        l *= alpha;
+        // P = 2^(s - m) as bf16, written as row r of the K-major P tile
+        float rs = 0.f;
+        uint32_t pk[TK / 2];
+#pragma unroll
+        for (int c = 0; c < TK / 2; ++c) {
+          const float a0 = exp2f(__uint_as_float(sv[2 * c]) - m_used);
+          const float a1 = exp2f(__uint_as_float(sv[2 * c + 1]) - m_used);
+          rs += a0 + a1;
+          pk[c] = pack_bf16x2(a0, a1);
+        }
+        l += rs;
+        // the previous PV has finished reading the P tile
+        if (j > 0) {
+          bool pok = mbar_wait(pv_done, (J + j - 1) & 1, abort_flag, p.status);
+          if (!__all_sync(0xffffffffu, pok)) {
+            ok = false;
+            break;
+          }
+        } else if (J > 0) {
+          // first block of a unit: the previous unit's last PV read the P tile
+          bool pok = mbar_wait(pv_done, (J - 1) & 1, abort_flag, p.status);
+          if (!__all_sync(0xffffffffu, pok)) {
+            ok = false;
+            break;
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < TK / 8; ++c) {  // 16-byte chunk c = keys 8c..8c+7
+          const int half = c >> 3, cc = c & 7;
+          uint4* dst = reinterpret_cast<uint4*>(sP + half * C::HALF_TILE + r * 128 + ((cc ^ (r & 7)) << 4));
+          *dst = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+        if (key0 + TK > key_end) {
+          // keys past key_end may hold uninitialised memory: zero their V rows
+          const int stage = (J + j) % NSTAGE;
+          uint8_t* sv_base = sKV + stage * C::STAGE_BYTES + C::KV_BYTES;
+          const int first = key_end - key0;
+          const int n16 = (TK - first) * C::HALVES * 8;
+          for (int i = r; i < n16; i += 128) {
+            const int per = C::HALVES * 8;
+            const int key = first + i / per, rem = i % per, hf = rem >> 3, cc = rem & 7;
+            *reinterpret_cast<uint4*>(sv_base + hf * C::HALF_TILE + key * 128 + ((cc ^ (key & 7)) << 4)) =
+                make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+      }
+      if (!ok) break;
+      J += w.nblk;
+      // epilogue: the unit's last PV block is complete -> O / l
+      bool pok = mbar_wait(pv_done, (J - 1) & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, pok)) break;
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* orow = p.out + static_cast<size_t>(w.row0 + r) * p.n_q * D + w.head * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + C::COL_O + c * 32, ov);
+        tmem_ld_wait();
+        if (r < w.nrows) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t q4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              q4[e] = pack_bf16x2(__uint_as_float(ov[8 * i + 2 * e]) * inv, __uint_as_float(ov[8 * i + 2 * e + 1]) * inv);
+            dst[i] = make_uint4(q4[0], q4[1], q4[2], q4[3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_empty);
+      ++nunit;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+hb_status chunk_tc_launch(const DeviceCtx& ctx, const void* q, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                          const hb_device_plan& plan, const hb_layer_dims& dm, int num_pages, int max_kv_len,
+                          void* out, int* work_counter, cudaStream_t stream) {
+  CUtensorMap tmQ;
+  hb_status st = encode_tmap_q3d(&tmQ, q, plan.n_rows, dm.n_q, dm.d_head);
+  if (st != HB_OK) return st;
+  TcParams p;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.q_start = plan.seq_q_start;
+  p.kv_len = plan.seq_kv_len;
+  p.block_table = plan.block_table;
+  p.S = plan.n_seqs;
+  p.T = plan.n_rows;
+  p.max_pages = plan.max_pages;
+  p.num_pages = num_pages;
+  p.n_q = dm.n_q;
+  p.n_kv = dm.n_kv;
+  p.grp = dm.n_q / dm.n_kv;
+  p.max_kv_len = max_kv_len;
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(dm.d_head)));
+  p.work_counter = work_counter;
+  p.status = ctx.status;
+  static bool attr_set[2][64] = {};
+  const int di = dm.d_head == 128 ? 1 : 0;
+  if (!attr_set[di][ctx.device]) {
+    st = dm.d_head == 128
+             ? cuda_status(cudaFuncSetAttribute(chunk_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                TC<128>::SMEM),
+                           "cudaFuncSetAttribute(chunk_tc)")
+             : cuda_status(cudaFuncSetAttribute(chunk_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                TC<64>::SMEM),
+                           "cudaFuncSetAttribute(chunk_tc)");
+    if (st != HB_OK) return st;
+    attr_set[di][ctx.device] = true;
+  }
+  if (dm.d_head == 128)
+    chunk_tc_kernel<128><<<ctx.num_sms, kThreads, TC<128>::SMEM, stream>>>(tmQ, tmK, tmV, p);
+  else
+    chunk_tc_kernel<64><<<ctx.num_sms, kThreads, TC<64>::SMEM, stream>>>(tmQ, tmK, tmV, p);
+  return launch_status("chunk_tc_kernel launch");
+}
+
+}  // namespace hb

@@ -66,24 +66,28 @@ hb_status device_context(DeviceCtx* ctx) {
   return HB_OK;
 }
 
+static hb_status resolve_encode() {
+  if (g_encode != nullptr) return HB_OK;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_encode != nullptr) return HB_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  hb_status st =
+      cuda_status(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q),
+                  "cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)");
+  if (st != HB_OK) return st;
+  if (q != cudaDriverEntryPointSuccess || fn == nullptr) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return HB_ERR_UNSUPPORTED;
+  }
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return HB_OK;
+}
+
 hb_status encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
-  if (g_encode == nullptr) {
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (g_encode == nullptr) {
-      void* fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      hb_status st = cuda_status(
-          cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q),
-          "cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)");
-      if (st != HB_OK) return st;
-      if (q != cudaDriverEntryPointSuccess || fn == nullptr) {
-        set_error("cuTensorMapEncodeTiled is not available from the driver");
-        return HB_ERR_UNSUPPORTED;
-      }
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-  }
+  hb_status st = resolve_encode();
+  if (st != HB_OK) return st;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_stride_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
@@ -95,6 +99,25 @@ hb_status encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uin
   if (r != CUDA_SUCCESS) {
     set_error("cuTensorMapEncodeTiled failed (%d): dims %llu x %llu, box %u x %u", static_cast<int>(r),
               static_cast<unsigned long long>(inner), static_cast<unsigned long long>(outer), box_inner, box_outer);
+    return HB_ERR_INVALID_ARG;
+  }
+  return HB_OK;
+}
+
+// 3-D map over q [T][n_q][d_head] bf16: box of 64 dims x 1 head x 128 tokens,
+// 128-byte swizzle (one K-major half tile of a 128-row attention unit).
+hb_status encode_tmap_q3d(CUtensorMap* map, const void* q, int T, int n_q, int d_head) {
+  hb_status st = resolve_encode();
+  if (st != HB_OK) return st;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d_head), static_cast<cuuint64_t>(n_q), static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d_head) * 2, static_cast<cuuint64_t>(n_q) * d_head * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (res != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled (q, 3-D) failed (%d)", static_cast<int>(res));
     return HB_ERR_INVALID_ARG;
   }
   return HB_OK;
