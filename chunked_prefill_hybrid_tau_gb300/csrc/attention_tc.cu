@@ -10,18 +10,23 @@
 // read through the block table.  Persistent CTAs take units from a global
 // counter, heaviest (latest) tiles first.
 //
-// Warp roles (192 threads, one CTA per SM):
-//   warp 0   TMA producer: the unit's Q tile (3-D box over [T][n_q][D]) and,
-//            per block, 8 pages of K and of V (16 keys x 64 dims per box, 128-
-//            byte swizzle) into a 2-stage ring;
-//   warp 1   MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM S
-//            buffers (K-major operands), then O += P_j V_j with P from shared
-//            memory (K-major) and V as an MN-major operand;
-//   warps 2-5 softmax, one query row per thread: tcgen05.ld of the S row,
-//            causal mask, online softmax in base 2 with a lazily updated
-//            maximum (O in TMEM is rescaled only when a row's maximum grows by
-//            more than 2^8), P written as bf16 into shared memory; finally
-//            O / l from TMEM to global memory.
+// Warp roles (352 threads, one CTA per SM):
+//   warps 0, 10  TMA producers: warp 0 loads the unit's Q tile (3-D box over
+//            [T][n_q][D]) and each block's 8 K pages into a 2-stage K ring,
+//            warp 10 the V pages into a 2-stage V ring (16 keys x 64 dims per
+//            box, 128-byte swizzle).  A K stage is released when its S block
+//            is computed, a V stage when its PV block is;
+//   warp 1   MMA issuer (one thread), issuing whichever is ready first:
+//            S_j = Q K_j^T into one of two TMEM S buffers (K-major operands),
+//            or O += P_j V_j with P from shared memory (K-major) and V as an
+//            MN-major operand;
+//   warps 2-9 softmax, two threads per query row (warps 2-5 take keys 0..63
+//            of a block, warps 6-9 keys 64..127; the halves exchange the row
+//            maximum once per block): tcgen05.ld of the S half row, causal
+//            mask, online softmax in base 2 with a lazily updated maximum (O in
+//            TMEM is rescaled only when a row's maximum grows by more than 2^8),
+//            P written as bf16 into shared memory; finally O / l from TMEM to
+//            global memory, each thread its half of the head dimension.
 // Every wait is bounded; an expired wait sets the status word and unwinds.
 #include <cuda_bf16.h>
 
@@ -37,7 +42,9 @@ constexpr int TQ = 128;           // query rows per unit (MMA M)
 constexpr int TK = 128;           // keys per block (MMA N of S, K of PV)
 constexpr int NSTAGE = 2;
 constexpr int MAX_SEQS = 1024;
-constexpr int kThreads = 192;
+constexpr int kSoftWarps = 8;                // two threads per query row (column halves)
+constexpr int kVWarp = 2 + kSoftWarps;        // the V producer
+constexpr int kThreads = 32 * (kVWarp + 1);
 constexpr float kRescale = 8.0f;  // log2 growth of a row maximum that forces an O rescale
 
 template <int D>
@@ -46,14 +53,16 @@ struct TC {
   static constexpr int HALF_TILE = 128 * 128;            // 128 rows x 128 bytes
   static constexpr int Q_BYTES = HALVES * HALF_TILE;     // Q tile
   static constexpr int KV_BYTES = HALVES * HALF_TILE;    // K (or V) block of 128 keys
-  static constexpr int STAGE_BYTES = 2 * KV_BYTES;
   static constexpr int P_BYTES = 2 * HALF_TILE;          // 128 rows x 128 keys bf16
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = Q_BYTES;
-  static constexpr int OFF_P = OFF_KV + NSTAGE * STAGE_BYTES;
+  static constexpr int OFF_K = Q_BYTES;                  // K ring [NSTAGE]
+  static constexpr int OFF_V = OFF_K + NSTAGE * KV_BYTES;  // V ring [NSTAGE]
+  static constexpr int OFF_P = OFF_V + NSTAGE * KV_BYTES;
   static constexpr int OFF_BAR = OFF_P + P_BYTES;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int OFF_PRE = OFF_BAR + BAR_BYTES;
+  static constexpr int OFF_XCH = OFF_BAR + BAR_BYTES;    // row maxima / sums exchanged by the two halves
+  static constexpr int XCH_BYTES = (2 * 2 * 128 + 2 * 128) * 4;
+  static constexpr int OFF_PRE = OFF_XCH + XCH_BYTES;
   static constexpr int SMEM = OFF_PRE + (MAX_SEQS + 1) * 4 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;             // S0 | S1 | O
   static constexpr uint32_t COL_O = 256;
@@ -145,11 +154,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + C::OFF_Q;
-  uint8_t* sKV = smem + C::OFF_KV;
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
   uint8_t* sP = smem + C::OFF_P;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* kv_full = bar;                  // [NSTAGE]
-  uint64_t* kv_empty = bar + 2;             // [NSTAGE]
+  uint64_t* k_full = bar;                   // [NSTAGE]
+  uint64_t* k_empty = bar + 2;              // [NSTAGE]
   uint64_t* q_full = bar + 4;
   uint64_t* q_empty = bar + 5;
   uint64_t* s_full = bar + 6;               // [2]
@@ -160,9 +170,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* uq_full = bar + 13;             // [2]
   uint64_t* uq_empty = bar + 15;            // [2]
   uint64_t* drain = bar + 17;
-  int* uq = reinterpret_cast<int*>(bar + 18);  // [2]
+  uint64_t* xbar = bar + 18;                // [2] row maxima exchanged (block parity)
+  uint64_t* xsbar = bar + 20;               // row sums exchanged (once per unit)
+  uint64_t* v_full = bar + 21;              // [NSTAGE]
+  uint64_t* v_empty = bar + 23;             // [NSTAGE]
+  int* uq = reinterpret_cast<int*>(bar + 25);  // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(uq + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* xmax = reinterpret_cast<float*>(smem + C::OFF_XCH);  // [2 parity][2 half][128 rows]
+  float* xsum = xmax + 2 * 2 * 128;                             // [2 half][128 rows]
   int* pre = reinterpret_cast<int*>(smem + C::OFF_PRE);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -180,20 +196,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 0) {
     for (int i = 0; i < NSTAGE; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
     }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 4);
+      mbar_init(&s_empty[i], kSoftWarps);
       mbar_init(&uq_full[i], 1);
-      mbar_init(&uq_empty[i], 5);
+      mbar_init(&uq_empty[i], 2 + kSoftWarps);
     }
-    mbar_init(p_full, 4);
+    mbar_init(p_full, kSoftWarps);
     mbar_init(pv_done, 1);
-    mbar_init(o_empty, 4);
+    mbar_init(o_empty, kSoftWarps);
+    mbar_init(&xbar[0], kSoftWarps);
+    mbar_init(&xbar[1], kSoftWarps);
+    mbar_init(xsbar, kSoftWarps);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -212,58 +233,89 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == kVWarp) {
+    // ------------------------------------------------------------ producers
+    // warp 0: unit queue, Q and the K ring; warp kVWarp: the V ring
     if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
+      const bool kside = warp == 0;
+      if (kside) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+      } else {
+        tma_prefetch_desc(&tmV);
+      }
+      const CUtensorMap* tm = kside ? &tmK : &tmV;
+      uint8_t* ring = kside ? sK : sV;
+      uint64_t* full = kside ? k_full : v_full;
+      uint64_t* empty = kside ? k_empty : v_empty;
       int qs = 0, stage = 0, nunit = 0;
       uint32_t qph = 0, kph = 0;
       uint32_t pending = 0, armed = 0;
       bool ok = true;
       while (ok) {
-        if (!mbar_wait(&uq_empty[qs], qph ^ 1u, abort_flag, p.status)) break;
-        const int u = atomicAdd(p.work_counter, 1);
-        uq[qs] = u;
-        mbar_arrive(&uq_full[qs]);
+        int u;
+        if (kside) {
+          if (!mbar_wait(&uq_empty[qs], qph ^ 1u, abort_flag, p.status)) break;
+          u = atomicAdd(p.work_counter, 1);
+          uq[qs] = u;
+          mbar_arrive(&uq_full[qs]);
+        } else {
+          if (!mbar_wait(&uq_full[qs], qph, abort_flag, p.status)) break;
+          u = uq[qs];
+          mbar_arrive(&uq_empty[qs]);
+        }
         if (++qs == 2) {
           qs = 0;
           qph ^= 1u;
         }
         const TcUnit w = tc_unit(p, pre, u);
         if (!w.valid) break;
-        // Q tile (the MMA of the previous unit's last S block has read it)
-        if (!mbar_wait(q_empty, (nunit & 1) ^ 1u, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+        if (kside) {
+          // Q tile (the last S block of the previous unit has read it)
+          if (!mbar_wait(q_empty, (nunit & 1) ^ 1u, abort_flag, p.status)) break;
+          mbar_arrive_expect_tx(q_full, C::Q_BYTES);
 #pragma unroll
-        for (int hf = 0; hf < C::HALVES; ++hf) tma_load_3d(sQ + hf * C::HALF_TILE, &tmQ, q_full, hf * 64, w.head, w.row0);
+          for (int hf = 0; hf < C::HALVES; ++hf)
+            tma_load_3d(sQ + hf * C::HALF_TILE, &tmQ, q_full, hf * 64, w.head, w.row0);
+        }
         ++nunit;
         const int g = w.head / p.grp;
         const int* bt = p.block_table + static_cast<size_t>(w.seq) * p.max_pages;
         const int key_end = w.pos0 + w.nrows;
+        // page ids of a block: 8 independent loads, fetched one block ahead so
+        // their latency overlaps the wait for a free stage
+        auto fetch_pages = [&](int j, int (&pg_ids)[8]) {
+          const int npg = min(8, (key_end - j * TK + 15) / 16);
+#pragma unroll
+          for (int pg = 0; pg < 8; ++pg) pg_ids[pg] = pg < npg ? __ldg(bt + j * 8 + pg) : 0;
+        };
+        int nxt[8];
+        fetch_pages(0, nxt);
         for (int j = 0; j < w.nblk; ++j) {
-          if (!mbar_wait(&kv_empty[stage], kph ^ 1u, abort_flag, p.status)) {
+          int cur[8];
+#pragma unroll
+          for (int pg = 0; pg < 8; ++pg) cur[pg] = nxt[pg];
+          if (j + 1 < w.nblk) fetch_pages(j + 1, nxt);
+          if (!mbar_wait(&empty[stage], kph ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
           }
           const int npg = min(8, (key_end - j * TK + 15) / 16);
           pending |= 1u << stage;
           armed = (armed & ~(1u << stage)) | (kph << stage);
-          mbar_arrive_expect_tx(&kv_full[stage], npg * 2 * C::HALVES * 2048);
-          uint8_t* sk = sKV + stage * C::STAGE_BYTES;
-          for (int pg = 0; pg < npg; ++pg) {
-            int page = bt[j * 8 + pg];
+          mbar_arrive_expect_tx(&full[stage], npg * C::HALVES * 2048);
+          uint8_t* dst = ring + stage * C::KV_BYTES;
+#pragma unroll
+          for (int pg = 0; pg < 8; ++pg) {
+            if (pg >= npg) break;
+            int page = cur[pg];
             if (page < 0 || page >= p.num_pages) {
               flag_error(p.status, kStatusIndex);
               page = 0;
             }
             const int y = (page * p.n_kv + g) * 16;
 #pragma unroll
-            for (int hf = 0; hf < C::HALVES; ++hf) {
-              tma_load_2d(sk + hf * C::HALF_TILE + pg * 2048, &tmK, &kv_full[stage], hf * 64, y);
-              tma_load_2d(sk + C::KV_BYTES + hf * C::HALF_TILE + pg * 2048, &tmV, &kv_full[stage], hf * 64, y);
-            }
+            for (int hf = 0; hf < C::HALVES; ++hf) tma_load_2d(dst + hf * C::HALF_TILE + pg * 2048, tm, &full[stage], hf * 64, y);
           }
           if (++stage == NSTAGE) {
             stage = 0;
@@ -273,15 +325,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok)
         for (int s = 0; s < NSTAGE; ++s)
-          if (pending & (1u << s)) mbar_drain(&kv_full[s], (armed >> s) & 1u);
+          if (pending & (1u << s)) mbar_drain(&full[s], (armed >> s) & 1u);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const bool leader = lane == 0;
     constexpr uint32_t idS = idesc_bf16_f32(TQ, TK);
     constexpr uint32_t idPV = idesc_bf16_f32(TQ, D) | (1u << 16);  // B (V) is MN-major
-    int qs = 0, stage = 0, J = 0, nunit = 0;
-    uint32_t qph = 0, kph = 0;
+    int qs = 0, J = 0, nunit = 0;
+    uint32_t qph = 0;
     bool ok = true;
     while (ok) {
       bool got = mbar_wait(&uq_full[qs], qph, abort_flag, p.status);
@@ -297,50 +349,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!w.valid) break;
       if (leader) {
         ok = mbar_wait(q_full, nunit & 1, abort_flag, p.status);
-        // O of the previous unit has been read by the epilogue
-        ok = ok && mbar_wait(o_empty, (nunit & 1) ^ 1u, abort_flag, p.status);
-        tc_fence_after();
         const uint32_t q_addr = smem_u32(sQ);
-        int pst = 0;  // stage of block j - 1
-        for (int j = 0; j <= w.nblk && ok; ++j) {
-          if (j < w.nblk) {
-            const int b = (J + j) & 1;
-            ok = mbar_wait(&kv_full[stage], kph, abort_flag, p.status) &&
-                 mbar_wait(&s_empty[b], (((J + j) >> 1) & 1) ^ 1u, abort_flag, p.status);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t k_addr = smem_u32(sKV + stage * C::STAGE_BYTES);
+        const uint32_t p_addr = smem_u32(sP);
+        // S_js and PV_jp are issued in whatever order their inputs arrive
+        int js = 0, jp = 0;
+        bool o_free = false;
+        uint64_t t0 = globaltimer();
+        while (ok && jp < w.nblk) {
+          bool progressed = false;
+          if (js < w.nblk) {
+            const int gk = J + js, b = gk & 1, st = gk % NSTAGE;
+            if (mbar_test(&k_full[st], (gk / NSTAGE) & 1) && mbar_test(&s_empty[b], ((gk >> 1) & 1) ^ 1u)) {
+              tc_fence_after();
+              const uint32_t k_addr = smem_u32(sK + st * C::KV_BYTES);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * C::HALF_TILE + (kk & 3) * 32;
-              mma_bf16(tmem + b * TK, smem_desc_sw128(q_addr + off), smem_desc_sw128(k_addr + off), idS,
-                       kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * C::HALF_TILE + (kk & 3) * 32;
+                mma_bf16(tmem + b * TK, smem_desc_sw128(q_addr + off), smem_desc_sw128(k_addr + off), idS,
+                         kk > 0 ? 1u : 0u);
+              }
+              mma_commit(&s_full[b]);
+              mma_commit(&k_empty[st]);
+              if (js == w.nblk - 1) mma_commit(q_empty);
+              ++js;
+              progressed = true;
             }
-            mma_commit(&s_full[b]);
-            if (j == w.nblk - 1) mma_commit(q_empty);
           }
-          if (j > 0) {
-            // O += P_{j-1} V_{j-1} once the softmax has written P_{j-1}
-            ok = mbar_wait(p_full, (J + j - 1) & 1, abort_flag, p.status);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t p_addr = smem_u32(sP);
-            const uint32_t v_addr = smem_u32(sKV + pst * C::STAGE_BYTES + C::KV_BYTES);
+          if (jp < js) {
+            const int gv = J + jp, st = gv % NSTAGE;
+            // O of the previous unit has been read by the epilogue before the first PV
+            if (!o_free) o_free = mbar_test(o_empty, (nunit & 1) ^ 1u);
+            if (o_free && mbar_test(p_full, gv & 1) && mbar_test(&v_full[st], (gv / NSTAGE) & 1)) {
+              tc_fence_after();
+              const uint32_t v_addr = smem_u32(sV + st * C::KV_BYTES);
 #pragma unroll
-            for (int kk = 0; kk < TK / 16; ++kk) {
-              const uint64_t a = smem_desc_sw128(p_addr + (kk >> 2) * C::HALF_TILE + (kk & 3) * 32);
-              const uint64_t bdesc = smem_desc_sw128_mn(v_addr + kk * 2048, C::HALF_TILE, 1024);
-              mma_bf16(tmem + C::COL_O, a, bdesc, idPV, (j > 1 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < TK / 16; ++kk) {
+                const uint64_t a = smem_desc_sw128(p_addr + (kk >> 2) * C::HALF_TILE + (kk & 3) * 32);
+                const uint64_t bdesc = smem_desc_sw128_mn(v_addr + kk * 2048, C::HALF_TILE, 1024);
+                mma_bf16(tmem + C::COL_O, a, bdesc, idPV, (jp > 0 || kk > 0) ? 1u : 0u);
+              }
+              mma_commit(&v_empty[st]);
+              mma_commit(pv_done);
+              ++jp;
+              progressed = true;
             }
-            mma_commit(&kv_empty[pst]);
-            mma_commit(pv_done);
           }
-          if (j < w.nblk) {
-            pst = stage;
-            if (++stage == NSTAGE) {
-              stage = 0;
-              kph ^= 1u;
-            }
+          if (progressed) {
+            t0 = globaltimer();
+          } else if (*abort_flag) {
+            ok = false;
+          } else if (globaltimer() - t0 > kWaitTimeoutNs) {
+            flag_error(p.status, kStatusTimeout);
+            *abort_flag = 1;
+            ok = false;
           }
         }
         J += w.nblk;
@@ -349,8 +410,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       J = __shfl_sync(0xffffffffu, J, 0);
       nunit = __shfl_sync(0xffffffffu, nunit, 0);
-      stage = __shfl_sync(0xffffffffu, stage, 0);
-      kph = __shfl_sync(0xffffffffu, kph, 0);
     }
     if (leader && !ok) {
       mma_commit(drain);
@@ -358,9 +417,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
+    constexpr int HK = TK / 2;        // keys per thread per block
+    constexpr int HD = D / 2;         // head dims per thread in O
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;  // 0: keys 0..63 / dims 0..D/2-1, 1: the rest
     const int r = quarter * 32 + lane;  // query row of this thread within the tile
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const int stid = (warp - 2) * 32 + lane;  // 0..255 among the softmax threads
     int qs = 0, J = 0, nunit = 0;
     uint32_t qph = 0;
     while (true) {
@@ -387,23 +450,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        uint32_t sv[TK];
+        uint32_t sv[HK];
 #pragma unroll
-        for (int c = 0; c < TK / 32; ++c) tmem_ld_32x32b_x32(tmem + lane_base + b * TK + c * 32,
-                                                            *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
+        for (int c = 0; c < HK / 32; ++c)
+          tmem_ld_32x32b_x32(tmem + lane_base + b * TK + half * HK + c * 32,
+                             *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_empty[b]);
-        // mask and scale (base 2), row maximum
-        const int key0 = j * TK;
+        // mask and scale (base 2), this half's row maximum, then the full row's
+        const int key0 = j * TK + half * HK;
         float mx = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < TK; ++c) {
+        for (int c = 0; c < HK; ++c) {
           const float v = key0 + c <= lim ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
           sv[c] = __float_as_uint(v);
           mx = fmaxf(mx, v);
         }
+        // exchange with the other half of the row (mbarrier per block parity;
+        // a phase cannot run ahead: it needs every softmax warp's arrival)
+        float* xm = xmax + ((J + j) & 1) * 256;
+        xm[half * 128 + r] = mx;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xbar[(J + j) & 1]);
+        bool xok = mbar_wait(&xbar[(J + j) & 1], ((J + j) >> 1) & 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, xok)) {
+          ok = false;
+          break;
+        }
+        mx = fmaxf(mx, xm[(half ^ 1) * 128 + r]);
         // lazily raise the maximum; rescale O (in TMEM) and l when it moves
         const bool raise = mx > m_used + kRescale;
         const float m_new = raise ? mx : m_used;
@@ -417,58 +493,57 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < HD / 32; ++c) {
             uint32_t ov[32];
-            tmem_ld_32x32b_x32(tmem + lane_base + C::COL_O + c * 32, ov);
+            const uint32_t ta = tmem + lane_base + C::COL_O + half * HD + c * 32;
+            tmem_ld_32x32b_x32(ta, ov);
             tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st_32x32b_x32(tmem + lane_base + C::COL_O + c * 32, ov);
+            tmem_st_32x32b_x32(ta, ov);
           }
           tmem_st_wait();
         }
         m_used = m_new;
         l *= alpha;
-        // P = 2^(s - m) as bf16, written as row r of the K-major P tile
+        // P = 2^(s - m) as bf16: this thread's 64 keys are row r of P half `half`
         float rs = 0.f;
-        uint32_t pk[TK / 2];
+        uint32_t pk[HK / 2];
 #pragma unroll
-        for (int c = 0; c < TK / 2; ++c) {
+        for (int c = 0; c < HK / 2; ++c) {
           const float a0 = exp2f(__uint_as_float(sv[2 * c]) - m_used);
           const float a1 = exp2f(__uint_as_float(sv[2 * c + 1]) - m_used);
           rs += a0 + a1;
           pk[c] = pack_bf16x2(a0, a1);
         }
         l += rs;
-        // the previous PV has finished reading the P tile
-        if (j > 0) {
+        // the previous PV block has finished reading the P tile
+        if (J + j > 0) {
           bool pok = mbar_wait(pv_done, (J + j - 1) & 1, abort_flag, p.status);
           if (!__all_sync(0xffffffffu, pok)) {
             ok = false;
             break;
           }
-        } else if (J > 0) {
-          // first block of a unit: the previous unit's last PV read the P tile
-          bool pok = mbar_wait(pv_done, (J - 1) & 1, abort_flag, p.status);
-          if (!__all_sync(0xffffffffu, pok)) {
+        }
+        uint8_t* prow = sP + half * C::HALF_TILE + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)  // 16-byte chunk c = keys 8c..8c+7 of this half
+          *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        if (j * TK + TK > key_end) {
+          // keys past key_end may hold uninitialised memory: zero their V rows
+          // once the V block has landed (its stage cannot be refilled before
+          // this block's PV, which waits for p_full below)
+          const int gv = J + j, stage = gv % NSTAGE;
+          bool vok = mbar_wait(&v_full[stage], (gv / NSTAGE) & 1, abort_flag, p.status);
+          if (!__all_sync(0xffffffffu, vok)) {
             ok = false;
             break;
           }
-        }
-#pragma unroll
-        for (int c = 0; c < TK / 8; ++c) {  // 16-byte chunk c = keys 8c..8c+7
-          const int half = c >> 3, cc = c & 7;
-          uint4* dst = reinterpret_cast<uint4*>(sP + half * C::HALF_TILE + r * 128 + ((cc ^ (r & 7)) << 4));
-          *dst = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        }
-        if (key0 + TK > key_end) {
-          // keys past key_end may hold uninitialised memory: zero their V rows
-          const int stage = (J + j) % NSTAGE;
-          uint8_t* sv_base = sKV + stage * C::STAGE_BYTES + C::KV_BYTES;
-          const int first = key_end - key0;
-          const int n16 = (TK - first) * C::HALVES * 8;
-          for (int i = r; i < n16; i += 128) {
-            const int per = C::HALVES * 8;
+          uint8_t* sv_base = sV + stage * C::KV_BYTES;
+          const int first = key_end - j * TK;
+          constexpr int per = C::HALVES * 8;
+          for (int i = stid; i < (TK - first) * per; i += 32 * kSoftWarps) {
             const int key = first + i / per, rem = i % per, hf = rem >> 3, cc = rem & 7;
             *reinterpret_cast<uint4*>(sv_base + hf * C::HALF_TILE + key * 128 + ((cc ^ (key & 7)) << 4)) =
                 make_uint4(0, 0, 0, 0);
@@ -481,16 +556,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       J += w.nblk;
-      // epilogue: the unit's last PV block is complete -> O / l
+      // epilogue: row sum of both halves; the unit's last PV block is complete -> O / l
+      xsum[half * 128 + r] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xsbar);
+      bool xok = mbar_wait(xsbar, nunit & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, xok)) break;
+      l += xsum[(half ^ 1) * 128 + r];
       bool pok = mbar_wait(pv_done, (J - 1) & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, pok)) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = p.out + static_cast<size_t>(w.row0 + r) * p.n_q * D + w.head * D;
+      __nv_bfloat16* orow = p.out + static_cast<size_t>(w.row0 + r) * p.n_q * D + w.head * D + half * HD;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < HD / 32; ++c) {
         uint32_t ov[32];
-        tmem_ld_32x32b_x32(tmem + lane_base + C::COL_O + c * 32, ov);
+        tmem_ld_32x32b_x32(tmem + lane_base + C::COL_O + half * HD + c * 32, ov);
         tmem_ld_wait();
         if (r < w.nrows) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
