@@ -652,20 +652,22 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
     }
     __syncwarp();
 
-    auto issue = [&](int b) {  // lane 0: page b of this unit into slot b % DR
+    // page b of this unit into slot b % DR: lane 0 arms the slot, lanes
+    // 0 .. 2*(D/64)-1 then issue one TMA box each (K or V, one 64-dim half)
+    auto issue = [&](int b) {
       const int slot = b % DR;
-      const int page = btc[b];
-      const int y = (page * p.n_kv + g) * 16;
       uint8_t* dst = ring + slot * STAGE_BYTES;
-      mbar_arrive_expect_tx(&full[slot], STAGE_BYTES);
-#pragma unroll
-      for (int hf = 0; hf < D / 64; ++hf) {
-        tma_load_2d(dst + hf * HALF_BYTES, &tmK, &full[slot], hf * 64, y);
-        tma_load_2d(dst + PAGE_BYTES + hf * HALF_BYTES, &tmV, &full[slot], hf * 64, y);
+      if (lane == 0) mbar_arrive_expect_tx(&full[slot], STAGE_BYTES);
+      __syncwarp();
+      if (lane < 2 * (D / 64)) {
+        const int page = btc[b];
+        const int y = (page * p.n_kv + g) * 16;
+        const int hf = lane >> 1;
+        const bool is_v = lane & 1;
+        tma_load_2d(dst + (is_v ? PAGE_BYTES : 0) + hf * HALF_BYTES, is_v ? &tmV : &tmK, &full[slot], hf * 64, y);
       }
     };
-    if (lane == 0)
-      for (int b = 0; b < min(DR, npages); ++b) issue(b);
+    for (int b = 0; b < min(DR, npages); ++b) issue(b);
 
     // q rows of this kv head's group (rows >= grp are zero padding)
     const bool oka = ga < p.grp, okb = ga + 8 < p.grp;
@@ -714,7 +716,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
       // zeroing writes of a tail page must be ordered before the next TMA write.
       if (tail) fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0 && b + DR < npages) issue(b + DR);
+      if (b + DR < npages) issue(b + DR);
     }
     if (!ok) {
       // unwind: let this warp's copies in flight land (bounded) before exiting

@@ -235,98 +235,113 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 || warp == kVWarp) {
     // ------------------------------------------------------------ producers
-    // warp 0: unit queue, Q and the K ring; warp kVWarp: the V ring
+    // warp 0: unit queue, Q and the K ring; warp kVWarp: the V ring.  Lane 0
+    // arms each stage; the warp's lanes then issue one TMA box each (page
+    // lane / HALVES, half lane % HALVES), so a block's 8 pages go out at once.
+    const bool kside = warp == 0;
     if (lane == 0) {
-      const bool kside = warp == 0;
       if (kside) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
       } else {
         tma_prefetch_desc(&tmV);
       }
-      const CUtensorMap* tm = kside ? &tmK : &tmV;
-      uint8_t* ring = kside ? sK : sV;
-      uint64_t* full = kside ? k_full : v_full;
-      uint64_t* empty = kside ? k_empty : v_empty;
-      int qs = 0, stage = 0, nunit = 0;
-      uint32_t qph = 0, kph = 0;
-      uint32_t pending = 0, armed = 0;
-      bool ok = true;
-      while (ok) {
-        int u;
+    }
+    const CUtensorMap* tm = kside ? &tmK : &tmV;
+    uint8_t* ring = kside ? sK : sV;
+    uint64_t* full = kside ? k_full : v_full;
+    uint64_t* empty = kside ? k_empty : v_empty;
+    int qs = 0, stage = 0, nunit = 0;
+    uint32_t qph = 0, kph = 0;
+    uint32_t pending = 0, armed = 0;
+    bool ok = true;
+    while (ok) {
+      int u = 0;
+      bool got = true;
+      if (lane == 0) {
         if (kside) {
-          if (!mbar_wait(&uq_empty[qs], qph ^ 1u, abort_flag, p.status)) break;
-          u = atomicAdd(p.work_counter, 1);
-          uq[qs] = u;
-          mbar_arrive(&uq_full[qs]);
+          got = mbar_wait(&uq_empty[qs], qph ^ 1u, abort_flag, p.status);
+          if (got) {
+            u = atomicAdd(p.work_counter, 1);
+            uq[qs] = u;
+            mbar_arrive(&uq_full[qs]);
+          }
         } else {
-          if (!mbar_wait(&uq_full[qs], qph, abort_flag, p.status)) break;
-          u = uq[qs];
-          mbar_arrive(&uq_empty[qs]);
+          got = mbar_wait(&uq_full[qs], qph, abort_flag, p.status);
+          if (got) {
+            u = uq[qs];
+            mbar_arrive(&uq_empty[qs]);
+          }
         }
-        if (++qs == 2) {
-          qs = 0;
-          qph ^= 1u;
-        }
-        const TcUnit w = tc_unit(p, pre, u);
-        if (!w.valid) break;
-        if (kside) {
-          // Q tile (the last S block of the previous unit has read it)
-          if (!mbar_wait(q_empty, (nunit & 1) ^ 1u, abort_flag, p.status)) break;
+      }
+      if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) break;
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (++qs == 2) {
+        qs = 0;
+        qph ^= 1u;
+      }
+      const TcUnit w = tc_unit(p, pre, u);
+      if (!w.valid) break;
+      if (kside && lane == 0) {
+        // Q tile (the last S block of the previous unit has read it)
+        ok = mbar_wait(q_empty, (nunit & 1) ^ 1u, abort_flag, p.status);
+        if (ok) {
           mbar_arrive_expect_tx(q_full, C::Q_BYTES);
 #pragma unroll
           for (int hf = 0; hf < C::HALVES; ++hf)
             tma_load_3d(sQ + hf * C::HALF_TILE, &tmQ, q_full, hf * 64, w.head, w.row0);
         }
-        ++nunit;
-        const int g = w.head / p.grp;
-        const int* bt = p.block_table + static_cast<size_t>(w.seq) * p.max_pages;
-        const int key_end = w.pos0 + w.nrows;
-        // page ids of a block: 8 independent loads, fetched one block ahead so
-        // their latency overlaps the wait for a free stage
-        auto fetch_pages = [&](int j, int (&pg_ids)[8]) {
-          const int npg = min(8, (key_end - j * TK + 15) / 16);
-#pragma unroll
-          for (int pg = 0; pg < 8; ++pg) pg_ids[pg] = pg < npg ? __ldg(bt + j * 8 + pg) : 0;
-        };
-        int nxt[8];
-        fetch_pages(0, nxt);
-        for (int j = 0; j < w.nblk; ++j) {
-          int cur[8];
-#pragma unroll
-          for (int pg = 0; pg < 8; ++pg) cur[pg] = nxt[pg];
-          if (j + 1 < w.nblk) fetch_pages(j + 1, nxt);
-          if (!mbar_wait(&empty[stage], kph ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          const int npg = min(8, (key_end - j * TK + 15) / 16);
-          pending |= 1u << stage;
-          armed = (armed & ~(1u << stage)) | (kph << stage);
-          mbar_arrive_expect_tx(&full[stage], npg * C::HALVES * 2048);
-          uint8_t* dst = ring + stage * C::KV_BYTES;
-#pragma unroll
-          for (int pg = 0; pg < 8; ++pg) {
-            if (pg >= npg) break;
-            int page = cur[pg];
-            if (page < 0 || page >= p.num_pages) {
-              flag_error(p.status, kStatusIndex);
-              page = 0;
-            }
-            const int y = (page * p.n_kv + g) * 16;
-#pragma unroll
-            for (int hf = 0; hf < C::HALVES; ++hf) tma_load_2d(dst + hf * C::HALF_TILE + pg * 2048, tm, &full[stage], hf * 64, y);
-          }
-          if (++stage == NSTAGE) {
-            stage = 0;
-            kph ^= 1u;
+      }
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      ++nunit;
+      const int g = w.head / p.grp;
+      const int* bt = p.block_table + static_cast<size_t>(w.seq) * p.max_pages;
+      const int key_end = w.pos0 + w.nrows;
+      const int my_pg = lane / C::HALVES, my_hf = lane % C::HALVES;
+      // this lane's page id of block j, validated (one block ahead)
+      auto fetch_page = [&](int j) {
+        const int npg = min(8, (key_end - j * TK + 15) / 16);
+        int page = 0;
+        if (my_pg < npg) {
+          page = __ldg(bt + j * 8 + my_pg);
+          if (page < 0 || page >= p.num_pages) {
+            flag_error(p.status, kStatusIndex);
+            page = 0;
           }
         }
+        return page;
+      };
+      int nxt = fetch_page(0);
+      for (int j = 0; j < w.nblk; ++j) {
+        const int cur = nxt;
+        if (j + 1 < w.nblk) nxt = fetch_page(j + 1);
+        const int npg = min(8, (key_end - j * TK + 15) / 16);
+        bool eok = true;
+        if (lane == 0) {
+          eok = mbar_wait(&empty[stage], kph ^ 1u, abort_flag, p.status);
+          if (eok) {
+            pending |= 1u << stage;
+            armed = (armed & ~(1u << stage)) | (kph << stage);
+            mbar_arrive_expect_tx(&full[stage], npg * C::HALVES * 2048);
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, eok ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+        if (my_pg < npg) {
+          uint8_t* dst = ring + stage * C::KV_BYTES + my_hf * C::HALF_TILE + my_pg * 2048;
+          tma_load_2d(dst, tm, &full[stage], my_hf * 64, (cur * p.n_kv + g) * 16);
+        }
+        if (++stage == NSTAGE) {
+          stage = 0;
+          kph ^= 1u;
+        }
       }
-      if (!ok)
-        for (int s = 0; s < NSTAGE; ++s)
-          if (pending & (1u << s)) mbar_drain(&full[s], (armed >> s) & 1u);
     }
+    if (!ok && lane == 0)
+      for (int s = 0; s < NSTAGE; ++s)
+        if (pending & (1u << s)) mbar_drain(&full[s], (armed >> s) & 1u);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const bool leader = lane == 0;
