@@ -21,10 +21,25 @@ block without biases:
 
 Everything is computed in `dtype` (float32 by default), with no intermediate
 rounding; inputs are the bf16-representable values the GPU also sees.
+
+Precision variant (storage="bf16"): the same arithmetic in fp32 but with every
+tensor that a bf16 implementation stores rounded to bf16 (round to nearest
+even) where it is stored: xn, qkv, the rotated q and k, the softmax weights P
+fed to the P V product, o, h, hn, the SwiGLU output a and the layer output.
+It quantifies how far bf16 storage alone moves a result from the fp32 one
+(used to bound deep stacks); the default path never rounds.
 """
 from __future__ import annotations
 
 import numpy as np
+
+
+def round_bf16(x):
+    """Round float32 values to bf16 (nearest, ties to even), kept in float32."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).reshape(x.shape)
 
 
 def rmsnorm(x, g, eps, dtype=np.float32):
@@ -70,9 +85,10 @@ def gather_keys(pool, table_row, n_keys, page):
     return pool[pages, :, j % page, :]
 
 
-def attention(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype=np.float32):
+def attention(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype=np.float32, round_p=None):
     """q [T, n_q, d_head] -> o [T, n_q, d_head]; row r of sequence s at
-    position p attends to keys 0..p of s (its block table)."""
+    position p attends to keys 0..p of s (its block table).  round_p, if
+    given, is applied to the softmax weights before the P V product."""
     T, _, d_head = q.shape
     scale = dtype(1.0 / np.sqrt(d_head))
     grp = n_q // n_kv
@@ -87,32 +103,38 @@ def attention(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype=np.float32):
                 sc = (qg @ K[:n_keys, g, :].T) * scale                  # [grp, n_keys]
                 sc = sc - sc.max(axis=1, keepdims=True)
                 w = np.exp(sc)
-                w = w / w.sum(axis=1, keepdims=True)
-                o[r, g * grp:(g + 1) * grp, :] = w @ V[:n_keys, g, :]
+                if round_p is None:
+                    w = w / w.sum(axis=1, keepdims=True)
+                    o[r, g * grp:(g + 1) * grp, :] = w @ V[:n_keys, g, :]
+                else:
+                    o[r, g * grp:(g + 1) * grp, :] = (round_p(w) @ V[:n_keys, g, :]) / w.sum(axis=1, keepdims=True)
     return o
 
 
 def layer_forward(w, dims, plan, x, k_pool, v_pool, cos, sin, dtype=np.float32,
-                  return_parts=False):
+                  return_parts=False, storage=None):
     """One decoder layer over the packed rows of `plan`.  k_pool / v_pool are
-    updated in place with the rows' rotated K and raw V."""
+    updated in place with the rows' rotated K and raw V.  storage="bf16"
+    selects the bf16-storage precision variant (module docstring)."""
     T = len(plan.row_seq)
     nq, nkv, dh = dims.n_q, dims.n_kv, dims.d_head
+    st = round_bf16 if storage == "bf16" else (lambda t: t)
     x = np.asarray(x, dtype)
-    xn = rmsnorm(x, w["g1"], dims.eps, dtype)
-    qkv = xn @ np.asarray(w["w_qkv"], dtype).T
+    xn = st(rmsnorm(x, w["g1"], dims.eps, dtype))
+    qkv = st(xn @ np.asarray(w["w_qkv"], dtype).T)
     q = qkv[:, :nq * dh].reshape(T, nq, dh)
     k = qkv[:, nq * dh:(nq + nkv) * dh].reshape(T, nkv, dh)
     v = qkv[:, (nq + nkv) * dh:].reshape(T, nkv, dh)
     pos = np.asarray(plan.row_pos)
-    q = rope(q, pos, cos, sin, dtype)
-    k = rope(k, pos, cos, sin, dtype)
+    q = st(rope(q, pos, cos, sin, dtype))
+    k = st(rope(k, pos, cos, sin, dtype))
     kv_append(k, v, plan.slot_mapping, k_pool, v_pool, dims.page)
-    o = attention(q, k_pool, v_pool, plan, nq, nkv, dims.page, dtype)
-    h = x + o.reshape(T, nq * dh) @ np.asarray(w["w_o"], dtype).T
-    hn = rmsnorm(h, w["g2"], dims.eps, dtype)
-    a = silu(hn @ np.asarray(w["w_g"], dtype).T) * (hn @ np.asarray(w["w_u"], dtype).T)
-    out = h + a @ np.asarray(w["w_d"], dtype).T
+    o = st(attention(q, k_pool, v_pool, plan, nq, nkv, dims.page, dtype,
+                     round_p=round_bf16 if storage == "bf16" else None))
+    h = st(x + o.reshape(T, nq * dh) @ np.asarray(w["w_o"], dtype).T)
+    hn = st(rmsnorm(h, w["g2"], dims.eps, dtype))
+    a = st(silu(hn @ np.asarray(w["w_g"], dtype).T) * (hn @ np.asarray(w["w_u"], dtype).T))
+    out = st(h + a @ np.asarray(w["w_d"], dtype).T)
     if return_parts:
         return out, dict(xn=xn, qkv=qkv, q=q, k=k, v=v, o=o, h=h, hn=hn, a=a)
     return out

@@ -474,7 +474,7 @@ _ORIG_ATTENTION = ol.attention
 _ORIG_ROPE = ol.rope
 
 
-def _attention_variant(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype, kv_head, n_keys):
+def _attention_variant(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype, kv_head, n_keys, round_p=None):
     """The oracle's attention loop with the head map and key count as parameters."""
     T, _, d_head = q.shape
     o = np.zeros((T, n_q, d_head), dtype)
@@ -491,17 +491,17 @@ def _attention_variant(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype, kv_head,
     return o
 
 
-def _attn_gqa_modulo(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype=np.float32):
+def _attn_gqa_modulo(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype=np.float32, round_p=None):
     return _attention_variant(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype,
                               lambda h, nq, nkv: h % nkv, lambda p, s, r: p.row_pos[r] + 1)
 
 
-def _attn_excludes_self(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype=np.float32):
+def _attn_excludes_self(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype=np.float32, round_p=None):
     return _attention_variant(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype,
                               lambda h, nq, nkv: h // (nq // nkv), lambda p, s, r: max(p.row_pos[r], 1))
 
 
-def _attn_noncausal_chunk(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype=np.float32):
+def _attn_noncausal_chunk(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype=np.float32, round_p=None):
     return _attention_variant(q, k_pool, v_pool, plan, n_q, n_kv, page, dtype,
                               lambda h, nq, nkv: h // (nq // nkv), lambda p, s, r: p.seq_kv_len[s])
 
@@ -553,3 +553,35 @@ def test_planted_residual_mistake_fails(monkeypatch):
     monkeypatch.setattr(ol, "layer_forward", no_residual)
     with pytest.raises(AssertionError):
         test_zero_projections_identity()
+
+
+# ----------------------------------------------------------------------------
+# bf16-storage precision variant
+# ----------------------------------------------------------------------------
+def test_round_bf16_against_bit_definition():
+    # bf16 keeps 7 mantissa bits: the grid spacing at 1.0 is 2^-7, ties go to
+    # the even neighbour
+    h = 2.0 ** -7
+    x = np.array([1.0, 1 + h / 2, 1 + 3 * h / 2, 1 + h / 4, 1 + 3 * h / 4, -2.5, 65504.0, 0.0], np.float32)
+    exp = np.array([1.0, 1.0, 1 + 2 * h, 1.0, 1 + h, -2.5, 65536.0, 0.0], np.float32)
+    assert np.array_equal(ol.round_bf16(x), exp)
+    # every output is representable (low 16 bits zero) and within half a spacing
+    v = np.random.default_rng(0).standard_normal(10000).astype(np.float32)
+    r = ol.round_bf16(v)
+    assert np.all((r.view(np.uint32) & 0xFFFF) == 0)
+    assert np.all(np.abs(r - v) <= np.abs(v) * 2.0 ** -8)
+
+
+def test_bf16_storage_variant_is_close_to_fp32_and_not_equal():
+    rng = np.random.default_rng(10)
+    dims = tiny_dims(d_model=64, d_ff=96)
+    w = wl.layer_weights(rng, dims)
+    st = tiny_state(rng, dims, [9, 30], [(40, 5)])
+    p = plan_from_state(st, 30, 30)
+    cos, sin = ol.rope_tables(64, dims.d_head, dims.theta)
+    x = wl.bf16_round(rng.standard_normal((p.n_rows, dims.d_model), dtype=np.float32))
+    a = ol.layer_forward(w, dims, p, x, st.k_pool.copy(), st.v_pool.copy(), cos, sin)
+    b = ol.layer_forward(w, dims, p, x, st.k_pool.copy(), st.v_pool.copy(), cos, sin, storage="bf16")
+    rl2 = np.linalg.norm(a - b) / np.linalg.norm(a)
+    assert 0 < rl2 < 1e-2
+    assert np.all((b.view(np.uint32) & 0xFFFF) == 0)

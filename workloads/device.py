@@ -50,3 +50,57 @@ def rope_table_device(max_pos: int, dims, device="cuda"):
 def workspace(nbytes: int, device="cuda"):
     import torch
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------- device-side generation
+# Model-scale inputs (tens of GB) are drawn on the device with torch's seeded
+# Philox generator, directly in bf16 (the draw is rounded to bf16 once); the
+# oracle side reads back exactly the tensors it needs.
+def device_generator(seed: int, device="cuda"):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def randn_bf16(shape, gen, scale=1.0, device="cuda"):
+    import torch
+    t = torch.randn(shape, generator=gen, dtype=torch.float32, device=device)
+    if scale != 1.0:
+        t.mul_(scale)
+    return t.to(torch.bfloat16)
+
+
+def _layer_draws(dims, seed, device):
+    """The layer's tensors in a fixed draw order from its own seed."""
+    gen = device_generator(seed, device)
+    d, f = dims.d_model, dims.d_ff
+    w_qkv = randn_bf16((dims.qkv_cols, d), gen, 0.02, device)
+    w_o = randn_bf16((d, dims.n_q * dims.d_head), gen, 0.02, device)
+    w_g = randn_bf16((f, d), gen, 0.02, device)
+    w_u = randn_bf16((f, d), gen, 0.02, device)
+    w_d = randn_bf16((d, f), gen, 0.02, device)
+    return w_qkv, w_o, w_g, w_u, w_d
+
+
+def layer_weights_random(dims, seed, device="cuda"):
+    """One layer's weights on the device from `seed`: N(0, 0.02) projections,
+    gains 1; gate/up interleaved by the library."""
+    import torch
+    import chunked_prefill_hybrid_tau_gb300 as hb
+    w_qkv, w_o, w_g, w_u, w_d = _layer_draws(dims, seed, device)
+    f_pad = (dims.d_ff + 63) // 64 * 64
+    w_gu = torch.empty((2 * f_pad, dims.d_model), dtype=torch.bfloat16, device=device)
+    hb.hb_interleave_gate_up(w_g, w_u, w_gu)
+    del w_g, w_u
+    ones = torch.ones(dims.d_model, dtype=torch.bfloat16, device=device)
+    return hb.LayerWeights(w_qkv=w_qkv, w_o=w_o, w_gu=w_gu, w_d=w_d, g1=ones, g2=ones.clone())
+
+
+def host_layer_weights(dims, seed, device="cuda") -> dict:
+    """The oracle's view of layer `seed` (float32 arrays of the same bf16
+    draws, regenerated from the seed)."""
+    w_qkv, w_o, w_g, w_u, w_d = _layer_draws(dims, seed, device)
+    ones = np.ones(dims.d_model, np.float32)
+    return dict(w_qkv=to_numpy(w_qkv), w_o=to_numpy(w_o), w_g=to_numpy(w_g), w_u=to_numpy(w_u), w_d=to_numpy(w_d),
+                g1=ones, g2=ones.copy())
