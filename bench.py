@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tau", type=int, default=512)
     ap.add_argument("--decodes", type=int, default=32)
+    ap.add_argument("--sweep", action="store_true",
+                    help="token-budget sweep (tau 64..4096, 64 decodes, c = tau - 64): one JSON line per tau")
     return ap.parse_args()
 
 
@@ -468,8 +470,91 @@ def run_hb(args, world, rank, local):
     return 0
 
 
+def run_sweep(args):
+    """ms/iter, tokens/s and roofline fraction against the token budget on the
+    Mistral-7B-shaped layer: 64 decodes with contexts uniform in [512, 8192]
+    plus a chunk of c = tau - 64 tokens at offset 0 of an 8192-token prompt."""
+    import torch
+    import chunked_prefill_hybrid_tau_gb300 as hb
+    from chunked_prefill_hybrid_tau_gb300 import costs
+    from workloads import device as wd
+    lib = hb.lib()
+    taus = [64, 128, 256, 512, 1024, 2048, 4096]
+    w = make_workload(max(taus), 64)
+    st, dims = w.state, w.dims
+    max_pos = 8192 + max(taus) + 1
+    gw = wd.layer_weights_device(w.weights[0], dims)
+    kc, vc = wd.bf16_tensor(st.k_pool), wd.bf16_tensor(st.v_pool)
+    rope = wd.rope_table_device(max_pos, dims)
+    x_all = wd.bf16_tensor(w.x)
+    peaks = load_peaks()
+    s_bar = float(np.mean([r.done for r in st.decodes]))
+    balance = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    for tau in taus:
+        stream = torch.cuda.Stream()
+        runner = PlanRunner(lib, st, tau, tau, "cuda")
+        ws = wd.workspace(hb.hb_layer_workspace_bytes(dims, runner.row_cap, runner.seq_cap, max_pos))
+        x = x_all[:tau].contiguous()
+        out = torch.empty_like(x)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(9)]
+        for e in ev:
+            e.record(stream)
+        arr = (C.c_void_p * 9)(*[e.cuda_event for e in ev])
+        from chunked_prefill_hybrid_tau_gb300 import _lib as L
+        prof = L.hb_profile(arr, 9)
+        ds, wsr = hb.dims_struct(dims), gw.struct()
+
+        def layer(dp, with_prof=False):
+            rc = lib.hb_layer_forward(C.byref(wsr), C.byref(ds), C.byref(dp), C.c_void_p(rope.data_ptr()), max_pos,
+                                      C.c_void_p(x.data_ptr()), C.c_void_p(out.data_ptr()), C.c_void_p(kc.data_ptr()),
+                                      C.c_void_p(vc.data_ptr()), int(kc.shape[0]), max_pos, C.c_void_p(ws.data_ptr()),
+                                      ws.numel(), C.c_void_p(stream.cuda_stream),
+                                      C.byref(prof) if with_prof else None)
+            if rc != 0:
+                raise RuntimeError(lib.hb_last_error().decode())
+
+        for _ in range(10):
+            layer(runner.step(stream))
+        steps = max(50, min(args.steps, 400))
+        stage_ms = np.zeros(8)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stream.synchronize()
+        s0.record(stream)
+        for _ in range(steps):
+            layer(runner.step(stream))
+        s1.record(stream)
+        stream.synchronize()
+        t_step = s0.elapsed_time(s1) / 1e3 / steps
+        for _ in range(20):
+            layer(runner.step(stream), with_prof=True)
+            stream.synchronize()
+            for s in range(8):
+                stage_ms[s] += ev[s].elapsed_time(ev[s + 1]) / 20
+        hb.hb_check_status(stream)
+        row_pos, q_start, kv_len = runner.host_plan_arrays()
+        sc = costs.stage_costs(dims, row_pos, q_start, kv_len)
+        flops, byts = costs.iteration_totals(sc)
+        t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
+        T = runner.n_rows
+        c = T - 64
+        print(json.dumps({
+            "sweep": "tau", "tau": tau, "rows": T, "chunk_tokens": c, "decodes": 64, "ms_per_step": 1e3 * t_step,
+            "tokens_per_s": T / t_step, "t_roof_ms": 1e3 * t_roof, "roofline_frac": t_roof / t_step,
+            "flops": flops, "bytes": byts, "intensity_flop_per_byte": flops / byts,
+            "intensity_page": costs.page_intensity(c, 64, dims.params_per_layer, 2, 1, dims.n_kv, dims.d_head, s_bar),
+            "stages_ms": {k: round(float(v), 5) for k, v in zip(costs.STAGES, stage_ms)}}), flush=True)
+    # the page's optimal chunk for this machine balance (I* = peak FLOP/s / peak B/s)
+    psi = dims.params_per_layer
+    c_star = balance / (2.0 * psi) * (2 * psi + 2.0 * dims.n_kv * dims.d_head * s_bar * 64) - 64
+    print(json.dumps({"sweep": "c_star", "machine_balance_flop_per_byte": balance, "c_star_tokens": c_star,
+                      "s_bar": s_bar}), flush=True)
+    return 0
+
+
 def main():
     args = parse()
+    if args.sweep:
+        return run_sweep(args)
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         rc = run_reference(args, world, rank)
