@@ -159,7 +159,8 @@ class PlanRunner:
         self.k += 1
         self.n_rows, self.n_seqs = P.n_rows, P.n_seqs
         d = self.dev.data_ptr()
-        return L.hb_device_plan(P.n_rows, P.n_seqs, self.max_pages, *[d + 4 * int(self.off[i]) for i in range(5)])
+        return L.hb_device_plan(P.n_rows, P.n_seqs, self.max_pages, *[d + 4 * int(self.off[i]) for i in range(5)],
+                                P.decode_pairs, P.chunk_pairs, P.chunk_rows)
 
     def host_plan_arrays(self):
         s = self.pinned[(self.k - 1) & 1].numpy()
@@ -458,7 +459,8 @@ def run_hb(args, world, rank, local):
                                                                       dims.n_kv, dims.d_head, s_bar)},
         "stages_ms": {k: round(float(v), 5) for k, v in zip(costs.STAGES, stage_ms)},
         "e2e": e2e,
-        "gpu_launches": 8 * args.steps,
+        # per layer forward: rmsnorm x2, GEMM x4, RoPE/KV append, chunk and decode attention
+        "gpu_launches": 9 * args.steps,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -32,12 +32,14 @@ class hb_plan(C.Structure):
                 ("pf_cap", i32), ("pf_take", p_i32), ("pf_finished", p_i32),
                 ("n_rows", i32), ("n_seqs", i32), ("n_decode_seqs", i32), ("pages_used", i32),
                 ("over_budget", i32), ("need_rows", i32), ("need_seqs", i32), ("need_max_pages", i32),
-                ("need_pages", i32)]
+                ("need_pages", i32), ("decode_pairs", C.c_int64), ("chunk_pairs", C.c_int64),
+                ("chunk_rows", C.c_int64)]
 
 
 class hb_device_plan(C.Structure):
     _fields_ = [("n_rows", i32), ("n_seqs", i32), ("max_pages", i32), ("row_pos", vp), ("slot_mapping", vp),
-                ("seq_q_start", vp), ("seq_kv_len", vp), ("block_table", vp)]
+                ("seq_q_start", vp), ("seq_kv_len", vp), ("block_table", vp),
+                ("decode_pairs", C.c_int64), ("chunk_pairs", C.c_int64), ("chunk_rows", C.c_int64)]
 
 
 class hb_layer_weights(C.Structure):

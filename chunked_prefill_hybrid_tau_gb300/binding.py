@@ -85,6 +85,9 @@ class HostPlan:
     free_pool: list
     pages_used: int
     over_budget: int
+    decode_pairs: int = 0        # scheduling hints (include/hb.h, hb_plan)
+    chunk_pairs: int = 0
+    chunk_rows: int = 0
 
     @property
     def n_rows(self) -> int:
@@ -156,7 +159,8 @@ def hb_plan_batch(dec_ctx, dec_pages, pf_len, pf_done, pf_pages, free_pool, tau,
             dec_pages=[list(bufs[i][:reqs_d[i].n_pages]) for i in range(n_dec)],
             pf_pages=[list(bufs[n_dec + j][:reqs_p[j].n_pages]) for j in range(n_pf)],
             free_pool=[int(v) for v in pool_arr[pool.head:]], pages_used=int(P.pages_used),
-            over_budget=int(P.over_budget))
+            over_budget=int(P.over_budget), decode_pairs=int(P.decode_pairs), chunk_pairs=int(P.chunk_pairs),
+            chunk_rows=int(P.chunk_rows))
     raise HBError(L.HB_ERR_CAPACITY, "hb_plan_batch: capacity retry failed")
 
 
@@ -177,6 +181,7 @@ class DevicePlan:
             self.host = self.host.pin_memory()
         self.dev = torch.empty(host.size, dtype=torch.int32, device=device)
         self.n_rows, self.n_seqs, self.max_pages = hp.n_rows, hp.n_seqs, hp.max_pages
+        self.hints = (int(hp.decode_pairs), int(hp.chunk_pairs), int(hp.chunk_rows))
         self.h2d_bytes = int(host.size * 4)
         self.upload(stream)
 
@@ -195,7 +200,7 @@ class DevicePlan:
     def struct(self) -> L.hb_device_plan:
         base = self.dev.data_ptr()
         ptr = [base + 4 * int(self.offsets[i]) for i in range(len(self.FIELDS))]
-        return L.hb_device_plan(self.n_rows, self.n_seqs, self.max_pages, *ptr)
+        return L.hb_device_plan(self.n_rows, self.n_seqs, self.max_pages, *ptr, *self.hints)
 
 
 # ---------------------------------------------------------------- device ops

@@ -21,6 +21,8 @@
 // 128-byte swizzle that makes the ldmatrix reads conflict-free.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "device.cuh"
 #include "runtime.h"
 
@@ -805,6 +807,75 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
   }
 }
 
+// ---------------------------------------------------------------- SM split
+// Chunk rows (tensor cores, latency-bound per tile) and decode rows (HBM
+// streaming) cannot share an SM (each kernel fills its shared memory), so
+// when the plan's hints give both kinds of work the SMs are split and the
+// two persistent kernels run at the same time on disjoint SMs: the chunk
+// kernel on a side stream forked from and joined back into the caller's
+// stream.  Cost model (GB300, measured):
+//   chunk : t_c(n) = max(W / n, one tile), W = pairs x q heads / kChunkRate
+//           SM-us, a 128-row tile costing (mean keys per chunk row + 64) x
+//           128 / kChunkRate us;
+//   decode: t_d(n) = bytes / min(kDecodeBw, n x kDecodeBwPerSm).
+// The split is the largest chunk share within 2% of the best
+// max(t_c, t_d).  It only moves work between SMs: every row's result is
+// the same for any split.
+constexpr double kChunkRate = 5900.0;       // query-key pairs x heads per us per SM, d_head 128
+constexpr double kDecodeBwPerSm = 55000.0;  // bytes per us per SM
+constexpr double kDecodeBw = 6.2e6;         // bytes per us, whole GPU
+
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+SideStream g_side[64];
+std::mutex g_side_mu;
+
+hb_status side_stream(int device, SideStream** out) {
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream& ss = g_side[device];
+  if (ss.stream == nullptr) {
+    hb_status st = cuda_status(cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking), "cudaStreamCreate(side)");
+    if (st != HB_OK) return st;
+    st = cuda_status(cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming), "cudaEventCreate(fork)");
+    if (st != HB_OK) return st;
+    st = cuda_status(cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming), "cudaEventCreate(join)");
+    if (st != HB_OK) return st;
+  }
+  *out = &ss;
+  return HB_OK;
+}
+
+// CTAs for the chunk kernel when both paths run concurrently (the decode
+// kernel gets the rest); 0 = run them one after the other on all SMs.
+int chunk_sms(const DeviceCtx& ctx, const hb_device_plan& plan, const hb_layer_dims& dm) {
+  const int S = ctx.num_sms;
+  if (plan.chunk_pairs <= 0 || plan.decode_pairs <= 0 || plan.chunk_rows <= 0 || S < 4) return 0;
+  const double dscale = dm.d_head / 128.0;
+  const double work_c = static_cast<double>(plan.chunk_pairs) * dm.n_q * dscale / kChunkRate;
+  const double mean_keys = static_cast<double>(plan.chunk_pairs) / static_cast<double>(plan.chunk_rows);
+  const double t_tile = (mean_keys + 64.0) * 128.0 * dscale / kChunkRate;
+  const double bytes_d = static_cast<double>(plan.decode_pairs) * dm.n_kv * dm.d_head * 4.0;
+  auto t_chunk = [&](int n) { return work_c / n > t_tile ? work_c / n : t_tile; };
+  auto t_decode = [&](int n) {
+    const double bw = n * kDecodeBwPerSm < kDecodeBw ? n * kDecodeBwPerSm : kDecodeBw;
+    return bytes_d / bw;
+  };
+  double best = 1e300;
+  for (int n = 1; n < S; ++n) {
+    const double t = t_chunk(n) > t_decode(S - n) ? t_chunk(n) : t_decode(S - n);
+    if (t < best) best = t;
+  }
+  if (best >= t_chunk(S) + t_decode(S)) return 0;
+  int nc = 1;
+  for (int n = 1; n < S; ++n) {
+    const double t = t_chunk(n) > t_decode(S - n) ? t_chunk(n) : t_decode(S - n);
+    if (t <= best * 1.02) nc = n;
+  }
+  return nc;
+}
+
 template <int D>
 hb_status attention_launch_d(const DeviceCtx& ctx, const void* q, const hb_device_plan& plan, const hb_layer_dims& dm,
                              const CUtensorMap& tmK, const CUtensorMap& tmV, Params p, cudaStream_t stream) {
@@ -819,11 +890,30 @@ hb_status attention_launch_d(const DeviceCtx& ctx, const void* q, const hb_devic
     if (st != HB_OK) return st;
     attr_set[ctx.device] = true;
   }
-  // chunk tiles (tcgen05 path), then decode rows (HBM path), both persistent
-  hb_status st = chunk_tc_launch(ctx, q, tmK, tmV, plan, dm, p.num_pages, p.max_kv_len, p.out, p.work_counter, stream);
+  const int nc = chunk_sms(ctx, plan, dm);
+  if (nc == 0) {
+    // chunk tiles (tcgen05 path), then decode rows (HBM path), both persistent on all SMs
+    hb_status st =
+        chunk_tc_launch(ctx, q, tmK, tmV, plan, dm, p.num_pages, p.max_kv_len, p.out, p.work_counter, ctx.num_sms, stream);
+    if (st != HB_OK) return st;
+    decode_kernel<D><<<ctx.num_sms, kDecWarps * 32, DC<D>::SMEM, stream>>>(tmK, tmV, p);
+    return launch_status("decode_kernel launch");
+  }
+  SideStream* ss = nullptr;
+  hb_status st = side_stream(ctx.device, &ss);
   if (st != HB_OK) return st;
-  decode_kernel<D><<<ctx.num_sms, kDecWarps * 32, DC<D>::SMEM, stream>>>(tmK, tmV, p);
-  return launch_status("decode_kernel launch");
+  st = cuda_status(cudaEventRecord(ss->fork, stream), "cudaEventRecord(fork)");
+  if (st != HB_OK) return st;
+  st = cuda_status(cudaStreamWaitEvent(ss->stream, ss->fork, 0), "cudaStreamWaitEvent(fork)");
+  if (st != HB_OK) return st;
+  st = chunk_tc_launch(ctx, q, tmK, tmV, plan, dm, p.num_pages, p.max_kv_len, p.out, p.work_counter, nc, ss->stream);
+  if (st != HB_OK) return st;
+  decode_kernel<D><<<ctx.num_sms - nc, kDecWarps * 32, DC<D>::SMEM, stream>>>(tmK, tmV, p);
+  st = launch_status("decode_kernel launch");
+  if (st != HB_OK) return st;
+  st = cuda_status(cudaEventRecord(ss->join, ss->stream), "cudaEventRecord(join)");
+  if (st != HB_OK) return st;
+  return cuda_status(cudaStreamWaitEvent(stream, ss->join, 0), "cudaStreamWaitEvent(join)");
 }
 
 }  // namespace

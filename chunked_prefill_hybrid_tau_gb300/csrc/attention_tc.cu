@@ -619,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 hb_status chunk_tc_launch(const DeviceCtx& ctx, const void* q, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const hb_device_plan& plan, const hb_layer_dims& dm, int num_pages, int max_kv_len,
-                          void* out, int* work_counter, cudaStream_t stream) {
+                          void* out, int* work_counter, int grid, cudaStream_t stream) {
   CUtensorMap tmQ;
   hb_status st = encode_tmap_q3d(&tmQ, q, plan.n_rows, dm.n_q, dm.d_head);
   if (st != HB_OK) return st;
@@ -653,9 +653,9 @@ hb_status chunk_tc_launch(const DeviceCtx& ctx, const void* q, const CUtensorMap
     attr_set[di][ctx.device] = true;
   }
   if (dm.d_head == 128)
-    chunk_tc_kernel<128><<<ctx.num_sms, kThreads, TC<128>::SMEM, stream>>>(tmQ, tmK, tmV, p);
+    chunk_tc_kernel<128><<<grid, kThreads, TC<128>::SMEM, stream>>>(tmQ, tmK, tmV, p);
   else
-    chunk_tc_kernel<64><<<ctx.num_sms, kThreads, TC<64>::SMEM, stream>>>(tmQ, tmK, tmV, p);
+    chunk_tc_kernel<64><<<grid, kThreads, TC<64>::SMEM, stream>>>(tmQ, tmK, tmV, p);
   return launch_status("chunk_tc_kernel launch");
 }
 

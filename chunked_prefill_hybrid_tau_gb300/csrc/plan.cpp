@@ -81,6 +81,7 @@ extern "C" hb_status hb_plan_batch(hb_request* decodes, int32_t n_dec, hb_reques
   plan->need_max_pages = width;
   plan->need_pages = pages;
   plan->n_rows = plan->n_seqs = plan->n_decode_seqs = plan->pages_used = 0;
+  plan->decode_pairs = plan->chunk_pairs = plan->chunk_rows = 0;
   plan->over_budget = n_dec > tau ? 1 : 0;
 
   if (pool->count - pool->head < pages) {
@@ -118,6 +119,14 @@ extern "C" hb_status hb_plan_batch(hb_request* decodes, int32_t n_dec, hb_reques
       plan->row_pos[row] = p;
       plan->slot_mapping[row] = r.pages[p / page_size] * page_size + p % page_size;
       ++row;
+    }
+    // a row at position p sees p + 1 keys: sum over p in [pos0, pos0 + q_len)
+    const int64_t pairs = static_cast<int64_t>(q_len) * pos0 + static_cast<int64_t>(q_len) * (q_len + 1) / 2;
+    if (q_len == 1) {
+      plan->decode_pairs += pairs;
+    } else {
+      plan->chunk_pairs += pairs;
+      plan->chunk_rows += q_len;
     }
     int32_t used = ceil_div(pos0 + q_len, page_size);
     int32_t* bt = plan->block_table + static_cast<int64_t>(s) * plan->max_pages;

@@ -29,7 +29,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 hb_status encode_tmap_q3d(CUtensorMap* map, const void* q, int T, int n_q, int d_head);
 hb_status chunk_tc_launch(const DeviceCtx& ctx, const void* q, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const hb_device_plan& plan, const hb_layer_dims& dims, int num_pages, int max_kv_len,
-                          void* out, int* work_counter, cudaStream_t stream);
+                          void* out, int* work_counter, int grid, cudaStream_t stream);
 
 // Shape checks shared by the layer entry points.
 hb_status check_dims(const hb_layer_dims* dims);

@@ -141,6 +141,15 @@ typedef struct hb_plan {
   int32_t pages_used;     /* pages popped from the pool */
   int32_t over_budget;    /* 1 if n_dec > tau */
   int32_t need_rows, need_seqs, need_max_pages, need_pages; /* sizes required (always written) */
+  /* scheduling hints for the attention launch: query-key pairs the
+   * iteration's attention visits (a row at position p sees p + 1 keys),
+   * split by path -- sequences of one row (the HBM-bound path: every decode,
+   * and a one-token chunk) and sequences of several rows (the tensor-core
+   * path: prompt chunks).  Their sum is the method's attention cost.
+   * chunk_rows: rows of the several-row sequences. */
+  int64_t decode_pairs;
+  int64_t chunk_pairs;
+  int64_t chunk_rows;
 } hb_plan;
 
 hb_status hb_plan_batch(hb_request* decodes, int32_t n_dec, hb_request* prefills, int32_t n_pf,
@@ -159,6 +168,13 @@ typedef struct hb_device_plan {
   const int32_t* seq_q_start;  /* [S + 1] */
   const int32_t* seq_kv_len;   /* [S] */
   const int32_t* block_table;  /* [S][max_pages] */
+  /* hb_plan's scheduling hints (host values).  hb_attention splits the SMs
+   * between chunk and decode rows by their estimated cost; with zeros
+   * (unknown) the two paths run one after the other on all SMs.  Results
+   * never depend on them. */
+  int64_t decode_pairs;
+  int64_t chunk_pairs;
+  int64_t chunk_rows;
 } hb_device_plan;
 
 /* ------------------------------------------------------------------------

@@ -244,6 +244,34 @@ def test_attention_decode_batch_invariance():
             assert np.array_equal(got[i], base[i]), (idx, ch, i)
 
 
+def test_attention_sm_split_never_changes_results():
+    """The plan's scheduling hints only move chunk and decode work between
+    SMs: real hints, none (the two paths one after the other), and hints
+    that push the split to either extreme give bit-identical outputs, which
+    match the oracle."""
+    dims = wl.Dims(d_model=256, n_q=32, n_kv=8, d_head=128, d_ff=64)
+    rng = np.random.default_rng(8)
+    st = wl.make_state(rng, dims, [5, 300, 1500, 2900, 700, 64], [(1500, 900), (400, 0)], slack_pages=64)
+    hp, o = plan_both(st, 6 + 300, 256)
+    assert hp.chunk_pairs > 0 and hp.decode_pairs > 0 and hp.chunk_rows == 300
+    q = wl.bf16_round(rng.standard_normal((hp.n_rows, dims.n_q, dims.d_head), dtype=np.float32))
+    qt, kt, vt = wd.bf16_tensor(q), wd.bf16_tensor(st.k_pool), wd.bf16_tensor(st.v_pool)
+    max_kv = int(hp.seq_kv_len.max())
+    ws = wd.workspace(hb.hb_attention_workspace_bytes(dims, hp.n_rows, hp.n_seqs, max_kv))
+    dp = hb.DevicePlan(hp)
+    outs = []
+    for hints in [dp.hints, (0, 0, 0), (1, 10**12, 300), (10**12, 1, 300)]:
+        dp.hints = hints
+        out = torch.empty((hp.n_rows, dims.n_q * dims.d_head), dtype=torch.bfloat16, device="cuda")
+        hb.hb_attention(qt, kt, vt, dp, dims, max_kv, out, ws)
+        hb.hb_check_status()
+        outs.append(out)
+    for k in range(1, len(outs)):
+        assert torch.equal(outs[k], outs[0]), k
+    ref = ol.attention(q, st.k_pool, st.v_pool, o, dims.n_q, dims.n_kv, 16).reshape(hp.n_rows, -1)
+    assert_close(wd.to_numpy(outs[0]), ref, "attention with an SM split")
+
+
 def test_status_word_reports_bad_slot():
     dims = wl.Dims(d_model=256, n_q=4, n_kv=2, d_head=64, d_ff=64)
     qkv = torch.zeros((2, dims.qkv_cols), dtype=torch.bfloat16, device="cuda")

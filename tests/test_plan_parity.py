@@ -32,6 +32,13 @@ def compare(args, **kw):
     assert c.dec_pages == o.dec_pages and c.pf_pages == o.pf_pages
     assert c.free_pool == o.free_pool and c.pages_used == o.pages_used
     assert c.over_budget == o.over_budget
+    # scheduling hints: query-key pairs (a row at position p sees p + 1 keys)
+    # of one-row and of several-row sequences, and the latter's rows
+    rows = [o.seq_q_start[k + 1] - o.seq_q_start[k] for k in range(len(o.seq_pos0))]
+    pairs = [sum(p + 1 for p in o.row_pos[o.seq_q_start[k]:o.seq_q_start[k + 1]]) for k in range(len(rows))]
+    assert c.decode_pairs == sum(pk for pk, n in zip(pairs, rows) if n == 1)
+    assert c.chunk_pairs == sum(pk for pk, n in zip(pairs, rows) if n > 1)
+    assert c.chunk_rows == sum(n for n in rows if n > 1)
     return o, c
 
 
