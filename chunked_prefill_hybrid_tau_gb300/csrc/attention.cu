@@ -595,6 +595,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
   int* dpre = btc_all + kDecWarps * (SPLIT / 16);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ga = lane >> 2, t4 = lane & 3;
+  griddep_launch_dependents();
+  griddep_wait();
 
   for (int s = tid; s < p.S; s += blockDim.x) {
     const int q0 = p.q_start[s], q1 = p.q_start[s + 1];

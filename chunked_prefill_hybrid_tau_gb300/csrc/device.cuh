@@ -103,6 +103,15 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   mbar_wait(bar, parity, nullptr, nullptr, kDrainTimeoutNs);
 }
 
+// ---------------------------------------------------------------- launch order
+// Programmatic dependent launch: let the next kernel on the stream start its
+// prologue now / wait until the previous kernel has completed and its memory
+// is visible (returns at once when the launch had no such predecessor).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -22,6 +22,8 @@ template <int NV>
 __global__ void __launch_bounds__(kNormWarps * 32)
     rmsnorm_kernel(const uint4* __restrict__ x, const int* __restrict__ rows, const uint4* __restrict__ gamma,
                    uint4* __restrict__ y, int n_rows, int d8, float inv_d, float eps, int n_src, int* status) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * kNormWarps + warp;
   if (r >= n_rows) return;
@@ -98,6 +100,8 @@ __global__ void kv_append_kernel(const __nv_bfloat16* __restrict__ qkv, const in
   constexpr int HALF = DH / 2;
   constexpr int RC = HALF / 8;  // rotating threads per head
   constexpr int VC = DH / 8;    // copy threads per v head
+  griddep_launch_dependents();
+  griddep_wait();
   const int r = blockIdx.x;
   const int pos = row_pos[r];
   const int slot = slots[r];
@@ -159,9 +163,8 @@ hb_status rmsnorm_launch(const DeviceCtx& ctx, const void* x, const int* rows, c
   auto* yp = static_cast<uint4*>(y);
 #define HB_NORM(NV_)                                                                                           \
   if (nv <= NV_) {                                                                                             \
-    rmsnorm_kernel<NV_><<<blocks, kNormWarps * 32, 0, stream>>>(xp, rows, gp, yp, n_rows, d8, 1.0f / d, eps,   \
-                                                                n_src, ctx.status);                            \
-    return launch_status("rmsnorm_kernel launch");                                                            \
+    return launch_pdl(rmsnorm_kernel<NV_>, blocks, kNormWarps * 32, 0, stream, "rmsnorm_kernel launch", xp, rows, \
+                      gp, yp, n_rows, d8, 1.0f / d, eps, n_src, ctx.status);                                     \
   }
   HB_NORM(1)
   HB_NORM(2)
@@ -187,12 +190,10 @@ hb_status kv_append_launch(const DeviceCtx& ctx, const void* qkv, int T, const i
   auto* in = static_cast<const __nv_bfloat16*>(qkv);
   auto* rp = static_cast<const float2*>(rope);
   if (dm.d_head == 128)
-    kv_append_kernel<128><<<T, threads, 0, stream>>>(in, row_pos, slots, rp, max_pos, dm.n_q, dm.n_kv, qo, kc, vc,
-                                                     num_slots, ctx.status);
-  else
-    kv_append_kernel<64><<<T, threads, 0, stream>>>(in, row_pos, slots, rp, max_pos, dm.n_q, dm.n_kv, qo, kc, vc,
-                                                    num_slots, ctx.status);
-  return launch_status("kv_append_kernel launch");
+    return launch_pdl(kv_append_kernel<128>, T, threads, 0, stream, "kv_append_kernel launch", in, row_pos, slots, rp,
+                      max_pos, dm.n_q, dm.n_kv, qo, kc, vc, num_slots, ctx.status);
+  return launch_pdl(kv_append_kernel<64>, T, threads, 0, stream, "kv_append_kernel launch", in, row_pos, slots, rp,
+                    max_pos, dm.n_q, dm.n_kv, qo, kc, vc, num_slots, ctx.status);
 }
 
 hb_status check_dims(const hb_layer_dims* dm) {

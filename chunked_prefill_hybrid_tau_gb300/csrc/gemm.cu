@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
+  griddep_launch_dependents();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -149,20 +150,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       uint32_t pending = 0;  // stages armed and not yet seen consumed (bit mask)
       uint32_t armed_parity = 0;
+      // The weights do not come from the previous kernel: the first ring
+      // fill of B is issued before waiting for it, then A follows.
+      const int pre = blockIdx.x < tiles ? (kblocks < C::STAGES ? kblocks : C::STAGES) : 0;
+      if (pre > 0) {
+        const int n0 = (blockIdx.x / m_tiles) * BN;
+        for (int kb = 0; kb < pre; ++kb) {
+          mbar_arrive_expect_tx(&full[kb], C::STAGE_BYTES);
+          tma_load_2d(smem + kb * C::STAGE_BYTES + C::A_BYTES, &tmB, &full[kb], kb * BK, n0);
+        }
+      }
+      griddep_wait();
       for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
         const int m0 = (tile % m_tiles) * BM;
         const int n0 = (tile / m_tiles) * BN;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
           uint8_t* sa = smem + stage * C::STAGE_BYTES;
-          pending |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
-          tma_load_2d(sa + C::A_BYTES, &tmB, &full[stage], kb * BK, n0);
+          if (tile == static_cast<int>(blockIdx.x) && kb < pre) {
+            // stage armed and its B box issued above (fresh barrier, phase 0)
+            pending |= 1u << stage;
+            tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
+          } else {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            pending |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+            mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+            tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
+            tma_load_2d(sa + C::A_BYTES, &tmB, &full[stage], kb * BK, n0);
+          }
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -177,7 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (pending & (1u << s)) mbar_drain(&full[s], (armed_parity >> s) & 1u);
       }
     }
+    if (lane != 0) griddep_wait();
   } else if (warp == 1) {
+    griddep_wait();
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
@@ -220,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- epilogue
+    griddep_wait();
     const int quarter = warp & 3;
     int t = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++t) {
@@ -310,8 +331,7 @@ hb_status launch(const DeviceCtx& ctx, const void* A, int lda, const void* B, vo
   p.status = ctx.status;
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
-  gemm_kernel<BN, EPI><<<grid, kThreads, C::SMEM, stream>>>(tmA, tmB, p);
-  return launch_status("gemm_kernel launch");
+  return launch_pdl(gemm_kernel<BN, EPI>, grid, kThreads, C::SMEM, stream, "gemm_kernel launch", tmA, tmB, p);
 }
 
 // Tile width: fewest waves of tiles over the SMs, weighted by a per-tile

@@ -26,6 +26,29 @@ hb_status encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uin
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Launch with programmatic stream serialization: the kernel may start while
+// its predecessor on the stream is still running (once every predecessor CTA
+// has signalled griddepcontrol.launch_dependents) and must execute
+// griddepcontrol.wait before it touches memory the predecessor writes or
+// reads.  Every kernel of this library does both, so kernels complete in
+// stream order.  Behind anything that is not such a kernel (a copy, an event,
+// another library's kernel) the launch waits as usual.
+template <typename... KArgs, typename... Args>
+hb_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                     const char* what, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...), what);
+}
+
 hb_status encode_tmap_q3d(CUtensorMap* map, const void* q, int T, int n_q, int d_head);
 hb_status chunk_tc_launch(const DeviceCtx& ctx, const void* q, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const hb_device_plan& plan, const hb_layer_dims& dims, int num_pages, int max_kv_len,
