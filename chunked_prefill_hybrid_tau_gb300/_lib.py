@@ -43,7 +43,7 @@ class hb_device_plan(C.Structure):
 
 
 class hb_layer_weights(C.Structure):
-    _fields_ = [("w_qkv", vp), ("w_o", vp), ("w_gu", vp), ("w_d", vp), ("g1", vp), ("g2", vp)]
+    _fields_ = [("w_qkv", vp), ("w_o", vp), ("w_gu", vp), ("w_d", vp)]
 
 
 class hb_profile(C.Structure):
@@ -72,6 +72,7 @@ PROTOTYPES = {
                                        vp, vp]),
     "hb_gemm": (C.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, vp]),
     "hb_interleave_gate_up": (C.c_int, [vp, vp, vp, i32, i32, vp]),
+    "hb_fold_gamma": (C.c_int, [vp, vp, vp, i32, i32, vp]),
     "hb_layer_workspace_bytes": (C.c_size_t, [C.POINTER(hb_layer_dims), i32, i32, i32]),
     "hb_layer_forward": (C.c_int, [C.POINTER(hb_layer_weights), C.POINTER(hb_layer_dims),
                                    C.POINTER(hb_device_plan), vp, i32, vp, vp, vp, vp, i32, i32, vp, C.c_size_t, vp,

@@ -245,6 +245,29 @@ def hb_interleave_gate_up(w_gate, w_up, w_gu, stream=None):
            "hb_interleave_gate_up")
 
 
+def hb_fold_gamma(w, gamma, out=None, stream=None):
+    """out = bf16(w * gamma) column-wise (in place when out is None)."""
+    rows, cols = w.shape
+    out = w if out is None else out
+    _check(lib().hb_fold_gamma(_p(w), _p(gamma), _p(out), rows, cols, _stream(stream)), "hb_fold_gamma")
+    return out
+
+
+def prepare_layer_weights(w_qkv, w_o, w_g, w_u, w_d, g1, g2, stream=None) -> "LayerWeights":
+    """Raw device bf16 weights of one layer -> the prepared form that
+    hb_layer_forward takes: g1 folded into W_qkv, gate/up interleaved and g2
+    folded into them (include/hb.h, hb_layer_weights).  w_qkv is folded in
+    place; w_g and w_u are left as they are."""
+    import torch
+    F, d = w_g.shape
+    f_pad = (F + 63) // 64 * 64
+    w_gu = torch.empty((2 * f_pad, d), dtype=torch.bfloat16, device=w_g.device)
+    hb_interleave_gate_up(w_g, w_u, w_gu, stream)
+    hb_fold_gamma(w_gu, g2, stream=stream)
+    hb_fold_gamma(w_qkv, g1, stream=stream)
+    return LayerWeights(w_qkv=w_qkv, w_o=w_o, w_gu=w_gu, w_d=w_d)
+
+
 def hb_layer_workspace_bytes(dims, max_rows, max_seqs, max_kv_len) -> int:
     ds = dims_struct(dims)
     return int(lib().hb_layer_workspace_bytes(C.byref(ds), int(max_rows), int(max_seqs), int(max_kv_len)))
@@ -252,16 +275,14 @@ def hb_layer_workspace_bytes(dims, max_rows, max_seqs, max_kv_len) -> int:
 
 @dataclasses.dataclass
 class LayerWeights:
-    """Device weights of one layer (bf16 tensors); w_gu already interleaved."""
+    """Prepared device weights of one layer (bf16 tensors, prepare_layer_weights)."""
     w_qkv: object
     w_o: object
     w_gu: object
     w_d: object
-    g1: object
-    g2: object
 
     def struct(self) -> L.hb_layer_weights:
-        return L.hb_layer_weights(*[self.__dict__[k].data_ptr() for k in ("w_qkv", "w_o", "w_gu", "w_d", "g1", "g2")])
+        return L.hb_layer_weights(*[self.__dict__[k].data_ptr() for k in ("w_qkv", "w_o", "w_gu", "w_d")])
 
 
 def hb_layer_forward(w: LayerWeights, dims, dplan: DevicePlan, rope, max_pos, x_in, x_out, k_cache, v_cache,

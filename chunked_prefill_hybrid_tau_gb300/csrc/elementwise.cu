@@ -72,6 +72,63 @@ __global__ void __launch_bounds__(kNormWarps * 32)
   }
 }
 
+// ---------------------------------------------------------------- row statistics
+// 32-column partial sums of squares of bf16 rows (the layout of GemmNorm):
+// one warp per row, lane i holds 16-byte pieces i, i+32, ...; four adjacent
+// pieces make one 32-column group, reduced over the four lanes by a fixed
+// xor pattern.
+template <int NV>
+__global__ void __launch_bounds__(kNormWarps * 32)
+    row_sumsq_kernel(const uint4* __restrict__ x, float* __restrict__ ss, int n_rows, int d8) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * kNormWarps + warp;
+  if (r >= n_rows) return;
+  const uint4* xr = x + static_cast<size_t>(r) * d8;
+  uint4 v[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int i = lane + 32 * k;
+    v[k] = i < d8 ? xr[i] : make_uint4(0, 0, 0, 0);
+  }
+  float* out = ss + static_cast<size_t>(r) * (d8 / 4);
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+    float a = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = unpack_bf16x2(w[j]);
+      a += f.x * f.x;
+      a += f.y * f.y;
+    }
+    a += __shfl_xor_sync(0xffffffffu, a, 1);
+    a += __shfl_xor_sync(0xffffffffu, a, 2);
+    const int i = lane + 32 * k;
+    if ((lane & 3) == 0 && i < d8) out[i / 4] = a;
+  }
+}
+
+// ---------------------------------------------------------------- gamma folding
+// out[r][c] = bf16(w[r][c] * gamma[c]): RMSNorm's gain moved into the
+// projection that consumes the normalised rows (x * inv * g) W^T =
+// inv * x (W diag(g))^T.  out may alias w.
+__global__ void fold_gamma_kernel(const uint4* w, const uint4* __restrict__ gamma, uint4* out, size_t total, int d8) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint4 a = w[i], g = gamma[i % d8];
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 fa = unpack_bf16x2(aw[j]), fg = unpack_bf16x2(gw[j]);
+      o[j] = pack_bf16x2(fa.x * fg.x, fa.y * fg.y);
+    }
+    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 // ---------------------------------------------------------------- RoPE table
 // table[p][i] = (cos, sin)(p * theta^(-2i/d_head)) in double, rounded to float.
 __global__ void rope_table_kernel(float2* __restrict__ t, int max_pos, int half, int d_head, double theta) {
@@ -177,6 +234,28 @@ hb_status rmsnorm_launch(const DeviceCtx& ctx, const void* x, const int* rows, c
   return HB_ERR_UNSUPPORTED;
 }
 
+hb_status row_sumsq_launch(const DeviceCtx& ctx, const void* x, float* ss, int rows, int d, cudaStream_t stream) {
+  if (rows == 0) return HB_OK;
+  const int blocks = (rows + kNormWarps - 1) / kNormWarps;
+  const int d8 = d / 8;
+  const int nv = (d8 + 31) / 32;
+  auto* xp = static_cast<const uint4*>(x);
+  (void)ctx;
+#define HB_SS(NV_)                                                                                                 \
+  if (nv <= NV_)                                                                                                   \
+    return launch_pdl(row_sumsq_kernel<NV_>, blocks, kNormWarps * 32, 0, stream, "row_sumsq_kernel launch", xp, ss, \
+                      rows, d8);
+  HB_SS(1)
+  HB_SS(2)
+  HB_SS(4)
+  HB_SS(8)
+  HB_SS(16)
+  HB_SS(32)
+#undef HB_SS
+  set_error("row statistics: d = %d above the supported 8192", d);
+  return HB_ERR_UNSUPPORTED;
+}
+
 hb_status kv_append_launch(const DeviceCtx& ctx, const void* qkv, int T, const int* row_pos, const int* slots,
                            const void* rope, int max_pos, const hb_layer_dims& dm, void* q_out, void* k_cache,
                            void* v_cache, int num_pages, cudaStream_t stream) {
@@ -250,4 +329,19 @@ extern "C" hb_status hb_kv_append(const void* qkv, int32_t T, const int32_t* row
   if (st != HB_OK) return st;
   return hb::kv_append_launch(ctx, qkv, T, row_pos, slot_mapping, rope, max_pos, *dims, q_out, k_cache, v_cache,
                               num_pages, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" hb_status hb_fold_gamma(const void* w, const void* gamma, void* out, int32_t rows, int32_t cols,
+                                   void* stream) {
+  hb::clear_error();
+  HB_REQUIRE(w && gamma && out, "hb_fold_gamma: null pointer");
+  HB_REQUIRE(rows > 0 && cols > 0 && cols % 8 == 0, "hb_fold_gamma: rows > 0 and cols %% 8 == 0 required");
+  HB_REQUIRE(hb::aligned16(w) && hb::aligned16(gamma) && hb::aligned16(out), "hb_fold_gamma: 16-byte alignment");
+  hb::DeviceCtx ctx;
+  hb_status st = hb::device_context(&ctx);
+  if (st != HB_OK) return st;
+  const size_t total = static_cast<size_t>(rows) * (cols / 8);
+  hb::fold_gamma_kernel<<<ctx.num_sms * 8, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(w), static_cast<const uint4*>(gamma), static_cast<uint4*>(out), total, cols / 8);
+  return hb::launch_status("fold_gamma_kernel launch");
 }

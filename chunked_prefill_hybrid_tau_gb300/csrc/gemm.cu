@@ -53,14 +53,31 @@ struct Params {
   int ldc;       // row stride of C and R (elements)
   int out_cols;  // valid output columns (N, or N/2 for SWIGLU)
   int* status;
+  GemmNorm norm;  // folded RMSNorm: row scaling in (STORE, SWIGLU), row statistics out (RESIDUAL)
 };
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
 
+// Inverse RMS of one row from its 32-column partial sums of squares, summed
+// in column order: rsqrt(sum / d + eps).
+__device__ __forceinline__ float row_inv_rms(const GemmNorm& nm, int row) {
+  const float2* sp = reinterpret_cast<const float2*>(nm.ss_in + static_cast<size_t>(row) * nm.parts);
+  float ss = 0.f;
+  for (int i = 0; i < nm.parts / 2; ++i) {
+    const float2 v = sp[i];
+    ss += v.x;
+    ss += v.y;
+  }
+  return rsqrtf(ss * nm.inv_d + nm.eps);
+}
+
 // Store 32 accumulator columns [col, col+32) of one row, 16-byte segments
-// past the last valid column skipped.
+// past the last valid column skipped.  STORE scales by `scale` (the row's
+// folded RMSNorm factor, else 1); RESIDUAL writes the sum of squares of the
+// 32 rounded outputs to ss_dst when it is given.
 template <int EPI>
-__device__ __forceinline__ void store_chunk(const Params& p, int row, int col, const uint32_t (&r)[32]) {
+__device__ __forceinline__ void store_chunk(const Params& p, int row, int col, const uint32_t (&r)[32], float scale,
+                                            float* ss_dst) {
   const int ncols = p.out_cols;
   if (EPI == HB_EPI_F32) {
     float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.C) + static_cast<size_t>(row) * p.ldc + col);
@@ -86,9 +103,20 @@ __device__ __forceinline__ void store_chunk(const Params& p, int row, int col, c
         w[4 * i + j] = pack_bf16x2(f.x + __uint_as_float(r[e]), f.y + __uint_as_float(r[e + 1]));
       }
     }
+    if (ss_dst) {
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float2 f = unpack_bf16x2(w[i]);
+        ss += f.x * f.x;
+        ss += f.y * f.y;
+      }
+      *ss_dst = ss;
+    }
   } else {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+    for (int i = 0; i < 16; ++i)
+      w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * scale, __uint_as_float(r[2 * i + 1]) * scale);
   }
   uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) + static_cast<size_t>(row) * p.ldc + col);
 #pragma unroll
@@ -246,13 +274,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++t) {
       const int acc = t & 1;
       const uint32_t acc_phase = (t >> 1) & 1;
-      bool ok = mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.status);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
       const int m0 = (tile % m_tiles) * BM;
       const int n_blk = tile / m_tiles;
       const int row = m0 + quarter * 32 + lane;
       const bool row_ok = row < p.M;
+      // the row's folded RMSNorm factor, read before the accumulator is ready
+      const float scale = (p.norm.ss_in != nullptr && row_ok) ? row_inv_rms(p.norm, row) : 1.f;
+      bool ok = mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
       const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
       if (EPI == HB_EPI_SWIGLU) {
 #pragma unroll 1
@@ -268,8 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint32_t w[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
-                const float a0 = silu(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
-                const float a1 = silu(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+                const float a0 = silu(__uint_as_float(g[2 * i]) * scale) * (__uint_as_float(u[2 * i]) * scale);
+                const float a1 =
+                    silu(__uint_as_float(g[2 * i + 1]) * scale) * (__uint_as_float(u[2 * i + 1]) * scale);
                 w[i] = pack_bf16x2(a0, a1);
               }
               uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) +
@@ -287,7 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_32x32b_x32(t_base + c * 32, r);
           tmem_ld_wait();
           const int col = n_blk * BN + c * 32;
-          if (row_ok && col < p.out_cols) store_chunk<EPI>(p, row, col, r);
+          float* ss_dst = (EPI == HB_EPI_RESIDUAL && p.norm.ss_out != nullptr)
+                              ? p.norm.ss_out + static_cast<size_t>(row) * p.norm.parts + col / 32
+                              : nullptr;
+          if (row_ok && col < p.out_cols) store_chunk<EPI>(p, row, col, r, scale, ss_dst);
         }
       }
       tc_fence_before();
@@ -306,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, int EPI>
 hb_status launch(const DeviceCtx& ctx, const void* A, int lda, const void* B, void* Cp, int ldc, const void* R, int M,
-                 int N, int K, cudaStream_t stream) {
+                 int N, int K, const GemmNorm* norm, cudaStream_t stream) {
   using C = Cfg<BN>;
   CUtensorMap tmA, tmB;
   hb_status st = encode_tmap_2d(&tmA, A, K, M, static_cast<uint64_t>(lda) * 2, BK, BM, true);
@@ -329,6 +363,7 @@ hb_status launch(const DeviceCtx& ctx, const void* A, int lda, const void* B, vo
   p.ldc = ldc;
   p.out_cols = EPI == HB_EPI_SWIGLU ? N / 2 : N;
   p.status = ctx.status;
+  p.norm = norm ? *norm : GemmNorm{};
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
   return launch_pdl(gemm_kernel<BN, EPI>, grid, kThreads, C::SMEM, stream, "gemm_kernel launch", tmA, tmB, p);
@@ -361,10 +396,10 @@ int choose_bn(int M, int N, int epi, int num_sms) {
 }  // namespace
 
 hb_status gemm_launch(const DeviceCtx& ctx, const void* A, int lda, const void* B, void* C, int ldc, const void* R,
-                      int M, int N, int K, int epi, cudaStream_t stream) {
+                      int M, int N, int K, int epi, cudaStream_t stream, const GemmNorm* norm) {
   const int bn = choose_bn(M, N, epi, ctx.num_sms);
 #define HB_GEMM_CASE(BN_, EPI_) \
-  if (bn == BN_ && epi == EPI_) return launch<BN_, EPI_>(ctx, A, lda, B, C, ldc, R, M, N, K, stream);
+  if (bn == BN_ && epi == EPI_) return launch<BN_, EPI_>(ctx, A, lda, B, C, ldc, R, M, N, K, norm, stream);
   HB_GEMM_CASE(256, HB_EPI_STORE)
   HB_GEMM_CASE(192, HB_EPI_STORE)
   HB_GEMM_CASE(128, HB_EPI_STORE)

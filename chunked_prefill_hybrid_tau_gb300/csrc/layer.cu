@@ -5,8 +5,13 @@
 //   rmsnorm1 -> qkv projection -> RoPE + paged KV append -> hybrid attention
 //   -> o projection + residual -> rmsnorm2 -> gate/up projection + SwiGLU
 //   -> down projection + residual.
-// Every stage is one kernel launch on the caller's stream; the workspace is
-// carved into 256-byte aligned regions.
+// Both RMSNorms are folded into the projections that consume them: the
+// gains are folded into W_qkv and W_gu at weight preparation, a row's
+// 1/rms factor scales its accumulators in the QKV and gate/up epilogues, and
+// the statistics come from a row pass over x (rmsnorm1) and from the o
+// projection's epilogue (rmsnorm2, no separate pass).  Every stage is one
+// kernel launch on the caller's stream (attention: two, see attention.cu);
+// the workspace is carved into 256-byte aligned regions.
 #include <cuda_runtime.h>
 
 #include "runtime.h"
@@ -20,14 +25,15 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline int ffn_pad(const hb_layer_dims& dm) { return (dm.d_ff + 63) / 64 * 64; }
 
 struct LayerWs {
-  size_t xn, qkv, q, o, h, a, attn, total;
+  size_t ss_x, ss_h, qkv, q, o, h, a, attn, total;
 };
 
 LayerWs layer_ws(const hb_layer_dims& dm, int T, int S, int max_kv_len) {
   LayerWs w;
   const size_t t = static_cast<size_t>(T);
   size_t off = 0;
-  w.xn = off;   off += align256(t * dm.d_model * 2);
+  w.ss_x = off; off += align256(t * (dm.d_model / 32) * 4);
+  w.ss_h = off; off += align256(t * (dm.d_model / 32) * 4);
   w.qkv = off;  off += align256(t * (dm.n_q + 2 * dm.n_kv) * dm.d_head * 2);
   w.q = off;    off += align256(t * dm.n_q * dm.d_head * 2);
   w.o = off;    off += align256(t * dm.n_q * dm.d_head * 2);
@@ -56,7 +62,7 @@ extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_
   hb_status st = check_dims(dims);
   if (st != HB_OK) return st;
   HB_REQUIRE(w && plan, "hb_layer_forward: null weights or plan");
-  HB_REQUIRE(w->w_qkv && w->w_o && w->w_gu && w->w_d && w->g1 && w->g2, "hb_layer_forward: null weight");
+  HB_REQUIRE(w->w_qkv && w->w_o && w->w_gu && w->w_d, "hb_layer_forward: null weight");
   HB_REQUIRE(x_in && x_out && k_cache && v_cache && rope, "hb_layer_forward: null pointer");
   HB_REQUIRE(plan->n_rows >= 0 && plan->n_seqs >= 0, "hb_layer_forward: bad plan sizes");
   HB_REQUIRE(plan->n_rows == 0 || (plan->row_pos && plan->slot_mapping && plan->seq_q_start && plan->seq_kv_len &&
@@ -78,7 +84,8 @@ extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_
   if (st != HB_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  void* xn = ws + lw.xn;
+  float* ss_x = reinterpret_cast<float*>(ws + lw.ss_x);
+  float* ss_h = reinterpret_cast<float*>(ws + lw.ss_h);
   void* qkv = ws + lw.qkv;
   void* q = ws + lw.q;
   void* o = ws + lw.o;
@@ -100,15 +107,24 @@ extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_
     if (st != HB_OK) return st;  \
   } while (0)
 
-  HB_STEP(0, rmsnorm_launch(ctx, x_in, nullptr, w->g1, xn, T, d, dm.rms_eps, T, s));
-  HB_STEP(1, gemm_launch(ctx, xn, d, w->w_qkv, qkv, qkv_cols, nullptr, T, qkv_cols, d, HB_EPI_STORE, s));
+  GemmNorm norm_x, norm_h_out, norm_h_in;
+  norm_x.ss_in = ss_x;
+  norm_h_out.ss_out = ss_h;
+  norm_h_in.ss_in = ss_h;
+  for (GemmNorm* nm : {&norm_x, &norm_h_out, &norm_h_in}) {
+    nm->parts = d / 32;
+    nm->inv_d = 1.0f / d;
+    nm->eps = dm.rms_eps;
+  }
+  HB_STEP(0, row_sumsq_launch(ctx, x_in, ss_x, T, d, s));
+  HB_STEP(1, gemm_launch(ctx, x_in, d, w->w_qkv, qkv, qkv_cols, nullptr, T, qkv_cols, d, HB_EPI_STORE, s, &norm_x));
   HB_STEP(2, kv_append_launch(ctx, qkv, T, plan->row_pos, plan->slot_mapping, rope, max_pos, dm, q, k_cache, v_cache,
                               num_pages, s));
   HB_STEP(3, attention_launch(ctx, q, k_cache, v_cache, num_pages, *plan, dm, max_kv_len, o, aws,
                               lw.total - lw.attn, s));
-  HB_STEP(4, gemm_launch(ctx, o, hd, w->w_o, h, d, x_in, T, d, hd, HB_EPI_RESIDUAL, s));
-  HB_STEP(5, rmsnorm_launch(ctx, h, nullptr, w->g2, xn, T, d, dm.rms_eps, T, s));
-  HB_STEP(6, gemm_launch(ctx, xn, d, w->w_gu, a, fp, nullptr, T, 2 * fp, d, HB_EPI_SWIGLU, s));
+  HB_STEP(4, gemm_launch(ctx, o, hd, w->w_o, h, d, x_in, T, d, hd, HB_EPI_RESIDUAL, s, &norm_h_out));
+  HB_STEP(5, HB_OK);  // rmsnorm2: statistics came from the o projection, scaling goes to gate/up
+  HB_STEP(6, gemm_launch(ctx, h, d, w->w_gu, a, fp, nullptr, T, 2 * fp, d, HB_EPI_SWIGLU, s, &norm_h_in));
   HB_STEP(7, gemm_launch(ctx, a, fp, w->w_d, x_out, d, h, T, d, dm.d_ff, HB_EPI_RESIDUAL, s));
 #undef HB_STEP
   return mark(HB_LAYER_STAGES);

@@ -64,9 +64,26 @@ hb_status kv_append_launch(const DeviceCtx& ctx, const void* qkv, int T, const i
                            const void* rope, int max_pos, const hb_layer_dims& dims, void* q_out, void* k_cache,
                            void* v_cache, int num_pages, cudaStream_t stream);
 hb_status gemm_check(const void* A, const void* B, void* C, const void* R, int M, int N, int K, int epi);
+
+// RMSNorm folded into the projections.  Row statistics are 32-column partial
+// sums of squares, float [rows][parts] with parts = d / 32, always grouped
+// the same way whatever the tile shape, so a row's factor never depends on
+// its batch.  ss_in: scale each output row by rsqrt(sum / d + eps) (STORE,
+// SWIGLU; the gamma is folded into the weights).  ss_out: write the
+// statistics of the rounded output rows (RESIDUAL).
+struct GemmNorm {
+  const float* ss_in = nullptr;
+  float* ss_out = nullptr;
+  int parts = 0;
+  float inv_d = 0.f, eps = 0.f;
+};
+
 // A [M][K] with row stride lda, B [N][K], C/R with row stride ldc (elements).
 hb_status gemm_launch(const DeviceCtx& ctx, const void* A, int lda, const void* B, void* C, int ldc, const void* R,
-                      int M, int N, int K, int epi, cudaStream_t stream);
+                      int M, int N, int K, int epi, cudaStream_t stream, const GemmNorm* norm = nullptr);
+
+// Row statistics of x [rows][d] bf16 in the GemmNorm layout.
+hb_status row_sumsq_launch(const DeviceCtx& ctx, const void* x, float* ss, int rows, int d, cudaStream_t stream);
 size_t attention_workspace_bytes(const hb_layer_dims& dims, int max_seqs, int max_kv_len);
 hb_status attention_launch(const DeviceCtx& ctx, const void* q, const void* k_cache, const void* v_cache,
                            int num_pages, const hb_device_plan& plan, const hb_layer_dims& dims, int max_kv_len,

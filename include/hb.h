@@ -288,29 +288,41 @@ hb_status hb_interleave_gate_up(const void* w_gate, const void* w_up, void* w_gu
                                 void* stream);
 
 /* ------------------------------------------------------------------------
+ * hb_fold_gamma - weight preparation for the folded RMSNorm:
+ * out[r][c] = bf16(w[r][c] * gamma[c]) for a weight w [rows][cols] that
+ * consumes RMSNorm(x; gamma) rows (cols = d_model).  Device bf16 buffers,
+ * cols % 8 == 0, 16-byte aligned; out may alias w.  Asynchronous on stream.
+ * ---------------------------------------------------------------------- */
+hb_status hb_fold_gamma(const void* w, const void* gamma, void* out, int32_t rows, int32_t cols, void* stream);
+
+/* ------------------------------------------------------------------------
  * hb_layer_forward - one decoder layer over a packed hybrid batch:
  *   xn = RMSNorm(x; g1); qkv = xn W_qkv^T; RoPE + KV append;
  *   o = attention; h = x + o W_o^T; hn = RMSNorm(h; g2);
  *   x_out = h + (silu(hn W_g^T) * hn W_u^T) W_d^T
  * the "run_iteration(B)" step of the scheduling loop (Sarathi-Serve reading
  * notes, section 3.4) for one layer.
- *   w      : device bf16 weights (w_gu interleaved by hb_interleave_gate_up)
+ *   w      : device bf16 weights, prepared once (see hb_layer_weights):
+ *            both RMSNorm gains folded in, gate/up interleaved.  The norms
+ *            run inside the projections: (x * r * g) W^T = r * x (W diag g)^T
+ *            with r = 1/sqrt(mean(x^2) + eps) applied per row in fp32 to the
+ *            accumulators of the QKV and gate/up GEMMs.
  *   plan   : device plan; rope: table from hb_rope_table with max_pos rows
  *   x_in   : device bf16 [T][d_model]; x_out may alias x_in
  *   caches : updated in place with this iteration's K/V
  *   workspace: hb_layer_workspace_bytes(dims, max_rows, max_seqs, max_kv_len)
  *   prof   : optional (NULL): when set, events[k] (cudaEvent_t) is recorded
  *            on `stream` before stage k and events[HB_LAYER_STAGES] after the
- *            last, stages = rmsnorm1, qkv, rope+kv, attention, o+residual,
- *            rmsnorm2, gate/up+swiglu, down+residual.
+ *            last, stages = rmsnorm1 (row statistics of x), qkv, rope+kv,
+ *            attention, o+residual (+ statistics of h), rmsnorm2 (no launch:
+ *            folded), gate/up+swiglu, down+residual.
  * ---------------------------------------------------------------------- */
 typedef struct hb_layer_weights {
-  const void* w_qkv;  /* bf16 [(n_q + 2 n_kv) d_head][d_model] */
+  const void* w_qkv;  /* bf16 [(n_q + 2 n_kv) d_head][d_model] = W_qkv diag(g1) (hb_fold_gamma) */
   const void* w_o;    /* bf16 [d_model][n_q d_head] */
-  const void* w_gu;   /* bf16 [2 Fp][d_model] from hb_interleave_gate_up (Fp = d_ff rounded up to 64) */
+  const void* w_gu;   /* bf16 [2 Fp][d_model]: hb_interleave_gate_up of W_g, W_u (Fp = d_ff rounded up to
+                         64), then hb_fold_gamma with g2 */
   const void* w_d;    /* bf16 [d_model][d_ff] */
-  const void* g1;     /* bf16 [d_model] */
-  const void* g2;     /* bf16 [d_model] */
 } hb_layer_weights;
 
 #define HB_LAYER_STAGES 8

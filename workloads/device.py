@@ -25,18 +25,11 @@ def to_numpy(t) -> np.ndarray:
 
 
 def layer_weights_device(w: dict, dims, device="cuda"):
-    """Upload one layer's weights; gate/up are interleaved by the library."""
-    import torch
+    """Upload one layer's weights and prepare them with the library (gains
+    folded, gate/up interleaved)."""
     import chunked_prefill_hybrid_tau_gb300 as hb
-    wg = bf16_tensor(w["w_g"], device)
-    wu = bf16_tensor(w["w_u"], device)
-    f_pad = (dims.d_ff + 63) // 64 * 64
-    w_gu = torch.empty((2 * f_pad, dims.d_model), dtype=torch.bfloat16, device=device)
-    hb.hb_interleave_gate_up(wg, wu, w_gu)
-    del wg, wu
-    return hb.LayerWeights(w_qkv=bf16_tensor(w["w_qkv"], device), w_o=bf16_tensor(w["w_o"], device), w_gu=w_gu,
-                           w_d=bf16_tensor(w["w_d"], device), g1=bf16_tensor(w["g1"], device),
-                           g2=bf16_tensor(w["g2"], device))
+    return hb.prepare_layer_weights(*[bf16_tensor(w[k], device) for k in ("w_qkv", "w_o", "w_g", "w_u", "w_d",
+                                                                          "g1", "g2")])
 
 
 def rope_table_device(max_pos: int, dims, device="cuda"):
@@ -85,16 +78,12 @@ def _layer_draws(dims, seed, device):
 
 def layer_weights_random(dims, seed, device="cuda"):
     """One layer's weights on the device from `seed`: N(0, 0.02) projections,
-    gains 1; gate/up interleaved by the library."""
+    gains 1, prepared by the library."""
     import torch
     import chunked_prefill_hybrid_tau_gb300 as hb
     w_qkv, w_o, w_g, w_u, w_d = _layer_draws(dims, seed, device)
-    f_pad = (dims.d_ff + 63) // 64 * 64
-    w_gu = torch.empty((2 * f_pad, dims.d_model), dtype=torch.bfloat16, device=device)
-    hb.hb_interleave_gate_up(w_g, w_u, w_gu)
-    del w_g, w_u
     ones = torch.ones(dims.d_model, dtype=torch.bfloat16, device=device)
-    return hb.LayerWeights(w_qkv=w_qkv, w_o=w_o, w_gu=w_gu, w_d=w_d, g1=ones, g2=ones.clone())
+    return hb.prepare_layer_weights(w_qkv, w_o, w_g, w_u, w_d, ones, ones)
 
 
 def host_layer_weights(dims, seed, device="cuda") -> dict:
