@@ -79,9 +79,11 @@ __global__ void __launch_bounds__(kNormWarps * 32)
 // xor pattern.
 template <int NV>
 __global__ void __launch_bounds__(kNormWarps * 32)
-    row_sumsq_kernel(const uint4* __restrict__ x, float* __restrict__ ss, int n_rows, int d8) {
+    row_sumsq_kernel(const uint4* __restrict__ x, float* __restrict__ ss, int n_rows, int d8, int* zero,
+                     int n_zero) {
   griddep_launch_dependents();
   griddep_wait();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_zero; i += gridDim.x * blockDim.x) zero[i] = 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * kNormWarps + warp;
   if (r >= n_rows) return;
@@ -234,7 +236,8 @@ hb_status rmsnorm_launch(const DeviceCtx& ctx, const void* x, const int* rows, c
   return HB_ERR_UNSUPPORTED;
 }
 
-hb_status row_sumsq_launch(const DeviceCtx& ctx, const void* x, float* ss, int rows, int d, cudaStream_t stream) {
+hb_status row_sumsq_launch(const DeviceCtx& ctx, const void* x, float* ss, int rows, int d, int* zero, int n_zero,
+                           cudaStream_t stream) {
   if (rows == 0) return HB_OK;
   const int blocks = (rows + kNormWarps - 1) / kNormWarps;
   const int d8 = d / 8;
@@ -244,7 +247,7 @@ hb_status row_sumsq_launch(const DeviceCtx& ctx, const void* x, float* ss, int r
 #define HB_SS(NV_)                                                                                                 \
   if (nv <= NV_)                                                                                                   \
     return launch_pdl(row_sumsq_kernel<NV_>, blocks, kNormWarps * 32, 0, stream, "row_sumsq_kernel launch", xp, ss, \
-                      rows, d8);
+                      rows, d8, zero, n_zero);
   HB_SS(1)
   HB_SS(2)
   HB_SS(4)

@@ -54,7 +54,30 @@ struct Params {
   int out_cols;  // valid output columns (N, or N/2 for SWIGLU)
   int* status;
   GemmNorm norm;  // folded RMSNorm: row scaling in (STORE, SWIGLU), row statistics out (RESIDUAL)
+  int ksplit;     // 1, or 2: each tile's K range in two halves (RESIDUAL only)
+  float* part;    // ksplit 2: fp32 partial tiles [tile][half][BN][BM] (column-major)
+  int* flags;     // ksplit 2: per (tile, 32-row slab) arrival counters, zero between launches
 };
+
+// Work unit u: tile u / ksplit, K half u % ksplit (k-blocks [kb0, kb1)).
+// The two halves of a tile are consecutive units, so they run at the same
+// time on neighbouring CTAs.
+struct Unit {
+  int tile, half, m0, n_blk, kb0, kb1;
+};
+
+template <int BN>
+__device__ __forceinline__ Unit unit_of(const Params& p, int u, int m_tiles, int kblocks) {
+  Unit w;
+  w.tile = u / p.ksplit;
+  w.half = u - w.tile * p.ksplit;
+  w.m0 = (w.tile % m_tiles) * BM;
+  w.n_blk = w.tile / m_tiles;
+  const int per = (kblocks + p.ksplit - 1) / p.ksplit;
+  w.kb0 = w.half * per;
+  w.kb1 = w.kb0 + per < kblocks ? w.kb0 + per : kblocks;
+  return w;
+}
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
 
@@ -72,12 +95,10 @@ __device__ __forceinline__ float row_inv_rms(const GemmNorm& nm, int row) {
 }
 
 // Store 32 accumulator columns [col, col+32) of one row, 16-byte segments
-// past the last valid column skipped.  STORE scales by `scale` (the row's
-// folded RMSNorm factor, else 1); RESIDUAL writes the sum of squares of the
-// 32 rounded outputs to ss_dst when it is given.
+// past the last valid column skipped (STORE: scaled by `scale`, the row's
+// folded RMSNorm factor, else 1; F32: as is).
 template <int EPI>
-__device__ __forceinline__ void store_chunk(const Params& p, int row, int col, const uint32_t (&r)[32], float scale,
-                                            float* ss_dst) {
+__device__ __forceinline__ void store_chunk(const Params& p, int row, int col, const uint32_t (&r)[32], float scale) {
   const int ncols = p.out_cols;
   if (EPI == HB_EPI_F32) {
     float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.C) + static_cast<size_t>(row) * p.ldc + col);
@@ -89,39 +110,45 @@ __device__ __forceinline__ void store_chunk(const Params& p, int row, int col, c
     return;
   }
   uint32_t w[16];
-  if (EPI == HB_EPI_RESIDUAL) {
-    const uint4* res = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.R) +
-                                                      static_cast<size_t>(row) * p.ldc + col);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 rv = col + 8 * i < ncols ? res[i] : make_uint4(0, 0, 0, 0);
-      const uint32_t rr[4] = {rv.x, rv.y, rv.z, rv.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f = unpack_bf16x2(rr[j]);
-        const int e = 8 * i + 2 * j;
-        w[4 * i + j] = pack_bf16x2(f.x + __uint_as_float(r[e]), f.y + __uint_as_float(r[e + 1]));
-      }
-    }
-    if (ss_dst) {
-      float ss = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float2 f = unpack_bf16x2(w[i]);
-        ss += f.x * f.x;
-        ss += f.y * f.y;
-      }
-      *ss_dst = ss;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * scale, __uint_as_float(r[2 * i + 1]) * scale);
-  }
+  for (int i = 0; i < 16; ++i)
+    w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * scale, __uint_as_float(r[2 * i + 1]) * scale);
   uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) + static_cast<size_t>(row) * p.ldc + col);
 #pragma unroll
   for (int i = 0; i < 4; ++i)
     if (col + 8 * i < ncols) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+// RESIDUAL: C = R + acc for 32 columns, with the residual already loaded
+// (rv); writes the sum of squares of the 32 rounded outputs to ss_dst when
+// it is given.
+__device__ __forceinline__ void residual_chunk(const Params& p, int row, int col, const uint32_t (&r)[32],
+                                               const uint4 (&rv)[4], float* ss_dst) {
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t rr[4] = {rv[i].x, rv[i].y, rv[i].z, rv[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = unpack_bf16x2(rr[j]);
+      const int e = 8 * i + 2 * j;
+      w[4 * i + j] = pack_bf16x2(f.x + __uint_as_float(r[e]), f.y + __uint_as_float(r[e + 1]));
+    }
+  }
+  if (ss_dst) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 f = unpack_bf16x2(w[i]);
+      ss += f.x * f.x;
+      ss += f.y * f.y;
+    }
+    *ss_dst = ss;
+  }
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) + static_cast<size_t>(row) * p.ldc + col);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (col + 8 * i < p.out_cols) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
 }
 
 template <int BN, int EPI>
@@ -143,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int m_tiles = (p.M + BM - 1) / BM;
   const int n_tiles = (p.N + BN - 1) / BN;
   const int tiles = m_tiles * n_tiles;
+  const int units = tiles * p.ksplit;
   const int kblocks = (p.K + BK - 1) / BK;  // TMA zero-fills columns past K
 
   if (threadIdx.x == 0) {
@@ -180,21 +208,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t armed_parity = 0;
       // The weights do not come from the previous kernel: the first ring
       // fill of B is issued before waiting for it, then A follows.
-      const int pre = blockIdx.x < tiles ? (kblocks < C::STAGES ? kblocks : C::STAGES) : 0;
-      if (pre > 0) {
-        const int n0 = (blockIdx.x / m_tiles) * BN;
-        for (int kb = 0; kb < pre; ++kb) {
-          mbar_arrive_expect_tx(&full[kb], C::STAGE_BYTES);
-          tma_load_2d(smem + kb * C::STAGE_BYTES + C::A_BYTES, &tmB, &full[kb], kb * BK, n0);
+      int pre = 0;
+      if (static_cast<int>(blockIdx.x) < units) {
+        const Unit w = unit_of<BN>(p, blockIdx.x, m_tiles, kblocks);
+        pre = w.kb1 - w.kb0 < C::STAGES ? w.kb1 - w.kb0 : C::STAGES;
+        for (int i = 0; i < pre; ++i) {
+          mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
+          tma_load_2d(smem + i * C::STAGE_BYTES + C::A_BYTES, &tmB, &full[i], (w.kb0 + i) * BK, w.n_blk * BN);
         }
       }
       griddep_wait();
-      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-        const int m0 = (tile % m_tiles) * BM;
-        const int n0 = (tile / m_tiles) * BN;
-        for (int kb = 0; kb < kblocks; ++kb) {
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit w = unit_of<BN>(p, u, m_tiles, kblocks);
+        const int m0 = w.m0;
+        const int n0 = w.n_blk * BN;
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           uint8_t* sa = smem + stage * C::STAGE_BYTES;
-          if (tile == static_cast<int>(blockIdx.x) && kb < pre) {
+          if (u == static_cast<int>(blockIdx.x) && kb - w.kb0 < pre) {
             // stage armed and its B box issued above (fresh barrier, phase 0)
             pending |= 1u << stage;
             tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
@@ -233,13 +263,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int t = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++t) {
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++t) {
+        const Unit w = unit_of<BN>(p, u, m_tiles, kblocks);
         const int acc = t & 1;
         const uint32_t acc_phase = (t >> 1) & 1;
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
             ok = false;
             break;
@@ -250,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             mma_bf16(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), kIdesc,
-                     (kb | k) != 0 ? 1u : 0u);
+                     (kb != w.kb0 || k != 0) ? 1u : 0u);
           }
           mma_commit(&empty[stage]);
           if (++stage == C::STAGES) {
@@ -271,12 +302,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     griddep_wait();
     const int quarter = warp & 3;
     int t = 0;
-    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++t) {
+    for (int un = blockIdx.x; un < units; un += gridDim.x, ++t) {
+      const Unit wu = unit_of<BN>(p, un, m_tiles, kblocks);
       const int acc = t & 1;
       const uint32_t acc_phase = (t >> 1) & 1;
-      const int m0 = (tile % m_tiles) * BM;
-      const int n_blk = tile / m_tiles;
-      const int row = m0 + quarter * 32 + lane;
+      const int m0 = wu.m0;
+      const int n_blk = wu.n_blk;
+      const int rloc = quarter * 32 + lane;  // row within the tile
+      const int row = m0 + rloc;
       const bool row_ok = row < p.M;
       // the row's folded RMSNorm factor, read before the accumulator is ready
       const float scale = (p.norm.ss_in != nullptr && row_ok) ? row_inv_rms(p.norm, row) : 1.f;
@@ -312,16 +345,82 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
+        bool finish = true;  // this warp writes the output rows of the tile
+        const float* other = nullptr;
+        if (p.ksplit == 2) {
+          // Split K: publish this half's fp32 partial (column-major, so each
+          // store is one coalesced 128-byte line per warp); the second warp
+          // to arrive for this 32-row slab adds the other half and finishes.
+          // p0 + p1 is commutative, so the result does not depend on which
+          // half arrives last.
+          float* mine = p.part + (static_cast<size_t>(wu.tile) * 2 + wu.half) * BN * BM;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t_base + c * 32, r);
-          tmem_ld_wait();
-          const int col = n_blk * BN + c * 32;
-          float* ss_dst = (EPI == HB_EPI_RESIDUAL && p.norm.ss_out != nullptr)
-                              ? p.norm.ss_out + static_cast<size_t>(row) * p.norm.parts + col / 32
-                              : nullptr;
-          if (row_ok && col < p.out_cols) store_chunk<EPI>(p, row, col, r, scale, ss_dst);
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(t_base + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) mine[static_cast<size_t>(c * 32 + j) * BM + rloc] = __uint_as_float(r[j]);
+          }
+          __threadfence();
+          __syncwarp();
+          int last = 0;
+          if (lane == 0) {
+            int* flag = p.flags + wu.tile * 4 + quarter;
+            last = atomicAdd(flag, 1) == 1;
+            if (last) *flag = 0;
+          }
+          finish = __shfl_sync(0xffffffffu, last, 0) != 0;
+          if (finish) {
+            __threadfence();
+            other = p.part + (static_cast<size_t>(wu.tile) * 2 + (1 - wu.half)) * BN * BM;
+          }
+        }
+        if (finish && EPI == HB_EPI_RESIDUAL) {
+          // software-pipelined: the residual (and the other half's partial)
+          // of chunk c + 1 is in flight while chunk c is combined and stored
+          constexpr int NC = BN / 32;
+          uint4 rv[2][4];
+          float ov[2][32];
+          auto fetch = [&](int c, int b) {
+            const int col = n_blk * BN + c * 32;
+            const uint4* res = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.R) +
+                                                              static_cast<size_t>(row) * p.ldc + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              rv[b][i] = (row_ok && col + 8 * i < p.out_cols) ? res[i] : make_uint4(0, 0, 0, 0);
+            if (other != nullptr) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) ov[b][j] = __ldcg(other + static_cast<size_t>(c * 32 + j) * BM + rloc);
+            }
+          };
+          fetch(0, 0);
+#pragma unroll
+          for (int c = 0; c < NC; ++c) {
+            const int b = c & 1;
+            if (c + 1 < NC) fetch(c + 1, b ^ 1);
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(t_base + c * 32, r);
+            tmem_ld_wait();
+            if (other != nullptr) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + ov[b][j]);
+            }
+            const int col = n_blk * BN + c * 32;
+            float* ss_dst = p.norm.ss_out != nullptr
+                                ? p.norm.ss_out + static_cast<size_t>(row) * p.norm.parts + col / 32
+                                : nullptr;
+            if (row_ok && col < p.out_cols) residual_chunk(p, row, col, r, rv[b], ss_dst);
+          }
+        } else if (finish) {
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(t_base + c * 32, r);
+            tmem_ld_wait();
+            const int col = n_blk * BN + c * 32;
+            if (row_ok && col < p.out_cols) store_chunk<EPI>(p, row, col, r, scale);
+          }
         }
       }
       tc_fence_before();
@@ -340,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, int EPI>
 hb_status launch(const DeviceCtx& ctx, const void* A, int lda, const void* B, void* Cp, int ldc, const void* R, int M,
-                 int N, int K, const GemmNorm* norm, cudaStream_t stream) {
+                 int N, int K, const GemmNorm* norm, const GemmSplit* split, cudaStream_t stream) {
   using C = Cfg<BN>;
   CUtensorMap tmA, tmB;
   hb_status st = encode_tmap_2d(&tmA, A, K, M, static_cast<uint64_t>(lda) * 2, BK, BM, true);
@@ -364,8 +463,12 @@ hb_status launch(const DeviceCtx& ctx, const void* A, int lda, const void* B, vo
   p.out_cols = EPI == HB_EPI_SWIGLU ? N / 2 : N;
   p.status = ctx.status;
   p.norm = norm ? *norm : GemmNorm{};
+  p.ksplit = split ? 2 : 1;
+  p.part = split ? split->part : nullptr;
+  p.flags = split ? split->flags : nullptr;
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
+  const int units = tiles * p.ksplit;
+  const int grid = units < ctx.num_sms ? units : ctx.num_sms;
   return launch_pdl(gemm_kernel<BN, EPI>, grid, kThreads, C::SMEM, stream, "gemm_kernel launch", tmA, tmB, p);
 }
 
@@ -395,11 +498,26 @@ int choose_bn(int M, int N, int epi, int num_sms) {
 
 }  // namespace
 
+bool gemm_split_k(int N, int K, int epi) {
+  // a function of the shape alone, never of M: a row's result must not
+  // depend on how many rows share the launch
+  return epi == HB_EPI_RESIDUAL && N % 256 == 0 && N <= 8192 && K >= 8192;
+}
+
+size_t gemm_split_part_bytes(int M, int N) {
+  const size_t tiles = static_cast<size_t>((M + BM - 1) / BM) * ((N + 255) / 256);
+  return tiles * 2 * 256 * BM * 4;
+}
+
+int gemm_split_flags(int M, int N) { return ((M + BM - 1) / BM) * ((N + 255) / 256) * 4; }
+
 hb_status gemm_launch(const DeviceCtx& ctx, const void* A, int lda, const void* B, void* C, int ldc, const void* R,
-                      int M, int N, int K, int epi, cudaStream_t stream, const GemmNorm* norm) {
-  const int bn = choose_bn(M, N, epi, ctx.num_sms);
+                      int M, int N, int K, int epi, cudaStream_t stream, const GemmNorm* norm, const GemmSplit* split) {
+  if (split != nullptr && !gemm_split_k(N, K, epi)) split = nullptr;
+  // split-K units use the widest tile (N = 256 MMAs run near the tensor peak)
+  const int bn = split ? 256 : choose_bn(M, N, epi, ctx.num_sms);
 #define HB_GEMM_CASE(BN_, EPI_) \
-  if (bn == BN_ && epi == EPI_) return launch<BN_, EPI_>(ctx, A, lda, B, C, ldc, R, M, N, K, norm, stream);
+  if (bn == BN_ && epi == EPI_) return launch<BN_, EPI_>(ctx, A, lda, B, C, ldc, R, M, N, K, norm, split, stream);
   HB_GEMM_CASE(256, HB_EPI_STORE)
   HB_GEMM_CASE(192, HB_EPI_STORE)
   HB_GEMM_CASE(128, HB_EPI_STORE)

@@ -25,7 +25,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline int ffn_pad(const hb_layer_dims& dm) { return (dm.d_ff + 63) / 64 * 64; }
 
 struct LayerWs {
-  size_t ss_x, ss_h, qkv, q, o, h, a, attn, total;
+  size_t ss_x, ss_h, qkv, q, o, h, a, part_o, part_d, flags, attn, total;
 };
 
 LayerWs layer_ws(const hb_layer_dims& dm, int T, int S, int max_kv_len) {
@@ -39,6 +39,9 @@ LayerWs layer_ws(const hb_layer_dims& dm, int T, int S, int max_kv_len) {
   w.o = off;    off += align256(t * dm.n_q * dm.d_head * 2);
   w.h = off;    off += align256(t * dm.d_model * 2);
   w.a = off;    off += align256(t * ffn_pad(dm) * 2);
+  w.part_o = off; off += align256(gemm_split_part_bytes(T, dm.d_model));
+  w.part_d = off; off += align256(gemm_split_part_bytes(T, dm.d_model));
+  w.flags = off;  off += align256(static_cast<size_t>(2) * gemm_split_flags(T, dm.d_model) * 4);
   w.attn = off; off += align256(attention_workspace_bytes(dm, S, max_kv_len));
   w.total = off;
   return w;
@@ -116,16 +119,24 @@ extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_
     nm->inv_d = 1.0f / d;
     nm->eps = dm.rms_eps;
   }
-  HB_STEP(0, row_sumsq_launch(ctx, x_in, ss_x, T, d, s));
+  // split-K workspaces of the o and down projections: fp32 partial tiles
+  // and arrival counters (zeroed by the row statistics pass, left zero)
+  const int n_flags = gemm_split_flags(T, d);
+  GemmSplit split_o, split_d;
+  split_o.part = reinterpret_cast<float*>(ws + lw.part_o);
+  split_d.part = reinterpret_cast<float*>(ws + lw.part_d);
+  split_o.flags = reinterpret_cast<int*>(ws + lw.flags);
+  split_d.flags = split_o.flags + n_flags;
+  HB_STEP(0, row_sumsq_launch(ctx, x_in, ss_x, T, d, split_o.flags, 2 * n_flags, s));
   HB_STEP(1, gemm_launch(ctx, x_in, d, w->w_qkv, qkv, qkv_cols, nullptr, T, qkv_cols, d, HB_EPI_STORE, s, &norm_x));
   HB_STEP(2, kv_append_launch(ctx, qkv, T, plan->row_pos, plan->slot_mapping, rope, max_pos, dm, q, k_cache, v_cache,
                               num_pages, s));
   HB_STEP(3, attention_launch(ctx, q, k_cache, v_cache, num_pages, *plan, dm, max_kv_len, o, aws,
                               lw.total - lw.attn, s));
-  HB_STEP(4, gemm_launch(ctx, o, hd, w->w_o, h, d, x_in, T, d, hd, HB_EPI_RESIDUAL, s, &norm_h_out));
+  HB_STEP(4, gemm_launch(ctx, o, hd, w->w_o, h, d, x_in, T, d, hd, HB_EPI_RESIDUAL, s, &norm_h_out, &split_o));
   HB_STEP(5, HB_OK);  // rmsnorm2: statistics came from the o projection, scaling goes to gate/up
   HB_STEP(6, gemm_launch(ctx, h, d, w->w_gu, a, fp, nullptr, T, 2 * fp, d, HB_EPI_SWIGLU, s, &norm_h_in));
-  HB_STEP(7, gemm_launch(ctx, a, fp, w->w_d, x_out, d, h, T, d, dm.d_ff, HB_EPI_RESIDUAL, s));
+  HB_STEP(7, gemm_launch(ctx, a, fp, w->w_d, x_out, d, h, T, d, dm.d_ff, HB_EPI_RESIDUAL, s, nullptr, &split_d));
 #undef HB_STEP
   return mark(HB_LAYER_STAGES);
 }

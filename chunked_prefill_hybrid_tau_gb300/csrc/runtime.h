@@ -78,12 +78,26 @@ struct GemmNorm {
   float inv_d = 0.f, eps = 0.f;
 };
 
+// Split-K workspace for RESIDUAL projections (fp32 partial tiles and arrival
+// counters; the counters must be zero at launch and are left zero).  Used
+// when gemm_split_k(N, K, epi) holds, which depends on the shape only.
+struct GemmSplit {
+  float* part = nullptr;
+  int* flags = nullptr;
+};
+bool gemm_split_k(int N, int K, int epi);
+size_t gemm_split_part_bytes(int M, int N);  // fp32 partial tiles
+int gemm_split_flags(int M, int N);          // arrival counters (ints)
+
 // A [M][K] with row stride lda, B [N][K], C/R with row stride ldc (elements).
 hb_status gemm_launch(const DeviceCtx& ctx, const void* A, int lda, const void* B, void* C, int ldc, const void* R,
-                      int M, int N, int K, int epi, cudaStream_t stream, const GemmNorm* norm = nullptr);
+                      int M, int N, int K, int epi, cudaStream_t stream, const GemmNorm* norm = nullptr,
+                      const GemmSplit* split = nullptr);
 
-// Row statistics of x [rows][d] bf16 in the GemmNorm layout.
-hb_status row_sumsq_launch(const DeviceCtx& ctx, const void* x, float* ss, int rows, int d, cudaStream_t stream);
+// Row statistics of x [rows][d] bf16 in the GemmNorm layout; also zeroes
+// n_zero ints at `zero` (split-K counters of the launches that follow).
+hb_status row_sumsq_launch(const DeviceCtx& ctx, const void* x, float* ss, int rows, int d, int* zero, int n_zero,
+                           cudaStream_t stream);
 size_t attention_workspace_bytes(const hb_layer_dims& dims, int max_seqs, int max_kv_len);
 hb_status attention_launch(const DeviceCtx& ctx, const void* q, const void* k_cache, const void* v_cache,
                            int num_pages, const hb_device_plan& plan, const hb_layer_dims& dims, int max_kv_len,
