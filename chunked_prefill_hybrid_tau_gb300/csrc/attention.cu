@@ -1,4 +1,6 @@
-// Varlen paged hybrid attention (one launch for chunk rows and decode rows).
+// Varlen paged hybrid attention: chunk rows on the tensor cores
+// (attention_tc.cu), decode rows here on the HBM path, and the split of the
+// SMs between the two.
 //
 // What it computes (Sarathi-Serve reading notes, sections 3.1 and 7.5b;
 // Chunked Prefill page, mechanism section): a prompt chunk's query at
@@ -7,18 +9,14 @@
 // decode row attends to its whole context.  Keys are read through the
 // sequence's block table from 16-token pages.
 //
-// Work units (scheduled dynamically from a global counter):
-//   * chunk tile: 64 consecutive query rows x one q head; four consumer warps
-//     own 16 rows each and sweep all key blocks 0..pos_last (tensor path:
-//     mma.sync m16n8k16, fp32 online softmax, causal mask by position);
-//   * decode unit: one decode row x one kv head (its n_q/n_kv q heads as MMA
-//     rows) x one 1024-key split at fixed absolute positions, so the result
-//     of a row never depends on its batch companions.  Warp w takes page w
-//     of every 64-key block; the four warps merge in shared memory; splits
-//     are combined in a fixed order by the last CTA to finish (HBM path).
-// A producer warp streams each 64-key block (4 pages of K and of V, one TMA
-// box of 16 keys x 64 dims per page half) into a 4-stage ring with the
-// 128-byte swizzle that makes the ldmatrix reads conflict-free.
+// Decode unit: one decode row x one kv head (its n_q/n_kv q heads as the
+// rows of an m16n8k16 MMA) x one SPLIT-key range at fixed absolute
+// positions, so the result of a row never depends on its batch companions.
+// Each warp owns whole units and streams the unit's pages (K and V of one kv
+// head, one TMA box of 16 keys x 64 dims per half) through its own ring with
+// the 128-byte swizzle that makes the ldmatrix reads conflict-free.  Split
+// results are combined in split order by the last warp to finish a
+// (row, kv head).
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -31,25 +29,9 @@ namespace {
 
 using namespace dev;
 
-constexpr int KB = 64;                      // keys per block (4 pages)
-constexpr int STAGES = 4;
 constexpr int SPLIT = 1024;                 // keys per decode split
-constexpr int QTILE = 64;                   // query rows per chunk tile
-constexpr int kConsumers = 128;             // 4 consumer warps
-constexpr int kThreads = kConsumers + 32;   // + producer warp
 constexpr int HALF_BYTES = 16 * 128;        // one TMA box: 16 keys x 64 dims (128-byte rows)
 constexpr int MAX_SEQS = 1024;
-constexpr int UQ = 2;                       // depth of the unit queue
-
-template <int D>
-struct AC {
-  static constexpr int PAGE_BYTES = (D / 64) * HALF_BYTES;  // 16 keys x D dims
-  static constexpr int K_BYTES = 4 * PAGE_BYTES;            // 64 keys
-  static constexpr int STAGE_BYTES = 2 * K_BYTES;           // K block then V block
-  static constexpr int REC_FLOATS = 16 * D + 32;            // partial record: O[16][D], m[16], l[16]
-  static constexpr int MERGE_FLOATS = 4 * REC_FLOATS;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + MERGE_FLOATS * 4 + 2 * (MAX_SEQS + 1) * 4 + 256 + 1024;
-};
 
 struct Params {
   const __nv_bfloat16* q;
@@ -58,21 +40,11 @@ struct Params {
   const int* kv_len;
   const int* block_table;
   int S, T, max_pages, num_pages, n_q, n_kv, grp, max_kv_len;
-  int chunk_only;  // 1: schedule chunk tiles only (decode rows go to decode_kernel)
   float scale_log2;
   int* work_counter;
   int* combine_counters;
   float* partials;
   int* status;
-};
-
-struct Unit {
-  int kind;       // 0 = chunk tile, 1 = decode unit, -1 = none
-  int seq, head;  // head: q head (chunk) or kv head (decode)
-  int row0, nrows, pos0;
-  int key_end;    // keys [key_begin, key_end) are visited
-  int key_begin;
-  int nsplit, rec;
 };
 
 __device__ __forceinline__ int upper_index(const int* pre, int n, int u) {
@@ -83,48 +55,6 @@ __device__ __forceinline__ int upper_index(const int* pre, int n, int u) {
     if (pre[mid] <= u) lo = mid; else hi = mid - 1;
   }
   return lo;
-}
-
-__device__ Unit unit_info(const Params& p, const int* cpre, const int* dpre, int u) {
-  Unit w;
-  const int total_c = cpre[p.S];
-  const int total_d = dpre[p.S];
-  if (u < total_c) {
-    const int s = upper_index(cpre, p.S, u);
-    const int local = u - cpre[s];
-    const int q0 = p.q_start[s], qlen = p.q_start[s + 1] - q0;
-    const int ntiles = (qlen + QTILE - 1) / QTILE;
-    const int t = ntiles - 1 - local / p.n_q;  // heaviest tiles first
-    w.kind = 0;
-    w.seq = s;
-    w.head = local % p.n_q;
-    w.row0 = q0 + t * QTILE;
-    w.nrows = min(QTILE, qlen - t * QTILE);
-    w.pos0 = p.kv_len[s] - qlen + t * QTILE;
-    w.key_begin = 0;
-    w.key_end = w.pos0 + w.nrows;
-    w.nsplit = 1;
-    w.rec = 0;
-  } else if (u < total_c + total_d) {
-    const int ud = u - total_c;
-    const int s = upper_index(dpre, p.S, ud);
-    const int local = ud - dpre[s];
-    const int kvl = p.kv_len[s];
-    const int split = local / p.n_kv;
-    w.kind = 1;
-    w.seq = s;
-    w.head = local % p.n_kv;
-    w.row0 = p.q_start[s];
-    w.nrows = 1;
-    w.pos0 = kvl - 1;
-    w.key_begin = split * SPLIT;
-    w.key_end = min(kvl, w.key_begin + SPLIT);
-    w.nsplit = (kvl + SPLIT - 1) / SPLIT;
-    w.rec = ud;
-  } else {
-    w.kind = -1;
-  }
-  return w;
 }
 
 // ---------------------------------------------------------------- MMA helpers
@@ -148,45 +78,40 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
                : "r"(addr));
 }
 
-// Byte offset of (key 0..63, 16-byte chunk 0..D/8-1) in a swizzled K or V block.
-template <int D>
+// Byte offset of (key 0..15, 16-byte chunk 0..D/8-1) in one swizzled K or V
+// page: 64-dim halves of 16 rows x 128 bytes, chunk index XOR row.
 __device__ __forceinline__ uint32_t blk_off(int key, int chunk) {
   const int r = key & 15;
-  return (key >> 4) * AC<D>::PAGE_BYTES + (chunk >> 3) * HALF_BYTES + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
+  return (chunk >> 3) * HALF_BYTES + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
 }
 
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// One warp: S = Q K^T over NG 16-key groups starting at group g0 of the block,
-// online-softmax update, O += P V.  Rows a (= lane/4) and b (= a + 8) see
-// keys <= lim_a / lim_b.
-template <int D, int NG>
-__device__ __forceinline__ void warp_block(uint32_t k_base, uint32_t v_base, int g0, int key0,
-                                           const uint32_t (&qa)[D / 16][4], float (&o)[D / 8][4], float (&m)[2],
-                                           float (&l)[2], int lim_a, int lim_b, float scale_log2, int lane) {
+// One warp, one 16-key page: S = Q K^T (rows a = lane/4 and b = a + 8 of the
+// q-head group; keys above `lim` masked), online-softmax update in log2
+// units, O += P V with P rounded to bf16 for the MMA.
+template <int D>
+__device__ __forceinline__ void warp_page(uint32_t k_base, uint32_t v_base, int key0, const uint32_t (&qa)[D / 16][4],
+                                          float (&o)[D / 8][4], float (&m)[2], float (&l)[2], int lim,
+                                          float scale_log2, int lane) {
   const int mat = lane >> 3, rr = lane & 7, t = lane & 3;
-  float s[2 * NG][4];
+  float s[2][4];
 #pragma unroll
-  for (int j = 0; j < 2 * NG; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll
-  for (int gi = 0; gi < NG; ++gi) {
-    const int key = (g0 + gi) * 16 + ((mat >> 1) << 3) + rr;
+  for (int j = 0; j < 2; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+  {
+    const int key = ((mat >> 1) << 3) + rr;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       uint32_t b[4];
-      ldsm_x4(k_base + blk_off<D>(key, 2 * kk + (mat & 1)), b);
-      mma16816(s[2 * gi], qa[kk], b[0], b[1]);
-      mma16816(s[2 * gi + 1], qa[kk], b[2], b[3]);
+      ldsm_x4(k_base + blk_off(key, 2 * kk + (mat & 1)), b);
+      mma16816(s[0], qa[kk], b[0], b[1]);
+      mma16816(s[1], qa[kk], b[2], b[3]);
     }
   }
-  // mask, scale to log2 units, row maxima over the quad
   float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-  for (int j = 0; j < 2 * NG; ++j) {
+  for (int j = 0; j < 2; ++j) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int key = key0 + (g0 * 16) + 8 * j + 2 * t + (e & 1);
-      const int lim = e < 2 ? lim_a : lim_b;
+      const int key = key0 + 8 * j + 2 * t + (e & 1);
       const float v = key <= lim ? s[j][e] * scale_log2 : -INFINITY;
       s[j][e] = v;
       mx[e >> 1] = fmaxf(mx[e >> 1], v);
@@ -207,7 +132,7 @@ __device__ __forceinline__ void warp_block(uint32_t k_base, uint32_t v_base, int
   }
   float rs[2] = {0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < 2 * NG; ++j) {
+  for (int j = 0; j < 2; ++j) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float pv = exp2f(s[j][e] - muse[e >> 1]);
@@ -224,342 +149,24 @@ __device__ __forceinline__ void warp_block(uint32_t k_base, uint32_t v_base, int
     o[j][2] *= alpha[1];
     o[j][3] *= alpha[1];
   }
-  // O += P V
+  uint32_t pa[4];
+  pa[0] = pack_bf16x2(s[0][0], s[0][1]);
+  pa[1] = pack_bf16x2(s[0][2], s[0][3]);
+  pa[2] = pack_bf16x2(s[1][0], s[1][1]);
+  pa[3] = pack_bf16x2(s[1][2], s[1][3]);
+  const int key = ((mat & 1) << 3) + rr;
 #pragma unroll
-  for (int gi = 0; gi < NG; ++gi) {
-    uint32_t pa[4];
-    pa[0] = pack_bf16x2(s[2 * gi][0], s[2 * gi][1]);
-    pa[1] = pack_bf16x2(s[2 * gi][2], s[2 * gi][3]);
-    pa[2] = pack_bf16x2(s[2 * gi + 1][0], s[2 * gi + 1][1]);
-    pa[3] = pack_bf16x2(s[2 * gi + 1][2], s[2 * gi + 1][3]);
-    const int key = (g0 + gi) * 16 + ((mat & 1) << 3) + rr;
-#pragma unroll
-    for (int jd = 0; jd < D / 16; ++jd) {
-      uint32_t b[4];
-      ldsm_x4_t(v_base + blk_off<D>(key, 2 * jd + (mat >> 1)), b);
-      mma16816(o[2 * jd], pa, b[0], b[1]);
-      mma16816(o[2 * jd + 1], pa, b[2], b[3]);
-    }
+  for (int jd = 0; jd < D / 16; ++jd) {
+    uint32_t b[4];
+    ldsm_x4_t(v_base + blk_off(key, 2 * jd + (mat >> 1)), b);
+    mma16816(o[2 * jd], pa, b[0], b[1]);
+    mma16816(o[2 * jd + 1], pa, b[2], b[3]);
   }
 }
 
 __device__ __forceinline__ uint32_t ld_q2(const __nv_bfloat16* rowp, int col, bool ok) {
   return ok ? __ldg(reinterpret_cast<const unsigned int*>(rowp + col)) : 0u;
 }
-
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_constant__ CUtensorMap tmK,
-                                                                const __grid_constant__ CUtensorMap tmV, Params p) {
-  using C = AC<D>;
-  constexpr int STAGE_BYTES = C::STAGE_BYTES, K_BYTES = C::K_BYTES, PAGE_BYTES = C::PAGE_BYTES;
-  constexpr int REC_FLOATS = C::REC_FLOATS, MERGE_FLOATS = C::MERGE_FLOATS;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* merge = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);
-  int* cpre = reinterpret_cast<int*>(merge + MERGE_FLOATS);
-  int* dpre = cpre + MAX_SEQS + 1;
-  uint64_t* full = reinterpret_cast<uint64_t*>(dpre + MAX_SEQS + 1);
-  uint64_t* empty = full + STAGES;
-  uint64_t* uq_full = empty + STAGES;
-  uint64_t* uq_empty = uq_full + UQ;
-  int* uq = reinterpret_cast<int*>(uq_empty + UQ);
-  volatile int* abort_flag = uq + UQ;
-  int* last_flag = uq + UQ + 1;
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  // ---- schedule: per-sequence unit counts, then prefix sums ----------------
-  // A sequence with inconsistent sizes (rows outside [0, T), kv_len above
-  // the workspace's max_kv_len or below its row count) gets no units and
-  // raises the index error.
-  for (int s = tid; s < p.S; s += kThreads) {
-    const int q0 = p.q_start[s], q1 = p.q_start[s + 1];
-    const int qlen = q1 - q0, kvl = p.kv_len[s];
-    int c = 0, d = 0;
-    if (q0 < 0 || q1 > p.T || qlen < 0 || kvl < qlen || kvl > p.max_kv_len ||
-        (kvl + 15) / 16 > p.max_pages) {
-      flag_error(p.status, kStatusIndex);
-    } else if (qlen > 1) {
-      c = p.n_q * ((qlen + QTILE - 1) / QTILE);
-    } else if (qlen == 1 && !p.chunk_only) {
-      d = p.n_kv * ((kvl + SPLIT - 1) / SPLIT);
-    }
-    cpre[s + 1] = c;
-    dpre[s + 1] = d;
-  }
-  if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 4);
-    }
-    for (int s = 0; s < UQ; ++s) {
-      mbar_init(&uq_full[s], 1);
-      mbar_init(&uq_empty[s], 4);
-    }
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  __syncthreads();
-  if (tid == 0) {
-    cpre[0] = dpre[0] = 0;
-    for (int s = 1; s <= p.S; ++s) {
-      cpre[s] += cpre[s - 1];
-      dpre[s] += dpre[s - 1];
-    }
-  }
-  __syncthreads();
-  const int total = cpre[p.S] + dpre[p.S];
-
-  if (warp == 4) {
-    // ---------------------------------------------------------- producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      int stage = 0, qs = 0;
-      uint32_t phase = 0, qphase = 0;
-      uint32_t pending = 0, armed_parity = 0;
-      bool ok = true;
-      while (ok) {
-        if (!mbar_wait(&uq_empty[qs], qphase ^ 1u, abort_flag, p.status)) break;
-        const int u = atomicAdd(p.work_counter, 1);
-        uq[qs] = u;
-        mbar_arrive(&uq_full[qs]);
-        if (++qs == UQ) {
-          qs = 0;
-          qphase ^= 1u;
-        }
-        if (u >= total) break;
-        const Unit w = unit_info(p, cpre, dpre, u);
-        const int g = w.kind == 0 ? w.head / p.grp : w.head;
-        const int* bt = p.block_table + static_cast<size_t>(w.seq) * p.max_pages;
-        for (int kb0 = w.key_begin; kb0 < w.key_end; kb0 += KB) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          int npages = min(4, (w.key_end - kb0 + 15) / 16);
-          pending |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          mbar_arrive_expect_tx(&full[stage], npages * 2 * PAGE_BYTES);
-          uint8_t* sk = smem + stage * STAGE_BYTES;
-          for (int pg = 0; pg < npages; ++pg) {
-            const int pidx = kb0 / 16 + pg;
-            int page = pidx < p.max_pages ? bt[pidx] : -1;
-            if (page < 0 || page >= p.num_pages) {
-              flag_error(p.status, kStatusIndex);
-              page = 0;
-            }
-            const int y = (page * p.n_kv + g) * 16;
-#pragma unroll
-            for (int hf = 0; hf < D / 64; ++hf) {
-              tma_load_2d(sk + pg * PAGE_BYTES + hf * HALF_BYTES, &tmK, &full[stage], hf * 64, y);
-              tma_load_2d(sk + K_BYTES + pg * PAGE_BYTES + hf * HALF_BYTES, &tmV, &full[stage], hf * 64, y);
-            }
-          }
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (!ok) {
-        for (int s = 0; s < STAGES; ++s)
-          if (pending & (1u << s)) mbar_drain(&full[s], (armed_parity >> s) & 1u);
-      }
-    }
-    return;
-  }
-
-  // ------------------------------------------------------------ consumers
-  const int ga = lane >> 2, t4 = lane & 3;
-  int stage = 0, qs = 0;
-  uint32_t phase = 0, qphase = 0;
-  while (true) {
-    bool ok = mbar_wait(&uq_full[qs], qphase, abort_flag, p.status);
-    if (!__all_sync(0xffffffffu, ok)) break;
-    const int u = uq[qs];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&uq_empty[qs]);
-    if (++qs == UQ) {
-      qs = 0;
-      qphase ^= 1u;
-    }
-    if (u >= total) break;
-    const Unit w = unit_info(p, cpre, dpre, u);
-
-    // Q fragments (A operand, rows ga / ga+8 of this warp's 16 rows)
-    uint32_t qa[D / 16][4];
-    int lim_a, lim_b;
-    const __nv_bfloat16 *qra, *qrb;
-    bool oka, okb;
-    if (w.kind == 0) {
-      const int ra = warp * 16 + ga, rb = ra + 8;
-      oka = ra < w.nrows;
-      okb = rb < w.nrows;
-      qra = p.q + (static_cast<size_t>(w.row0 + (oka ? ra : 0)) * p.n_q + w.head) * D;
-      qrb = p.q + (static_cast<size_t>(w.row0 + (okb ? rb : 0)) * p.n_q + w.head) * D;
-      lim_a = w.pos0 + ra;
-      lim_b = w.pos0 + rb;
-    } else {
-      oka = ga < p.grp;
-      okb = ga + 8 < p.grp;
-      const size_t base = static_cast<size_t>(w.row0) * p.n_q + w.head * p.grp;
-      qra = p.q + (base + (oka ? ga : 0)) * D;
-      qrb = p.q + (base + (okb ? ga + 8 : 0)) * D;
-      lim_a = lim_b = w.key_end - 1;
-    }
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      qa[kk][0] = ld_q2(qra, 16 * kk + 2 * t4, oka);
-      qa[kk][1] = ld_q2(qrb, 16 * kk + 2 * t4, okb);
-      qa[kk][2] = ld_q2(qra, 16 * kk + 8 + 2 * t4, oka);
-      qa[kk][3] = ld_q2(qrb, 16 * kk + 8 + 2 * t4, okb);
-    }
-    float o[D / 8][4];
-#pragma unroll
-    for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-    const int warp_pos_max = w.kind == 0 ? w.pos0 + min(warp * 16 + 15, w.nrows - 1) : w.key_end - 1;
-    const bool warp_rows = w.kind == 1 || warp * 16 < w.nrows;
-
-    bool unit_ok = true;
-    for (int kb0 = w.key_begin; kb0 < w.key_end; kb0 += KB) {
-      bool fok = mbar_wait(&full[stage], phase, abort_flag, p.status);
-      if (!__all_sync(0xffffffffu, fok)) {
-        unit_ok = false;
-        break;
-      }
-      uint8_t* sk = smem + stage * STAGE_BYTES;
-      const bool tail = kb0 + KB > w.key_end;
-      if (tail) {
-        // keys past key_end may hold uninitialised memory: zero their V rows
-        // so that P = 0 never meets a NaN in the PV product
-        consumer_sync();
-        const int first = w.key_end - kb0;
-        uint4* vb = reinterpret_cast<uint4*>(sk + K_BYTES);
-        for (int i = tid; i < (KB - first) * (D / 8); i += kConsumers) {
-          const int key = first + i / (D / 8), c = i % (D / 8);
-          vb[blk_off<D>(key, c) / 16] = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        consumer_sync();
-      }
-      const uint32_t kbase = smem_u32(sk), vbase = kbase + K_BYTES;
-      if (w.kind == 0) {
-        if (warp_rows && kb0 <= warp_pos_max)
-          warp_block<D, 4>(kbase, vbase, 0, kb0, qa, o, m, l, lim_a, lim_b, p.scale_log2, lane);
-      } else {
-        if (kb0 + warp * 16 < w.key_end)
-          warp_block<D, 1>(kbase, vbase, warp, kb0, qa, o, m, l, lim_a, lim_b, p.scale_log2, lane);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
-      if (++stage == STAGES) {
-        stage = 0;
-        phase ^= 1u;
-      }
-    }
-    if (!unit_ok) break;
-
-    // full row sums over the quad
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
-      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
-    }
-    if (w.kind == 0) {
-      // chunk tile: normalise and store this warp's rows
-      const int ra = warp * 16 + ga, rb = ra + 8;
-      const float ia = l[0] > 0.f ? 1.f / l[0] : 0.f, ib = l[1] > 0.f ? 1.f / l[1] : 0.f;
-      __nv_bfloat16* outa = p.out + static_cast<size_t>(w.row0 + ra) * p.n_q * D + w.head * D;
-      __nv_bfloat16* outb = p.out + static_cast<size_t>(w.row0 + rb) * p.n_q * D + w.head * D;
-#pragma unroll
-      for (int j = 0; j < D / 8; ++j) {
-        const int col = 8 * j + 2 * t4;
-        if (ra < w.nrows)
-          *reinterpret_cast<uint32_t*>(outa + col) = pack_bf16x2(o[j][0] * ia, o[j][1] * ia);
-        if (rb < w.nrows)
-          *reinterpret_cast<uint32_t*>(outb + col) = pack_bf16x2(o[j][2] * ib, o[j][3] * ib);
-      }
-      continue;
-    }
-
-    // decode unit: merge the four warps (each saw every 4th page)
-    float* mw = merge + warp * REC_FLOATS;
-    consumer_sync();  // previous unit's readers of `merge` are done
-#pragma unroll
-    for (int j = 0; j < D / 8; ++j) {
-      const int col = 8 * j + 2 * t4;
-      mw[ga * D + col] = o[j][0];
-      mw[ga * D + col + 1] = o[j][1];
-      mw[(ga + 8) * D + col] = o[j][2];
-      mw[(ga + 8) * D + col + 1] = o[j][3];
-    }
-    if (t4 == 0) {
-      mw[16 * D + ga] = m[0];
-      mw[16 * D + ga + 8] = m[1];
-      mw[16 * D + 16 + ga] = l[0];
-      mw[16 * D + 16 + ga + 8] = l[1];
-    }
-    consumer_sync();
-    const int nout = p.grp * D;
-    __nv_bfloat16* orow = p.out + static_cast<size_t>(w.row0) * p.n_q * D + w.head * p.grp * D;
-    float* rec = p.partials + static_cast<size_t>(w.rec) * REC_FLOATS;
-    for (int i = tid; i < nout; i += kConsumers) {
-      const int r = i / D, c = i % D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int v = 0; v < 4; ++v) M = fmaxf(M, merge[v * REC_FLOATS + 16 * D + r]);
-      const float Mu = M == -INFINITY ? 0.f : M;
-      float L = 0.f, O = 0.f;
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const float sc = exp2f(merge[v * REC_FLOATS + 16 * D + r] - Mu);
-        L += merge[v * REC_FLOATS + 16 * D + 16 + r] * sc;
-        O += merge[v * REC_FLOATS + r * D + c] * sc;
-      }
-      if (w.nsplit == 1) {
-        orow[i] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
-      } else {
-        rec[r * D + c] = O;
-        if (c == 0) {
-          rec[16 * D + r] = M;
-          rec[16 * D + 16 + r] = L;
-        }
-      }
-    }
-    if (w.nsplit == 1) continue;
-    __threadfence();
-    consumer_sync();
-    if (tid == 0) {
-      int* cnt = p.combine_counters + w.seq * p.n_kv + w.head;
-      const int old = atomicAdd(cnt, 1);
-      *last_flag = old == w.nsplit - 1;
-      if (old == w.nsplit - 1) *cnt = 0;
-    }
-    consumer_sync();
-    if (*last_flag) {
-      __threadfence();
-      // combine every split of this (row, kv head) in split order
-      const float* rec0 = p.partials + static_cast<size_t>(w.rec - (w.key_begin / SPLIT) * p.n_kv) * REC_FLOATS;
-      for (int i = tid; i < nout; i += kConsumers) {
-        const int r = i / D, c = i % D;
-        float M = -INFINITY;
-        for (int sp = 0; sp < w.nsplit; ++sp)
-          M = fmaxf(M, __ldcg(rec0 + static_cast<size_t>(sp) * p.n_kv * REC_FLOATS + 16 * D + r));
-        float L = 0.f, O = 0.f;
-        for (int sp = 0; sp < w.nsplit; ++sp) {
-          const float* rs = rec0 + static_cast<size_t>(sp) * p.n_kv * REC_FLOATS;
-          const float sc = exp2f(__ldcg(rs + 16 * D + r) - M);
-          L += __ldcg(rs + 16 * D + 16 + r) * sc;
-          O += __ldcg(rs + r * D + c) * sc;
-        }
-        orow[i] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
-      }
-    }
-  }
-}
-
 
 // ---------------------------------------------------------------- decode rows
 // HBM path.  Each warp owns whole units -- one decode row x one kv head (its
@@ -710,12 +317,12 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
         const int first = key_end - key0;
         for (int i = lane; i < (16 - first) * (D / 8); i += 32) {
           const int key = first + i / (D / 8), c = i % (D / 8);
-          vb[blk_off<D>(key, c) / 16] = make_uint4(0, 0, 0, 0);
+          vb[blk_off(key, c) / 16] = make_uint4(0, 0, 0, 0);
         }
         __syncwarp();
       }
       const uint32_t kb = smem_u32(st);
-      warp_block<D, 1>(kb, kb + PAGE_BYTES, 0, key0, qa, o, m, l, lim, lim, p.scale_log2, lane);
+      warp_page<D>(kb, kb + PAGE_BYTES, key0, qa, o, m, l, lim, p.scale_log2, lane);
       // slot consumed.  Reads are complete (their results fed the MMAs); the
       // zeroing writes of a tail page must be ordered before the next TMA write.
       if (tail) fence_proxy_async_smem();
@@ -884,11 +491,8 @@ hb_status attention_launch_d(const DeviceCtx& ctx, const void* q, const hb_devic
   static bool attr_set[64] = {};
   if (!attr_set[ctx.device]) {
     hb_status st = cuda_status(
-        cudaFuncSetAttribute(attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, AC<D>::SMEM),
-        "cudaFuncSetAttribute(attention)");
-    if (st != HB_OK) return st;
-    st = cuda_status(cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DC<D>::SMEM),
-                     "cudaFuncSetAttribute(decode)");
+        cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DC<D>::SMEM),
+        "cudaFuncSetAttribute(decode)");
     if (st != HB_OK) return st;
     attr_set[ctx.device] = true;
   }
