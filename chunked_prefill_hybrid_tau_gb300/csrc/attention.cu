@@ -423,14 +423,21 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
 // two persistent kernels run at the same time on disjoint SMs: the chunk
 // kernel on a side stream forked from and joined back into the caller's
 // stream.  Cost model (GB300, measured):
-//   chunk : t_c(n) = max(W / n, one tile), W = pairs x q heads / kChunkRate
-//           SM-us, a 128-row tile costing (mean keys per chunk row + 64) x
-//           128 / kChunkRate us;
-//   decode: t_d(n) = bytes / min(kDecodeBw, n x kDecodeBwPerSm).
-// The split is the largest chunk share within 2% of the best
-// max(t_c, t_d).  It only moves work between SMs: every row's result is
-// the same for any split.
-constexpr double kChunkRate = 5900.0;       // query-key pairs x heads per us per SM, d_head 128
+//   chunk : U = 128-row tiles x q heads units of about kUnitUs + (key blocks
+//           per tile) x kBlockUs each (key blocks over all tiles ~ pairs /
+//           128^2 + rows / 128), taken heaviest first, so on n SMs the
+//           makespan is about W / n + half a unit, and at least the heaviest
+//           unit;
+//   decode: the larger of bytes / min(kDecodeBw, n x kDecodeBwPerSm) and
+//           ceil(units / (8 warps x n)) x kSplitUs, with units ~ 1.1 x
+//           pairs / SPLIT x n_kv (one warp streams one SPLIT-key unit).
+// The split is the middle of the chunk shares within 2% of the best
+// max(t_c, t_d) (the decode's one-round boundary is sharp), or none when
+// running the two one after the other is estimated faster.  It only moves
+// work between SMs: every row's result is the same for any split.
+constexpr double kUnitUs = 8.0;             // per chunk unit, d_head 128
+constexpr double kBlockUs = 1.5;            // per 128-key block of a chunk unit, d_head 128
+constexpr double kSplitUs = 50.0;           // one full decode split on one warp, d_head 128
 constexpr double kDecodeBwPerSm = 55000.0;  // bytes per us per SM
 constexpr double kDecodeBw = 6.2e6;         // bytes per us, whole GPU
 
@@ -462,27 +469,39 @@ int chunk_sms(const DeviceCtx& ctx, const hb_device_plan& plan, const hb_layer_d
   const int S = ctx.num_sms;
   if (plan.chunk_pairs <= 0 || plan.decode_pairs <= 0 || plan.chunk_rows <= 0 || S < 4) return 0;
   const double dscale = dm.d_head / 128.0;
-  const double work_c = static_cast<double>(plan.chunk_pairs) * dm.n_q * dscale / kChunkRate;
-  const double mean_keys = static_cast<double>(plan.chunk_pairs) / static_cast<double>(plan.chunk_rows);
-  const double t_tile = (mean_keys + 64.0) * 128.0 * dscale / kChunkRate;
+  const double blk = kBlockUs * (0.5 + 0.5 * dscale);
+  const double rows = static_cast<double>(plan.chunk_rows);
+  const double tiles = ceil(rows / 128.0);
+  const double units_c = tiles * dm.n_q;
+  const double blocks = static_cast<double>(plan.chunk_pairs) / 16384.0 + rows / 128.0;
+  const double t_unit = kUnitUs + blocks / tiles * blk;
+  const double t_max = t_unit + (tiles - 1.0) / 2.0 * blk;
+  const double work_c = units_c * t_unit;
   const double bytes_d = static_cast<double>(plan.decode_pairs) * dm.n_kv * dm.d_head * 4.0;
-  auto t_chunk = [&](int n) { return work_c / n > t_tile ? work_c / n : t_tile; };
+  const double units_d = 1.1 * static_cast<double>(plan.decode_pairs) / SPLIT * dm.n_kv;
+  auto t_chunk = [&](int n) {
+    if (units_c <= n) return t_max;
+    const double t = work_c / n + 0.5 * t_unit;
+    return t > t_max ? t : t_max;
+  };
   auto t_decode = [&](int n) {
     const double bw = n * kDecodeBwPerSm < kDecodeBw ? n * kDecodeBwPerSm : kDecodeBw;
-    return bytes_d / bw;
+    const double t_bw = bytes_d / bw;
+    const double t_units = ceil(units_d / (kDecWarps * n)) * kSplitUs * dscale;
+    return t_bw > t_units ? t_bw : t_units;
   };
+  auto t_both = [&](int n) { return t_chunk(n) > t_decode(S - n) ? t_chunk(n) : t_decode(S - n); };
   double best = 1e300;
-  for (int n = 1; n < S; ++n) {
-    const double t = t_chunk(n) > t_decode(S - n) ? t_chunk(n) : t_decode(S - n);
-    if (t < best) best = t;
-  }
+  for (int n = 1; n < S; ++n)
+    if (t_both(n) < best) best = t_both(n);
   if (best >= t_chunk(S) + t_decode(S)) return 0;
-  int nc = 1;
-  for (int n = 1; n < S; ++n) {
-    const double t = t_chunk(n) > t_decode(S - n) ? t_chunk(n) : t_decode(S - n);
-    if (t <= best * 1.02) nc = n;
-  }
-  return nc;
+  int lo = S, hi = 0;
+  for (int n = 1; n < S; ++n)
+    if (t_both(n) <= best * 1.02) {
+      lo = n < lo ? n : lo;
+      hi = n;
+    }
+  return (lo + hi) / 2;
 }
 
 template <int D>

@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // lazily raise the maximum; rescale O (in TMEM) and l when it moves
         const bool raise = mx > m_used + kRescale;
         const float m_new = raise ? mx : m_used;
-        const float alpha = raise ? exp2f(m_used - m_new) : 1.f;
+        const float alpha = raise ? ex2_approx(m_used - m_new) : 1.f;
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
           // the previous PV block must be complete before O is touched
           bool pok = mbar_wait(pv_done, (J + j - 1) & 1, abort_flag, p.status);
@@ -528,8 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[HK / 2];
 #pragma unroll
         for (int c = 0; c < HK / 2; ++c) {
-          const float a0 = exp2f(__uint_as_float(sv[2 * c]) - m_used);
-          const float a1 = exp2f(__uint_as_float(sv[2 * c + 1]) - m_used);
+          const float a0 = ex2_approx(__uint_as_float(sv[2 * c]) - m_used);
+          const float a1 = ex2_approx(__uint_as_float(sv[2 * c + 1]) - m_used);
           rs += a0 + a1;
           pk[c] = pack_bf16x2(a0, a1);
         }
