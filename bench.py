@@ -438,12 +438,13 @@ def run_hb(args, world, rank, local):
         achieved, peak, unit = f_dom / dur / 1e12, peaks["bf16_tflops"], "TFLOP/s"
     else:
         achieved, peak, unit = b_dom / dur / 1e9, peaks["hbm_gbs"], "GB/s"
-    traffic = None
-    prof_path = os.path.join(ROOT, "profiles", "traffic.json")
+    traffic = None  # measured DRAM bytes per launch (ncu), when recorded for this kernel and workload
+    prof_path = os.path.join(ROOT, "profiles", "traffic.txt")
     if os.path.exists(prof_path):
-        tr = json.load(open(prof_path))
-        if tr.get("workload") == WORKLOAD and name in tr.get("kernels", {}):
-            traffic = tr["kernels"][name]
+        entries = dict(ln.split(None, 1) for ln in open(prof_path).read().splitlines()
+                       if ln.strip() and not ln.startswith("#"))
+        if entries.get("workload", "").strip() == WORKLOAD and name in entries:
+            traffic = float(entries[name])
 
     n_dec = sum(1 for r in st.decodes)
     c = T - n_dec
