@@ -48,6 +48,12 @@ def parse():
     ap.add_argument("--decodes", type=int, default=32)
     ap.add_argument("--sweep", action="store_true",
                     help="token-budget sweep (tau 64..4096, 64 decodes, c = tau - 64): one JSON line per tau")
+    ap.add_argument("--calibrate", type=float, default=None, metavar="SLO_MS",
+                    help="pick tau from a time-per-iteration SLO: the largest swept tau whose --layers-layer "
+                         "iteration fits the SLO, next to the c* closed form")
+    ap.add_argument("--layers", type=int, default=32, help="layers per iteration for --calibrate")
+    ap.add_argument("--chunk-study", action="store_true",
+                    help="prefill time of 8K and 32K prompts chunked at C = 128..2048 against unchunked")
     return ap.parse_args()
 
 
@@ -479,16 +485,18 @@ def run_hb(args, world, rank, local):
     return 0
 
 
-def run_sweep(args):
+def run_sweep(args, taus=None, emit=True):
     """ms/iter, tokens/s and roofline fraction against the token budget on the
     Mistral-7B-shaped layer: 64 decodes with contexts uniform in [512, 8192]
-    plus a chunk of c = tau - 64 tokens at offset 0 of an 8192-token prompt."""
+    plus a chunk of c = tau - 64 tokens at offset 0 of an 8192-token prompt.
+    Returns the per-tau records (and prints them as JSON lines if emit)."""
     import torch
     import chunked_prefill_hybrid_tau_gb300 as hb
     from chunked_prefill_hybrid_tau_gb300 import costs
     from workloads import device as wd
     lib = hb.lib()
-    taus = [64, 128, 256, 512, 1024, 2048, 4096]
+    taus = taus or [64, 128, 256, 512, 1024, 2048, 4096]
+    records = []
     w = make_workload(max(taus), 64)
     st, dims = w.state, w.dims
     max_pos = 8192 + max(taus) + 1
@@ -546,24 +554,112 @@ def run_sweep(args):
         t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
         T = runner.n_rows
         c = T - 64
-        print(json.dumps({
+        rec = {
             "sweep": "tau", "tau": tau, "rows": T, "chunk_tokens": c, "decodes": 64, "ms_per_step": 1e3 * t_step,
             "tokens_per_s": T / t_step, "t_roof_ms": 1e3 * t_roof, "roofline_frac": t_roof / t_step,
             "flops": flops, "bytes": byts, "intensity_flop_per_byte": flops / byts,
             "intensity_page": costs.page_intensity(c, 64, dims.params_per_layer, 2, 1, dims.n_kv, dims.d_head, s_bar),
-            "stages_ms": {k: round(float(v), 5) for k, v in zip(costs.STAGES, stage_ms)}}), flush=True)
+            "stages_ms": {k: round(float(v), 5) for k, v in zip(costs.STAGES, stage_ms)}}
+        records.append(rec)
+        if emit:
+            print(json.dumps(rec), flush=True)
     # the page's optimal chunk for this machine balance (I* = peak FLOP/s / peak B/s)
     psi = dims.params_per_layer
     c_star = balance / (2.0 * psi) * (2 * psi + 2.0 * dims.n_kv * dims.d_head * s_bar * 64) - 64
-    print(json.dumps({"sweep": "c_star", "machine_balance_flop_per_byte": balance, "c_star_tokens": c_star,
-                      "s_bar": s_bar}), flush=True)
+    cs = {"sweep": "c_star", "machine_balance_flop_per_byte": balance, "c_star_tokens": c_star, "s_bar": s_bar}
+    records.append(cs)
+    if emit:
+        print(json.dumps(cs), flush=True)
+    return records
+
+
+def run_calibrate(args):
+    """The scheduling method's tau calibration (the Sarathi-Serve reading notes'
+    profiling step): measure the iteration time T(tau) over a range of token
+    budgets, then take the largest tau whose time fits the per-iteration SLO.
+    T(tau) is the measured single-layer time times --layers (the layers are
+    identical in shape).  Prints the profile and one summary line."""
+    taus = [64, 128, 192, 256, 384, 512, 640, 768, 1024, 1536, 2048, 3072, 4096]
+    recs = run_sweep(args, taus, emit=False)
+    prof = [r for r in recs if r["sweep"] == "tau"]
+    c_star = [r for r in recs if r["sweep"] == "c_star"][0]
+    for r in prof:
+        print(json.dumps({"calibrate": "profile", "tau": r["tau"], "layer_ms": r["ms_per_step"],
+                          "iteration_ms": r["ms_per_step"] * args.layers, "tokens_per_s": r["tokens_per_s"],
+                          "roofline_frac": r["roofline_frac"]}), flush=True)
+    fits = [r for r in prof if r["ms_per_step"] * args.layers <= args.calibrate]
+    base = prof[0]["ms_per_step"]
+    knee = next((r["tau"] for r in prof if r["ms_per_step"] >= 1.1 * base), None)
+    best = max(fits, key=lambda r: r["tau"]) if fits else None
+    print(json.dumps({"calibrate": "tau", "slo_ms": args.calibrate, "layers": args.layers,
+                      "tau": best["tau"] if best else None,
+                      "iteration_ms": best["ms_per_step"] * args.layers if best else None,
+                      "tau_knee_10pct": knee, "c_star_tokens": c_star["c_star_tokens"],
+                      "decodes": 64}), flush=True)
+    return 0
+
+
+def run_chunk_study(args):
+    """Prefill cost of chunking (the pages' chunk-size overhead claims): one
+    prompt of P tokens through the Mistral-7B-shaped layer in chunks of C,
+    every chunk attending to the KV the earlier chunks wrote, against one
+    unchunked pass.  Time is the whole prefill, best of three."""
+    import torch
+    import chunked_prefill_hybrid_tau_gb300 as hb
+    from workloads import device as wd
+    import workloads as wl
+    dims = wl.MISTRAL
+    lw = wd.layer_weights_random(dims, 4100)
+    gen = wd.device_generator(41)
+    for P in (8192, 32768):
+        x = wd.randn_bf16((P, dims.d_model), gen)
+        out = torch.empty_like(x)
+        rope = wd.rope_table_device(P + 1, dims)
+        num_pages = P // 16 + 8
+        kc = torch.zeros((num_pages, dims.n_kv, 16, dims.d_head), dtype=torch.bfloat16, device="cuda")
+        vc = torch.zeros_like(kc)
+        pool = list(range(num_pages))
+        results = {}
+        for C in [P, 2048, 1024, 512, 256, 128]:
+            plans = []
+            done, pages, fp = 0, [], pool
+            while done < P:
+                hp = hb.hb_plan_batch([], [], [P], [done], [pages], fp, C, C)
+                pages, fp = hp.pf_pages[0], hp.free_pool
+                plans.append((done, int(hp.pf_take[0]), hb.DevicePlan(hp)))
+                done += int(hp.pf_take[0])
+            ws = wd.workspace(hb.hb_layer_workspace_bytes(dims, C, 1, P))
+            best = None
+            for _ in range(3):
+                s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                s0.record()
+                for d0, t, dp in plans:
+                    hb.hb_layer_forward(lw, dims, dp, rope, P + 1, x[d0:d0 + t], out[d0:d0 + t], kc, vc, P, ws)
+                s1.record()
+                torch.cuda.synchronize()
+                ms = s0.elapsed_time(s1)
+                best = ms if best is None else min(best, ms)
+            hb.hb_check_status()
+            results[C] = best
+            print(json.dumps({"chunk_study": "prefill", "prompt": P, "chunk": C, "chunks": len(plans), "ms": best,
+                              "tokens_per_s": P / (best / 1e3),
+                              "overhead_vs_unchunked": best / results[P] - 1.0}), flush=True)
+            del ws, plans
+        del x, out, kc, vc
+        torch.cuda.empty_cache()
     return 0
 
 
 def main():
     args = parse()
     if args.sweep:
-        return run_sweep(args)
+        run_sweep(args)
+        return 0
+    if args.calibrate is not None:
+        return run_calibrate(args)
+    if args.chunk_study:
+        return run_chunk_study(args)
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         rc = run_reference(args, world, rank)
