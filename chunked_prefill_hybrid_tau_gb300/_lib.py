@@ -62,6 +62,14 @@ PROTOTYPES = {
     "hb_version": (i32, []),
     "hb_plan_batch": (C.c_int, [C.POINTER(hb_request), i32, C.POINTER(hb_request), i32, C.POINTER(hb_page_pool),
                                 i32, i32, i32, C.POINTER(hb_plan)]),
+    "hb_sched_create": (C.c_int, [i32, i32, i32, p_i32, i32, C.POINTER(vp)]),
+    "hb_sched_destroy": (None, [vp]),
+    "hb_sched_add": (C.c_int, [vp, i32, i32, p_i32]),
+    "hb_sched_plan": (C.c_int, [vp, C.POINTER(hb_plan), p_i32]),
+    "hb_sched_commit": (C.c_int, [vp]),
+    "hb_sched_info": (C.c_int, [vp, i32, p_i32, p_i32, p_i32, p_i32]),
+    "hb_sched_active": (i32, [vp]),
+    "hb_sched_free_pages": (i32, [vp]),
     "hb_rope_table": (C.c_int, [vp, i32, i32, C.c_double, vp]),
     "hb_rmsnorm": (C.c_int, [vp, vp, vp, i32, i32, C.c_float, vp]),
     "hb_kv_append": (C.c_int, [vp, i32, vp, vp, vp, i32, C.POINTER(hb_layer_dims), vp, vp, vp, i32, vp]),

@@ -164,6 +164,85 @@ def hb_plan_batch(dec_ctx, dec_pages, pf_len, pf_done, pf_pages, free_pool, tau,
     raise HBError(L.HB_ERR_CAPACITY, "hb_plan_batch: capacity retry failed")
 
 
+# ---------------------------------------------------------------- iteration driver
+class Scheduler:
+    """The scheduling loop around the planner (include/hb.h, hb_sched):
+    add requests, then per iteration plan() -> run the forward -> commit()."""
+
+    def __init__(self, tau, chunk, pool, page_size=16):
+        self._lib = lib()
+        self.h = C.c_void_p()
+        arr = np.ascontiguousarray(np.asarray(pool, np.int32))
+        _check(self._lib.hb_sched_create(int(tau), int(chunk), int(page_size), arr.ctypes.data_as(L.p_i32),
+                                         int(arr.size), C.byref(self.h)), "hb_sched_create")
+        self.tau, self.chunk = int(tau), int(chunk)
+        self.caps = [max(int(tau), 1), 16, 16, 16]  # rows, seqs, max_pages, prefills
+
+    def close(self):
+        if self.h:
+            self._lib.hb_sched_destroy(self.h)
+            self.h = C.c_void_p()
+
+    def __del__(self):
+        self.close()
+
+    def add(self, prompt_len, max_new) -> int:
+        rid = C.c_int32()
+        _check(self._lib.hb_sched_add(self.h, int(prompt_len), int(max_new), C.byref(rid)), "hb_sched_add")
+        return int(rid.value)
+
+    def plan(self):
+        """-> (HostPlan, row_req): the next iteration and each row's request id."""
+        for _attempt in range(4):
+            rc, sc, mp, pc = self.caps
+            out = {k: np.zeros(rc, np.int32) for k in ("row_seq", "row_pos", "slot_mapping")}
+            out.update({k: np.zeros(sc, np.int32) for k in ("seq_pos0", "seq_kv_len", "seq_kind", "seq_req")})
+            out["seq_q_start"] = np.zeros(sc + 1, np.int32)
+            out["block_table"] = np.zeros(sc * mp, np.int32)
+            out["pf_take"] = np.zeros(pc, np.int32)
+            out["pf_finished"] = np.zeros(pc, np.int32)
+            row_req = np.zeros(rc, np.int32)
+            P = L.hb_plan()
+            P.row_cap, P.seq_cap, P.max_pages, P.pf_cap = rc, sc, mp, pc
+            for k, a in out.items():
+                setattr(P, k, a.ctypes.data_as(L.p_i32))
+            st = self._lib.hb_sched_plan(self.h, C.byref(P), row_req.ctypes.data_as(L.p_i32))
+            if st == L.HB_ERR_CAPACITY:
+                self.caps = [max(rc, P.need_rows), max(sc, P.need_seqs), max(mp, P.need_max_pages),
+                             max(pc, 2 * pc)]
+                continue
+            _check(st, "hb_sched_plan")
+            T, S = P.n_rows, P.n_seqs
+            n_pf = int(np.count_nonzero(out["seq_kind"][:S] == 1))
+            hp = HostPlan(
+                row_seq=out["row_seq"][:T].copy(), row_pos=out["row_pos"][:T].copy(),
+                slot_mapping=out["slot_mapping"][:T].copy(), seq_q_start=out["seq_q_start"][:S + 1].copy(),
+                seq_pos0=out["seq_pos0"][:S].copy(), seq_kv_len=out["seq_kv_len"][:S].copy(),
+                seq_kind=out["seq_kind"][:S].copy(), seq_req=out["seq_req"][:S].copy(),
+                block_table=out["block_table"][:S * mp].reshape(S, mp).copy(),
+                pf_take=out["pf_take"][:pc].copy(), pf_finished=out["pf_finished"][:pc].copy(),
+                dec_pages=[], pf_pages=[], free_pool=[], pages_used=int(P.pages_used),
+                over_budget=int(P.over_budget), decode_pairs=int(P.decode_pairs), chunk_pairs=int(P.chunk_pairs),
+                chunk_rows=int(P.chunk_rows))
+            del n_pf
+            return hp, row_req[:T].copy()
+        raise HBError(L.HB_ERR_CAPACITY, "hb_sched_plan: capacity retry failed")
+
+    def commit(self):
+        _check(self._lib.hb_sched_commit(self.h), "hb_sched_commit")
+
+    def info(self, rid):
+        v = [C.c_int32() for _ in range(4)]
+        _check(self._lib.hb_sched_info(self.h, int(rid), *[C.byref(x) for x in v]), "hb_sched_info")
+        return tuple(int(x.value) for x in v)  # state, cached, generated, pages
+
+    def active(self) -> int:
+        return int(self._lib.hb_sched_active(self.h))
+
+    def free_pages(self) -> int:
+        return int(self._lib.hb_sched_free_pages(self.h))
+
+
 # ---------------------------------------------------------------- device plan
 class DevicePlan:
     """Device copy of a plan's kernel-facing arrays in one int32 buffer

@@ -157,6 +157,48 @@ hb_status hb_plan_batch(hb_request* decodes, int32_t n_dec, hb_request* prefills
                         hb_plan* plan);
 
 /* ------------------------------------------------------------------------
+ * hb_sched - the iteration driver: the scheduling loop of the Sarathi-Serve
+ * reading notes (section 3.4) around hb_plan_batch.  Host only, opaque
+ * state, not thread-safe.
+ *   hb_sched_create : budget tau, chunk size, page size and the free page
+ *                     ids (FIFO) the scheduler owns from then on.
+ *   hb_sched_add    : a request of prompt_len tokens that generates max_new
+ *                     tokens; queued behind the other waiting prompts.
+ *                     Refused between hb_sched_plan and hb_sched_commit.
+ *   hb_sched_plan   : packs the next iteration into `plan` exactly as
+ *                     hb_plan_batch does (all running decodes in the order
+ *                     their prompts completed, then one chunk per waiting
+ *                     prompt in FIFO order under tau), and writes the request
+ *                     id of every row to row_req[row_cap] (may be NULL).
+ *                     plan->n_rows == 0 when nothing is active.  Errors as
+ *                     hb_plan_batch (CAPACITY reports sizes; OUT_OF_PAGES:
+ *                     there is no preemption); on error the state is
+ *                     unchanged.
+ *   hb_sched_commit : after the iteration's forward: each decode has one
+ *                     more cached token and one more new token; each chunk
+ *                     advanced its prompt; a completed prompt has produced
+ *                     its first new token and starts decoding; a request
+ *                     with max_new tokens is finished and its pages go to
+ *                     the back of the free pool in page order.
+ *   hb_sched_info   : state (0 prefilling, 1 decoding, 2 finished), cached
+ *                     tokens, new tokens so far and pages held (any output
+ *                     may be NULL).
+ *   hb_sched_active : requests not finished.  hb_sched_free_pages: pool size.
+ * A request holds at most ceil((prompt_len + max_new - 1) / page_size) pages.
+ * ---------------------------------------------------------------------- */
+typedef struct hb_sched hb_sched;
+hb_status hb_sched_create(int32_t tau, int32_t chunk, int32_t page_size, const int32_t* pages, int32_t n_pages,
+                          hb_sched** out);
+void hb_sched_destroy(hb_sched* s);
+hb_status hb_sched_add(hb_sched* s, int32_t prompt_len, int32_t max_new, int32_t* id);
+hb_status hb_sched_plan(hb_sched* s, hb_plan* plan, int32_t* row_req);
+hb_status hb_sched_commit(hb_sched* s);
+hb_status hb_sched_info(const hb_sched* s, int32_t id, int32_t* state, int32_t* cached, int32_t* generated,
+                        int32_t* n_pages);
+int32_t hb_sched_active(const hb_sched* s);
+int32_t hb_sched_free_pages(const hb_sched* s);
+
+/* ------------------------------------------------------------------------
  * Device view of a plan (device pointers; copies of the hb_plan arrays).
  * ---------------------------------------------------------------------- */
 typedef struct hb_device_plan {

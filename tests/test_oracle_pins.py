@@ -585,3 +585,123 @@ def test_bf16_storage_variant_is_close_to_fp32_and_not_equal():
     rl2 = np.linalg.norm(a - b) / np.linalg.norm(a)
     assert 0 < rl2 < 1e-2
     assert np.all((b.view(np.uint32) & 0xFFFF) == 0)
+
+
+# ---------------------------------------------------------------- iteration driver
+def _run_loop(loop, arrivals, max_iters=10_000):
+    """arrivals: {iteration: [(prompt_len, max_new), ...]}; returns per-iteration (plan, row_req)."""
+    hist = []
+    it = 0
+    while it < max_iters:
+        for pl, mn in arrivals.get(it, []):
+            loop.add(pl, mn)
+        if loop.active() == 0 and it > max(arrivals, default=0):
+            break
+        p, rr = loop.plan()
+        hist.append((p, rr))
+        loop.commit()
+        it += 1
+    return hist
+
+
+def test_sched_loop_single_request_closed_form():
+    """A lone request: ceil(L / C) prefill iterations (C <= tau), then one
+    decode iteration per further token; positions 0..L + max_new - 2 each
+    processed once, in order."""
+    import oracle.sched as osch
+    for L, mn, C, tau in [(100, 3, 48, 64), (16, 1, 16, 16), (33, 5, 8, 8), (200, 10, 64, 512)]:
+        loop = osch.SchedLoop(tau, C, list(range(100)))
+        hist = _run_loop(loop, {0: [(L, mn)]})
+        assert len(hist) == -(-L // min(C, tau)) + mn - 1
+        pos = [q for p, rr in hist for q in p.row_pos]
+        assert pos == list(range(L + mn - 1))
+        r = loop.reqs[0]
+        assert r["state"] == osch.FINISHED and r["generated"] == mn and r["cached"] == L + mn - 1
+        assert sorted(loop.pool) == list(range(100))
+
+
+def test_sched_loop_conservation_and_pages():
+    """Random streams: every request is finished with max_new tokens, each
+    cached position is processed exactly once, no page is ever held twice,
+    and every page returns to the pool."""
+    import oracle.sched as osch
+    rng = np.random.default_rng(11)
+    for trial in range(25):
+        tau = int(rng.integers(8, 200))
+        C = int(rng.integers(4, 2 * tau))
+        n_pages = 400
+        loop = osch.SchedLoop(tau, C, list(rng.permutation(n_pages)))
+        arrivals = {}
+        for _ in range(int(rng.integers(1, 9))):
+            arrivals.setdefault(int(rng.integers(0, 12)), []).append((int(rng.integers(1, 120)),
+                                                                      int(rng.integers(1, 9))))
+        seen = {}
+        it = 0
+        while True:
+            for pl, mn in arrivals.get(it, []):
+                loop.add(pl, mn)
+            if loop.active() == 0 and it > max(arrivals):
+                break
+            p, rr = loop.plan()
+            assert p.n_rows <= tau or p.over_budget
+            for q, req in zip(p.row_pos, rr):
+                assert (req, q) not in seen
+                seen[(req, q)] = it
+            loop.commit()
+            held = [pg for r in loop.reqs for pg in r["pages"]]
+            assert len(set(held)) == len(held) and not set(held) & set(loop.pool)
+            assert len(held) + len(loop.pool) == n_pages
+            it += 1
+        for i, r in enumerate(loop.reqs):
+            assert r["state"] == osch.FINISHED and r["generated"] == r["max_new"]
+            assert sorted(q for (req, q) in seen if req == i) == list(range(r["prompt_len"] + r["max_new"] - 1))
+            # a position is processed only after all earlier positions of its request
+            its = [seen[(i, q)] for q in range(r["prompt_len"] + r["max_new"] - 1)]
+            assert its == sorted(its)
+        assert len(loop.pool) == n_pages
+
+
+def test_sched_loop_matches_replay_on_tiny_streams():
+    """Brute force on tiny streams: replaying the definition by hand --
+    decodes first in completion order, then FIFO chunks of min(C, rest,
+    budget left) -- gives the same row sets per iteration."""
+    import oracle.sched as osch
+    rng = np.random.default_rng(12)
+    for trial in range(60):
+        tau, C = int(rng.integers(2, 12)), int(rng.integers(1, 12))
+        reqs = [(int(rng.integers(1, 14)), int(rng.integers(1, 5))) for _ in range(int(rng.integers(1, 5)))]
+        loop = osch.SchedLoop(tau, C, list(range(64)))
+        for pl, mn in reqs:
+            loop.add(pl, mn)
+        # replay
+        state = [dict(pl=pl, mn=mn, cached=0, gen=0) for pl, mn in reqs]
+        waiting = list(range(len(reqs)))
+        running = []
+        while waiting or running:
+            p, rr = loop.plan()
+            want = [(i, state[i]["cached"]) for i in running]
+            n = len(running)
+            takes = {}
+            for i in waiting:
+                t = max(0, min(C, state[i]["pl"] - state[i]["cached"], tau - n))
+                if t:
+                    takes[i] = t
+                    want += [(i, state[i]["cached"] + k) for k in range(t)]
+                    n += t
+            assert list(zip(rr, p.row_pos)) == want
+            loop.commit()
+            nrun = []
+            for i in running:
+                state[i]["cached"] += 1
+                state[i]["gen"] += 1
+                if state[i]["gen"] < state[i]["mn"]:
+                    nrun.append(i)
+            nwait = []
+            for i in waiting:
+                state[i]["cached"] += takes.get(i, 0)
+                if state[i]["cached"] < state[i]["pl"]:
+                    nwait.append(i)
+                elif state[i]["mn"] > 1:
+                    state[i]["gen"] = 1
+                    nrun.append(i)
+            running, waiting = nrun, nwait

@@ -141,3 +141,66 @@ def test_config_packings_bit_exact():
     o, c = compare(([r.done for r in st.decodes], [r.pages for r in st.decodes], [4096], [1024],
                     [st.prefills[0].pages], st.free_pool, 512, 512))
     assert c.n_rows == 512 and list(c.pf_take) == [480]
+
+
+# ---------------------------------------------------------------- iteration driver
+def test_scheduler_matches_oracle_loop_bit_exact():
+    """The C iteration driver against the oracle loop on random streams with
+    arrivals between iterations: every iteration's plan arrays and row
+    request ids, and every request's state after each commit."""
+    import oracle.sched as osch
+    rng = np.random.default_rng(21)
+    for trial in range(30):
+        tau = int(rng.integers(4, 300))
+        C = int(rng.integers(1, 2 * tau))
+        pool = [int(v) for v in rng.permutation(600)]
+        c = B.Scheduler(tau, C, pool)
+        o = osch.SchedLoop(tau, C, pool)
+        arrivals = {}
+        for _ in range(int(rng.integers(1, 10))):
+            arrivals.setdefault(int(rng.integers(0, 15)), []).append((int(rng.integers(1, 200)),
+                                                                      int(rng.integers(1, 12))))
+        it = 0
+        while True:
+            for pl, mn in arrivals.get(it, []):
+                assert c.add(pl, mn) == o.add(pl, mn)
+            if o.active() == 0 and it > max(arrivals):
+                assert c.active() == 0
+                break
+            hc, rc = c.plan()
+            po, ro = o.plan()
+            assert list(rc) == ro
+            assert list(hc.row_pos) == po.row_pos and list(hc.slot_mapping) == po.slot_mapping
+            assert list(hc.seq_q_start) == po.seq_q_start and list(hc.seq_kv_len) == po.seq_kv_len
+            assert list(hc.seq_kind) == po.seq_kind and list(hc.seq_req) == po.seq_req
+            S = len(po.seq_pos0)
+            assert [list(r) for r in hc.block_table] == [row[:hc.max_pages] + [-1] * (hc.max_pages - len(row))
+                                                         if len(row) < hc.max_pages else row[:hc.max_pages]
+                                                         for row in po.block_table][:S]
+            c.commit()
+            o.commit()
+            for i, r in enumerate(o.reqs):
+                assert c.info(i) == (r["state"], r["cached"], r["generated"], len(r["pages"]))
+            assert c.free_pages() == len(o.pool)
+            it += 1
+        c.close()
+
+
+def test_scheduler_errors_leave_state_unchanged(lib):
+    s = B.Scheduler(32, 32, list(range(3)))  # three pages: room for one 48-token prompt
+    a = s.add(40, 2)
+    s.add(40, 2)
+    hp, rr = s.plan()
+    assert set(rr.tolist()) == {a} and hp.n_rows == 32  # the second prompt gets no tokens this iteration
+    with pytest.raises(B.HBError):
+        s.add(5, 1)  # refused between plan and commit
+    s.commit()
+    with pytest.raises(B.HBError) as e:
+        s.plan()  # both prompts need pages now: out of pages, no preemption
+    assert e.value.status == L.HB_ERR_OUT_OF_PAGES
+    assert s.info(a) == (0, 32, 0, 2) and s.free_pages() == 1
+    with pytest.raises(B.HBError):
+        s.commit()  # nothing planned
+    with pytest.raises(B.HBError):
+        s.info(7)
+    s.close()
