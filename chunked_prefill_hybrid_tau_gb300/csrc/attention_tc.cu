@@ -18,15 +18,17 @@
 //            is computed, a V stage when its PV block is;
 //   warp 1   MMA issuer (one thread), issuing whichever is ready first:
 //            S_j = Q K_j^T into one of two TMEM S buffers (K-major operands),
-//            or O += P_j V_j with P from shared memory (K-major) and V as an
-//            MN-major operand;
+//            or O += P_j V_j with P read from one of two TMEM P buffers and V
+//            as an MN-major shared-memory operand;
 //   warps 2-9 softmax, two threads per query row (warps 2-5 take keys 0..63
 //            of a block, warps 6-9 keys 64..127; the halves exchange the row
 //            maximum once per block): tcgen05.ld of the S half row, causal
 //            mask, online softmax in base 2 with a lazily updated maximum (O in
 //            TMEM is rescaled only when a row's maximum grows by more than 2^8),
-//            P written as bf16 into shared memory; finally O / l from TMEM to
-//            global memory, each thread its half of the head dimension.
+//            P written as bf16 into the block's TMEM P buffer (two buffers, so
+//            a block's P waits only for the PV of two blocks back); finally
+//            O / l from TMEM to global memory, each thread its half of the
+//            head dimension.
 // Every wait is bounded; an expired wait sets the status word and unwinds.
 #include <cuda_bf16.h>
 
@@ -53,19 +55,18 @@ struct TC {
   static constexpr int HALF_TILE = 128 * 128;            // 128 rows x 128 bytes
   static constexpr int Q_BYTES = HALVES * HALF_TILE;     // Q tile
   static constexpr int KV_BYTES = HALVES * HALF_TILE;    // K (or V) block of 128 keys
-  static constexpr int P_BYTES = 2 * HALF_TILE;          // 128 rows x 128 keys bf16
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = Q_BYTES;                  // K ring [NSTAGE]
   static constexpr int OFF_V = OFF_K + NSTAGE * KV_BYTES;  // V ring [NSTAGE]
-  static constexpr int OFF_P = OFF_V + NSTAGE * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NSTAGE * KV_BYTES;
   static constexpr int BAR_BYTES = 256;
   static constexpr int OFF_XCH = OFF_BAR + BAR_BYTES;    // row maxima / sums exchanged by the two halves
   static constexpr int XCH_BYTES = (2 * 2 * 128 + 2 * 128) * 4;
   static constexpr int OFF_PRE = OFF_XCH + XCH_BYTES;
   static constexpr int SMEM = OFF_PRE + (MAX_SEQS + 1) * 4 + 1024;
-  static constexpr uint32_t TMEM_COLS = 512;             // S0 | S1 | O
+  static constexpr uint32_t TMEM_COLS = 512;             // S0 | S1 | O | P0 | P1
   static constexpr uint32_t COL_O = 256;
+  static constexpr uint32_t COL_P = 384;                 // P_b (bf16, 2 keys per column) at COL_P + 64 b
 };
 
 struct TcParams {
@@ -119,6 +120,19 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// O (+)= A B^T with A (M x K bf16) read from tensor memory, B a shared-memory
+// descriptor; kind::f16, fp32 accumulate.  A: lane = row, column c holds
+// elements 2c (low half) and 2c + 1 of the row.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -158,7 +172,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
-  uint8_t* sP = smem + C::OFF_P;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* k_full = bar;                   // [NSTAGE]
   uint64_t* k_empty = bar + 2;              // [NSTAGE]
@@ -166,8 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_empty = bar + 5;
   uint64_t* s_full = bar + 6;               // [2]
   uint64_t* s_empty = bar + 8;              // [2]
-  uint64_t* p_full = bar + 10;
-  uint64_t* pv_done = bar + 11;             // one completion per PV block
+  uint64_t* p_full = bar + 25;              // [2] P_b stored (8 warps), once per use of buffer b
+  uint64_t* pv_done = bar + 27;             // [2] the PV that read P_b has completed
   uint64_t* o_empty = bar + 12;
   uint64_t* uq_full = bar + 13;             // [2]
   uint64_t* uq_empty = bar + 15;            // [2]
@@ -176,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* xsbar = bar + 20;               // row sums exchanged (once per unit)
   uint64_t* v_full = bar + 21;              // [NSTAGE]
   uint64_t* v_empty = bar + 23;             // [NSTAGE]
-  int* uq = reinterpret_cast<int*>(bar + 25);  // [2]
+  int* uq = reinterpret_cast<int*>(bar + 29);  // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(uq + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* xmax = reinterpret_cast<float*>(smem + C::OFF_XCH);  // [2 parity][2 half][128 rows]
@@ -211,8 +224,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&uq_full[i], 1);
       mbar_init(&uq_empty[i], 2 + kSoftWarps);
     }
-    mbar_init(p_full, kSoftWarps);
-    mbar_init(pv_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&p_full[b], kSoftWarps);
+      mbar_init(&pv_done[b], 1);
+    }
     mbar_init(o_empty, kSoftWarps);
     mbar_init(&xbar[0], kSoftWarps);
     mbar_init(&xbar[1], kSoftWarps);
@@ -367,7 +382,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) {
         ok = mbar_wait(q_full, nunit & 1, abort_flag, p.status);
         const uint32_t q_addr = smem_u32(sQ);
-        const uint32_t p_addr = smem_u32(sP);
         // S_js and PV_jp are issued in whatever order their inputs arrive
         int js = 0, jp = 0;
         bool o_free = false;
@@ -396,17 +410,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int gv = J + jp, st = gv % NSTAGE;
             // O of the previous unit has been read by the epilogue before the first PV
             if (!o_free) o_free = mbar_test(o_empty, (nunit & 1) ^ 1u);
-            if (o_free && mbar_test(p_full, gv & 1) && mbar_test(&v_full[st], (gv / NSTAGE) & 1)) {
+            const int pb = gv & 1;  // P buffer of this block; its use number is gv >> 1
+            if (o_free && mbar_test(&p_full[pb], (gv >> 1) & 1) && mbar_test(&v_full[st], (gv / NSTAGE) & 1)) {
               tc_fence_after();
               const uint32_t v_addr = smem_u32(sV + st * C::KV_BYTES);
 #pragma unroll
               for (int kk = 0; kk < TK / 16; ++kk) {
-                const uint64_t a = smem_desc_sw128(p_addr + (kk >> 2) * C::HALF_TILE + (kk & 3) * 32);
                 const uint64_t bdesc = smem_desc_sw128_mn(v_addr + kk * 2048, C::HALF_TILE, 1024);
-                mma_bf16(tmem + C::COL_O, a, bdesc, idPV, (jp > 0 || kk > 0) ? 1u : 0u);
+                mma_bf16_ts(tmem + C::COL_O, tmem + C::COL_P + pb * 64 + kk * 8, bdesc, idPV,
+                            (jp > 0 || kk > 0) ? 1u : 0u);
               }
               mma_commit(&v_empty[st]);
-              mma_commit(pv_done);
+              mma_commit(&pv_done[pb]);
               ++jp;
               progressed = true;
             }
@@ -503,7 +518,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float alpha = raise ? ex2_approx(m_used - m_new) : 1.f;
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
           // the previous PV block must be complete before O is touched
-          bool pok = mbar_wait(pv_done, (J + j - 1) & 1, abort_flag, p.status);
+          const int gp = J + j - 1;
+          bool pok = mbar_wait(&pv_done[gp & 1], (gp >> 1) & 1, abort_flag, p.status);
           if (!__all_sync(0xffffffffu, pok)) {
             ok = false;
             break;
@@ -534,19 +550,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[c] = pack_bf16x2(a0, a1);
         }
         l += rs;
-        // the previous PV block has finished reading the P tile
-        if (J + j > 0) {
-          bool pok = mbar_wait(pv_done, (J + j - 1) & 1, abort_flag, p.status);
+        // P of this block goes to TMEM buffer b = block & 1 once the PV that
+        // read the buffer two blocks ago has completed
+        const int gb = J + j, pb = gb & 1;
+        if (gb >= 2) {
+          bool pok = mbar_wait(&pv_done[pb], ((gb >> 1) - 1) & 1, abort_flag, p.status);
           if (!__all_sync(0xffffffffu, pok)) {
             ok = false;
             break;
           }
+          tc_fence_after();
         }
-        uint8_t* prow = sP + half * C::HALF_TILE + r * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)  // 16-byte chunk c = keys 8c..8c+7 of this half
-          *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        // row r's keys half * 64 .. + 63 -> columns half * 32 .. + 31 of P_b
+        tmem_st_32x32b_x32(tmem + lane_base + C::COL_P + pb * 64 + half * 32, pk);
         if (j * TK + TK > key_end) {
           // keys past key_end may hold uninitialised memory: zero their V rows
           // once the V block has landed (its stage cannot be refilled before
@@ -565,11 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(sv_base + hf * C::HALF_TILE + key * 128 + ((cc ^ (key & 7)) << 4)) =
                 make_uint4(0, 0, 0, 0);
           }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
+        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
+        if (lane == 0) mbar_arrive(&p_full[pb]);
       }
       if (!ok) break;
       J += w.nblk;
@@ -580,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool xok = mbar_wait(xsbar, nunit & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, xok)) break;
       l += xsum[(half ^ 1) * 128 + r];
-      bool pok = mbar_wait(pv_done, (J - 1) & 1, abort_flag, p.status);
+      bool pok = mbar_wait(&pv_done[(J - 1) & 1], ((J - 1) >> 1) & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, pok)) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
