@@ -32,4 +32,15 @@ Parity status per function (what pins it, in tests/test_oracle_pins.py):
                          identity when the output projections are zero
   costs.*                chunked-attention pair-count identity (section
                          7.5b); closed form of I and c* against counters
+  sched.SchedLoop        closed form of one request's iterations; token and
+                         page conservation; a step-by-step replay on tiny
+                         streams
+  fp8.* (E4M3 projections, reading notes section 7.7; tests/test_oracle_fp8.py)
+                         the 256-code table and round-to-nearest-even
+                         against torch's float8_e4m3fn conversion;
+                         saturation; per-row scaling bounds and invariances;
+                         the projection against exact rational sums; the
+                         layer's QKV exact on representable inputs, chunked
+                         == unchunked, and within E4M3's error of the bf16
+                         layer
 """
