@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tau", type=int, default=512)
     ap.add_argument("--decodes", type=int, default=32)
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "e4m3"],
+                    help="projection weights: bf16, or E4M3 codes with per-row scales (FP8 projections)")
     ap.add_argument("--sweep", action="store_true",
                     help="token-budget sweep (tau 64..4096, 64 decodes, c = tau - 64): one JSON line per tau")
     ap.add_argument("--calibrate", type=float, default=None, metavar="SLO_MS",
@@ -334,7 +336,8 @@ def run_hb(args, world, rank, local):
     w = make_workload(args.tau, args.decodes)
     st, dims = w.state, w.dims
     max_pos = max(r.done for r in st.decodes + st.prefills) + w.tau + 1
-    gw = wd.layer_weights_device(w.weights[0], dims, dev)
+    f8 = args.weights == "e4m3"
+    gw = wd.layer_weights_device(w.weights[0], dims, dev, fmt=args.weights)
     kc, vc = wd.bf16_tensor(st.k_pool, dev), wd.bf16_tensor(st.v_pool, dev)
     rope = wd.rope_table_device(max_pos, dims, dev)
     x_dev = wd.bf16_tensor(w.x, dev)
@@ -432,16 +435,20 @@ def run_hb(args, world, rank, local):
     # ---- roofline --------------------------------------------------------
     peaks = load_peaks()
     row_pos, q_start, kv_len = runner.host_plan_arrays()
-    sc = costs.stage_costs(dims, row_pos, q_start, kv_len)
+    sc = costs.stage_costs(dims, row_pos, q_start, kv_len, weight_bytes=1 if f8 else 2)
     flops, byts = costs.iteration_totals(sc)
     t_step = t_dev / args.steps
-    t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
+    t_roof = costs.roofline_time(sc, peaks["bf16_tflops"], peaks["hbm_gbs"], f8)
     dom = int(np.argmax(stage_ms))
     name = costs.STAGES[dom]
     f_dom, b_dom, bound = sc[name]
     dur = stage_ms[dom] / 1e3
+    peak_source = peaks["source"] + " burst"
     if bound == "tensor":
-        achieved, peak, unit = f_dom / dur / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        tensor_peak = peaks["bf16_tflops"] * (2.0 if f8 else 1.0)
+        achieved, peak, unit = f_dom / dur / 1e12, tensor_peak, "TFLOP/s"
+        if f8:
+            peak_source += " x 2 (nominal FP8/bf16 dense ratio, 4.5/2.25 PFLOP/s)"
     else:
         achieved, peak, unit = b_dom / dur / 1e9, peaks["hbm_gbs"], "GB/s"
     traffic = None  # measured DRAM bytes per launch (ncu), when recorded for this kernel and workload
@@ -449,7 +456,7 @@ def run_hb(args, world, rank, local):
     if os.path.exists(prof_path):
         entries = dict(ln.split(None, 1) for ln in open(prof_path).read().splitlines()
                        if ln.strip() and not ln.startswith("#"))
-        if entries.get("workload", "").strip() == WORKLOAD and name in entries:
+        if entries.get("workload", "").strip() == WORKLOAD and name in entries and not f8:
             traffic = float(entries[name])
 
     n_dec = sum(1 for r in st.decodes)
@@ -458,22 +465,24 @@ def run_hb(args, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * t_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tau": w.tau, "chunk_tokens": c, "decodes": n_dec, "rows": T,
+        "vs_baseline": None, "dtype": "e4m3 projections, bf16 attention" if f8 else "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD + ("_e4m3" if f8 else ""), "tau": w.tau, "weights": args.weights, "chunk_tokens": c, "decodes": n_dec, "rows": T,
                    "d_model": dims.d_model, "heads": f"{dims.n_q}q/{dims.n_kv}kv", "d_head": dims.d_head,
                    "d_ff": dims.d_ff, "page": 16, "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "inputs larger than L2 (436 MB weights + 308 MB KV per step), no flush"},
         "roofline": {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak, "traffic": traffic, "peak_source": peaks["source"] + " burst",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_source,
                      "launch_ms": stage_ms[dom]},
         "iteration_roofline": {"flops": flops, "bytes": byts, "t_roof_ms": 1e3 * t_roof,
                                "frac": t_roof / t_step, "intensity_flop_per_byte": flops / byts,
-                               "intensity_page": costs.page_intensity(c, n_dec, dims.params_per_layer, 2, 1,
-                                                                      dims.n_kv, dims.d_head, s_bar)},
+                               "intensity_page": costs.page_intensity(c, n_dec, dims.params_per_layer,
+                                                                      1 if f8 else 2, 1, dims.n_kv, dims.d_head,
+                                                                      s_bar)},
         "stages_ms": {k: round(float(v), 5) for k, v in zip(costs.STAGES, stage_ms)},
         "e2e": e2e,
-        # per layer forward: rmsnorm x2, GEMM x4, RoPE/KV append, chunk and decode attention
-        "gpu_launches": 9 * args.steps,
+        # per layer forward: row statistics, QKV, RoPE/KV append, chunk and decode
+        # attention, O, gate/up, down (E4M3: three more quantization kernels)
+        "gpu_launches": (11 if f8 else 8) * args.steps,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -500,13 +509,15 @@ def run_sweep(args, taus=None, emit=True):
     w = make_workload(max(taus), 64)
     st, dims = w.state, w.dims
     max_pos = 8192 + max(taus) + 1
-    gw = wd.layer_weights_device(w.weights[0], dims)
+    f8 = args.weights == "e4m3"
+    gw = wd.layer_weights_device(w.weights[0], dims, fmt=args.weights)
     kc, vc = wd.bf16_tensor(st.k_pool), wd.bf16_tensor(st.v_pool)
     rope = wd.rope_table_device(max_pos, dims)
     x_all = wd.bf16_tensor(w.x)
     peaks = load_peaks()
     s_bar = float(np.mean([r.done for r in st.decodes]))
-    balance = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    s_psi = 1 if f8 else 2  # bytes per weight
+    balance = peaks["bf16_tflops"] * (2.0 if f8 else 1.0) * 1e12 / (peaks["hbm_gbs"] * 1e9)
     for tau in taus:
         stream = torch.cuda.Stream()
         runner = PlanRunner(lib, st, tau, tau, "cuda")
@@ -549,24 +560,26 @@ def run_sweep(args, taus=None, emit=True):
                 stage_ms[s] += ev[s].elapsed_time(ev[s + 1]) / 20
         hb.hb_check_status(stream)
         row_pos, q_start, kv_len = runner.host_plan_arrays()
-        sc = costs.stage_costs(dims, row_pos, q_start, kv_len)
+        sc = costs.stage_costs(dims, row_pos, q_start, kv_len, weight_bytes=s_psi)
         flops, byts = costs.iteration_totals(sc)
-        t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
+        t_roof = costs.roofline_time(sc, peaks["bf16_tflops"], peaks["hbm_gbs"], f8)
         T = runner.n_rows
         c = T - 64
         rec = {
-            "sweep": "tau", "tau": tau, "rows": T, "chunk_tokens": c, "decodes": 64, "ms_per_step": 1e3 * t_step,
+            "sweep": "tau", "weights": args.weights, "tau": tau, "rows": T, "chunk_tokens": c, "decodes": 64, "ms_per_step": 1e3 * t_step,
             "tokens_per_s": T / t_step, "t_roof_ms": 1e3 * t_roof, "roofline_frac": t_roof / t_step,
             "flops": flops, "bytes": byts, "intensity_flop_per_byte": flops / byts,
-            "intensity_page": costs.page_intensity(c, 64, dims.params_per_layer, 2, 1, dims.n_kv, dims.d_head, s_bar),
+            "intensity_page": costs.page_intensity(c, 64, dims.params_per_layer, s_psi, 1, dims.n_kv, dims.d_head,
+                                                   s_bar),
             "stages_ms": {k: round(float(v), 5) for k, v in zip(costs.STAGES, stage_ms)}}
         records.append(rec)
         if emit:
             print(json.dumps(rec), flush=True)
     # the page's optimal chunk for this machine balance (I* = peak FLOP/s / peak B/s)
     psi = dims.params_per_layer
-    c_star = balance / (2.0 * psi) * (2 * psi + 2.0 * dims.n_kv * dims.d_head * s_bar * 64) - 64
-    cs = {"sweep": "c_star", "machine_balance_flop_per_byte": balance, "c_star_tokens": c_star, "s_bar": s_bar}
+    c_star = balance / (2.0 * psi) * (s_psi * psi + 2.0 * dims.n_kv * dims.d_head * s_bar * 64) - 64
+    cs = {"sweep": "c_star", "weights": args.weights, "machine_balance_flop_per_byte": balance, "c_star_tokens": c_star,
+          "s_bar": s_bar}
     records.append(cs)
     if emit:
         print(json.dumps(cs), flush=True)
@@ -584,7 +597,7 @@ def run_calibrate(args):
     prof = [r for r in recs if r["sweep"] == "tau"]
     c_star = [r for r in recs if r["sweep"] == "c_star"][0]
     for r in prof:
-        print(json.dumps({"calibrate": "profile", "tau": r["tau"], "layer_ms": r["ms_per_step"],
+        print(json.dumps({"calibrate": "profile", "weights": args.weights, "tau": r["tau"], "layer_ms": r["ms_per_step"],
                           "iteration_ms": r["ms_per_step"] * args.layers, "tokens_per_s": r["tokens_per_s"],
                           "roofline_frac": r["roofline_frac"]}), flush=True)
     fits = [r for r in prof if r["ms_per_step"] * args.layers <= args.calibrate]
@@ -595,7 +608,7 @@ def run_calibrate(args):
                       "tau": best["tau"] if best else None,
                       "iteration_ms": best["ms_per_step"] * args.layers if best else None,
                       "tau_knee_10pct": knee, "c_star_tokens": c_star["c_star_tokens"],
-                      "decodes": 64}), flush=True)
+                      "decodes": 64, "weights": args.weights}), flush=True)
     return 0
 
 

@@ -43,7 +43,8 @@ class hb_device_plan(C.Structure):
 
 
 class hb_layer_weights(C.Structure):
-    _fields_ = [("w_qkv", vp), ("w_o", vp), ("w_gu", vp), ("w_d", vp)]
+    _fields_ = [("w_qkv", vp), ("w_o", vp), ("w_gu", vp), ("w_d", vp),
+                ("s_qkv", vp), ("s_o", vp), ("s_gu", vp), ("s_d", vp), ("format", i32)]
 
 
 class hb_profile(C.Structure):
@@ -52,6 +53,7 @@ class hb_profile(C.Structure):
 
 HB_LAYER_STAGES = 8
 HB_EPI_STORE, HB_EPI_RESIDUAL, HB_EPI_SWIGLU, HB_EPI_F32 = 0, 1, 2, 3
+HB_WEIGHTS_BF16, HB_WEIGHTS_E4M3 = 0, 1
 HB_OK, HB_ERR_INVALID_ARG, HB_ERR_CAPACITY, HB_ERR_OUT_OF_PAGES = 0, 1, 2, 3
 HB_ERR_CUDA, HB_ERR_TIMEOUT, HB_ERR_UNSUPPORTED, HB_ERR_DEVICE = 4, 5, 6, 7
 
@@ -79,6 +81,8 @@ PROTOTYPES = {
     "hb_attention_noalloc": (C.c_int, [vp, vp, vp, i32, C.POINTER(hb_device_plan), C.POINTER(hb_layer_dims), i32,
                                        vp, vp]),
     "hb_gemm": (C.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, vp]),
+    "hb_gemm_e4m3": (C.c_int, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]),
+    "hb_quantize_e4m3": (C.c_int, [vp, vp, vp, i32, i32, vp]),
     "hb_interleave_gate_up": (C.c_int, [vp, vp, vp, i32, i32, vp]),
     "hb_fold_gamma": (C.c_int, [vp, vp, vp, i32, i32, vp]),
     "hb_layer_workspace_bytes": (C.c_size_t, [C.POINTER(hb_layer_dims), i32, i32, i32]),

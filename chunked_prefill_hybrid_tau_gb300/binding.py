@@ -318,6 +318,25 @@ def hb_gemm(A, B, Cout, R=None, epilogue=L.HB_EPI_STORE, stream=None):
     _check(lib().hb_gemm(_p(A), _p(B), _p(Cout), _p(R), M, N, K, int(epilogue), _stream(stream)), "hb_gemm")
 
 
+def hb_gemm_e4m3(A, s_a, B, s_b, Cout, R=None, epilogue=L.HB_EPI_STORE, stream=None):
+    """E4M3 codes A [M][K], B [N][K] (uint8 tensors) with fp32 per-row scales."""
+    M, K = A.shape
+    N = B.shape[0]
+    _check(lib().hb_gemm_e4m3(_p(A), _p(s_a), _p(B), _p(s_b), _p(Cout), _p(R), M, N, K, int(epilogue),
+                              _stream(stream)), "hb_gemm_e4m3")
+
+
+def hb_quantize_e4m3(x, q=None, scale=None, stream=None):
+    """Per-row E4M3 codes (uint8 [rows][cols]) and fp32 scales [rows] of a
+    device bf16 matrix x; returns (q, scale)."""
+    import torch
+    rows, cols = x.shape
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device) if q is None else q
+    scale = torch.empty(max(rows, 4), dtype=torch.float32, device=x.device) if scale is None else scale
+    _check(lib().hb_quantize_e4m3(_p(x), _p(q), _p(scale), rows, cols, _stream(stream)), "hb_quantize_e4m3")
+    return q, scale[:rows]
+
+
 def hb_interleave_gate_up(w_gate, w_up, w_gu, stream=None):
     F, d = w_gate.shape
     _check(lib().hb_interleave_gate_up(_p(w_gate), _p(w_up), _p(w_gu), F, d, _stream(stream)),
@@ -332,11 +351,13 @@ def hb_fold_gamma(w, gamma, out=None, stream=None):
     return out
 
 
-def prepare_layer_weights(w_qkv, w_o, w_g, w_u, w_d, g1, g2, stream=None) -> "LayerWeights":
+def prepare_layer_weights(w_qkv, w_o, w_g, w_u, w_d, g1, g2, stream=None, fmt="bf16") -> "LayerWeights":
     """Raw device bf16 weights of one layer -> the prepared form that
     hb_layer_forward takes: g1 folded into W_qkv, gate/up interleaved and g2
     folded into them (include/hb.h, hb_layer_weights).  w_qkv is folded in
-    place; w_g and w_u are left as they are."""
+    place; w_g and w_u are left as they are.  fmt="e4m3": each prepared
+    matrix is then quantized per row (hb_quantize_e4m3) and the bf16 forms
+    are released."""
     import torch
     F, d = w_g.shape
     f_pad = (F + 63) // 64 * 64
@@ -344,7 +365,14 @@ def prepare_layer_weights(w_qkv, w_o, w_g, w_u, w_d, g1, g2, stream=None) -> "La
     hb_interleave_gate_up(w_g, w_u, w_gu, stream)
     hb_fold_gamma(w_gu, g2, stream=stream)
     hb_fold_gamma(w_qkv, g1, stream=stream)
-    return LayerWeights(w_qkv=w_qkv, w_o=w_o, w_gu=w_gu, w_d=w_d)
+    if fmt == "bf16":
+        return LayerWeights(w_qkv=w_qkv, w_o=w_o, w_gu=w_gu, w_d=w_d)
+    if fmt != "e4m3":
+        raise ValueError(f"unknown weight format {fmt!r}")
+    q = {k: hb_quantize_e4m3(v, stream=stream) for k, v in
+         (("qkv", w_qkv), ("o", w_o), ("gu", w_gu), ("d", w_d))}
+    return LayerWeights(w_qkv=q["qkv"][0], w_o=q["o"][0], w_gu=q["gu"][0], w_d=q["d"][0], s_qkv=q["qkv"][1],
+                        s_o=q["o"][1], s_gu=q["gu"][1], s_d=q["d"][1], fmt="e4m3")
 
 
 def hb_layer_workspace_bytes(dims, max_rows, max_seqs, max_kv_len) -> int:
@@ -354,14 +382,24 @@ def hb_layer_workspace_bytes(dims, max_rows, max_seqs, max_kv_len) -> int:
 
 @dataclasses.dataclass
 class LayerWeights:
-    """Prepared device weights of one layer (bf16 tensors, prepare_layer_weights)."""
+    """Prepared device weights of one layer (prepare_layer_weights): bf16
+    tensors, or E4M3 codes (uint8) with fp32 per-row scales."""
     w_qkv: object
     w_o: object
     w_gu: object
     w_d: object
+    s_qkv: object = None
+    s_o: object = None
+    s_gu: object = None
+    s_d: object = None
+    fmt: str = "bf16"
 
     def struct(self) -> L.hb_layer_weights:
-        return L.hb_layer_weights(*[self.__dict__[k].data_ptr() for k in ("w_qkv", "w_o", "w_gu", "w_d")])
+        ptrs = [self.__dict__[k].data_ptr() for k in ("w_qkv", "w_o", "w_gu", "w_d")]
+        if self.fmt == "e4m3":
+            scales = [self.__dict__[k].data_ptr() for k in ("s_qkv", "s_o", "s_gu", "s_d")]
+            return L.hb_layer_weights(*ptrs, *scales, L.HB_WEIGHTS_E4M3)
+        return L.hb_layer_weights(*ptrs, None, None, None, None, L.HB_WEIGHTS_BF16)
 
 
 def hb_layer_forward(w: LayerWeights, dims, dplan: DevicePlan, rope, max_pos, x_in, x_out, k_cache, v_cache,

@@ -11,6 +11,11 @@ The per-iteration roofline is t_roof = max(FLOPs / peak FLOP/s, bytes / peak
 B/s) of the whole layer (linear-layer roofline of the Sarathi-Serve reading
 notes, section 1.6, extended with the attention's KV reads as in the hybrid-
 iteration intensity of the Chunked Prefill page).
+
+E4M3 weights (weight_bytes=1): a weight matrix is read at one byte per
+parameter and the projections' FLOPs run at the FP8 tensor rate, twice the
+bf16 one (section 7.7 of the reading notes: FP8 doubles FLOPs per byte);
+activations stay bf16 in the algorithmic count.
 """
 from __future__ import annotations
 
@@ -19,16 +24,17 @@ import numpy as np
 STAGES = ["rmsnorm1", "qkv", "rope_kv", "attention", "o_proj", "rmsnorm2", "gate_up", "down"]
 
 
-def stage_costs(dims, row_pos, seq_q_start, seq_kv_len):
+def stage_costs(dims, row_pos, seq_q_start, seq_kv_len, weight_bytes=2):
     """{stage: (flops, bytes, bound)} for one layer over the packed rows."""
     T = len(row_pos)
     d, dh, nq, nkv, F = dims.d_model, dims.d_head, dims.n_q, dims.n_kv, dims.d_ff
     qkv_cols = (nq + 2 * nkv) * dh
     hd = nq * dh
     b = 2  # bf16
+    sw = weight_bytes
 
     def gemm(N, K):
-        return 2.0 * T * N * K, float(N * K * b + T * K * b + T * N * b)
+        return 2.0 * T * N * K, float(N * K * sw + T * K * b + T * N * b)
 
     kv_len = np.asarray(seq_kv_len, np.int64)
     pos = np.asarray(row_pos, np.int64)
@@ -41,10 +47,22 @@ def stage_costs(dims, row_pos, seq_q_start, seq_kv_len):
         "attention": (attn_flops, attn_bytes, "hbm"),
         "o_proj": (gemm(d, hd)[0], gemm(d, hd)[1] + T * d * b, "tensor"),
         "rmsnorm2": (3.0 * T * d, float(2 * T * d * b + d * b), "hbm"),
-        "gate_up": (2.0 * T * 2 * F * d, float(2 * F * d * b + T * d * b + T * F * b), "tensor"),
+        "gate_up": (2.0 * T * 2 * F * d, float(2 * F * d * sw + T * d * b + T * F * b), "tensor"),
         "down": (gemm(d, F)[0], gemm(d, F)[1] + T * d * b, "tensor"),
     }
     return c
+
+
+def roofline_time(costs: dict, tflops_bf16: float, hbm_gbs: float, f8: bool = False) -> float:
+    """t_roof = max(sum of FLOPs over their tensor rates, bytes / HBM B/s); with
+    f8 the projections (the "tensor" stages other than attention) run at twice
+    the bf16 rate."""
+    t_math = 0.0
+    for name, (fl, _, bound) in costs.items():
+        rate = tflops_bf16 * (2.0 if (f8 and bound == "tensor") else 1.0)
+        t_math += fl / (rate * 1e12)
+    byts = sum(v[1] for v in costs.values())
+    return max(t_math, byts / (hbm_gbs * 1e9))
 
 
 def iteration_totals(costs: dict):

@@ -1,506 +1,10 @@
-// Packed-token projections on the 5th-generation tensor cores:
-//   C = epilogue(A B^T),  A [M][K] bf16 (activations), B [N][K] bf16 (weights).
-//
-// These are the linear layers whose cost model the pages use (Sarathi-Serve
-// reading notes, section 1.6: T = max(T_math, T_mem) with
-// T_math = 2 n d_in d_out / FLOPS and T_mem = (d_in d_out bytes_w + ...) / BW).
-//
-// Design (sm_103a):
-//   * persistent grid (<= one CTA per SM), 128 x BN output tiles walked with
-//     the M index fastest, so the CTAs that share a weight tile run together
-//     and the weights stream from HBM once;
-//   * warp 0: TMA producer.  128-byte swizzled 128x64 (A) and BNx64 (B) boxes
-//     into a STAGES-deep shared-memory ring, completion via mbarrier tx bytes;
-//   * warp 1: one elected thread issues tcgen05.mma (kind::f16, M=128,
-//     N=BN, K=16) into a TMEM accumulator; tcgen05.commit frees a ring slot
-//     and, after the last K block, signals the epilogue;
-//   * warps 2-5: epilogue.  tcgen05.ld 32x32b (warp w reads TMEM lanes
-//     32*(w%4)..), fused STORE / RESIDUAL / SWIGLU / F32 epilogue, then the
-//     accumulator buffer is handed back.  Two accumulator buffers let the
-//     epilogue of one tile overlap the main loop of the next.
-//   * every wait is bounded (device.cuh); on expiry the kernel unwinds.
-#include <cuda_bf16.h>
-
-#include "device.cuh"
-#include "runtime.h"
+// Packed-token projections on the 5th-generation tensor cores, bf16
+// operands (kind::f16, fp32 accumulate): the host side of hb_gemm, the
+// tile-width and split-K rules, and the gate/up interleave of the weights.
+// The kernel template is in gemm_kernel.cuh.
+#include "gemm_kernel.cuh"
 
 namespace hb {
-namespace {
-
-using namespace dev;
-
-constexpr int BM = 128;
-constexpr int BK = 64;
-constexpr int kThreads = 192;
-
-template <int BN>
-struct Cfg {
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 256 ? 4 : (BN == 192 ? 5 : 6);
-  static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
-  static constexpr int BAR_BYTES = 512;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
-  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
-  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
-};
-
-struct Params {
-  int M, N, K;
-  void* C;
-  const void* R;
-  int ldc;       // row stride of C and R (elements)
-  int out_cols;  // valid output columns (N, or N/2 for SWIGLU)
-  int* status;
-  GemmNorm norm;  // folded RMSNorm: row scaling in (STORE, SWIGLU), row statistics out (RESIDUAL)
-  int ksplit;     // 1, or 2: each tile's K range in two halves (RESIDUAL only)
-  float* part;    // ksplit 2: fp32 partial tiles [tile][half][BN][BM] (column-major)
-  int* flags;     // ksplit 2: per (tile, 32-row slab) arrival counters, zero between launches
-};
-
-// Work unit u: tile u / ksplit, K half u % ksplit (k-blocks [kb0, kb1)).
-// The two halves of a tile are consecutive units, so they run at the same
-// time on neighbouring CTAs.
-struct Unit {
-  int tile, half, m0, n_blk, kb0, kb1;
-};
-
-template <int BN>
-__device__ __forceinline__ Unit unit_of(const Params& p, int u, int m_tiles, int kblocks) {
-  Unit w;
-  w.tile = u / p.ksplit;
-  w.half = u - w.tile * p.ksplit;
-  w.m0 = (w.tile % m_tiles) * BM;
-  w.n_blk = w.tile / m_tiles;
-  const int per = (kblocks + p.ksplit - 1) / p.ksplit;
-  w.kb0 = w.half * per;
-  w.kb1 = w.kb0 + per < kblocks ? w.kb0 + per : kblocks;
-  return w;
-}
-
-// silu(g) = g / (1 + e^-g).  The fast divide (2 ulp) is far below the bf16
-// rounding of the result; an IEEE divide here made the SwiGLU epilogue the
-// most expensive part of the gate/up projection.  For g -> -inf the
-// denominator overflows to inf and the quotient is 0, the correct limit.
-__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
-
-// Inverse RMS of one row from its 32-column partial sums of squares, summed
-// in column order: rsqrt(sum / d + eps).
-__device__ __forceinline__ float row_inv_rms(const GemmNorm& nm, int row) {
-  const float2* sp = reinterpret_cast<const float2*>(nm.ss_in + static_cast<size_t>(row) * nm.parts);
-  float ss = 0.f;
-  for (int i = 0; i < nm.parts / 2; ++i) {
-    const float2 v = sp[i];
-    ss += v.x;
-    ss += v.y;
-  }
-  return rsqrtf(ss * nm.inv_d + nm.eps);
-}
-
-// Store 32 accumulator columns [col, col+32) of one row, 16-byte segments
-// past the last valid column skipped (STORE: scaled by `scale`, the row's
-// folded RMSNorm factor, else 1; F32: as is).
-template <int EPI>
-__device__ __forceinline__ void store_chunk(const Params& p, int row, int col, const uint32_t (&r)[32], float scale) {
-  const int ncols = p.out_cols;
-  if (EPI == HB_EPI_F32) {
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.C) + static_cast<size_t>(row) * p.ldc + col);
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (col + 4 * i < ncols)
-        dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                             __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
-    return;
-  }
-  uint32_t w[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i)
-    w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * scale, __uint_as_float(r[2 * i + 1]) * scale);
-  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) + static_cast<size_t>(row) * p.ldc + col);
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    if (col + 8 * i < ncols) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-}
-
-// RESIDUAL: C = R + acc for 32 columns, with the residual already loaded
-// (rv); writes the sum of squares of the 32 rounded outputs to ss_dst when
-// it is given.
-__device__ __forceinline__ void residual_chunk(const Params& p, int row, int col, const uint32_t (&r)[32],
-                                               const uint4 (&rv)[4], float* ss_dst) {
-  uint32_t w[16];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t rr[4] = {rv[i].x, rv[i].y, rv[i].z, rv[i].w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f = unpack_bf16x2(rr[j]);
-      const int e = 8 * i + 2 * j;
-      w[4 * i + j] = pack_bf16x2(f.x + __uint_as_float(r[e]), f.y + __uint_as_float(r[e + 1]));
-    }
-  }
-  if (ss_dst) {
-    float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float2 f = unpack_bf16x2(w[i]);
-      ss += f.x * f.x;
-      ss += f.y * f.y;
-    }
-    *ss_dst = ss;
-  }
-  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) + static_cast<size_t>(row) * p.ldc + col);
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    if (col + 8 * i < p.out_cols) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-}
-
-template <int BN, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
-  using C = Cfg<BN>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
-  uint64_t* empty = full + C::STAGES;
-  uint64_t* acc_full = empty + C::STAGES;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int m_tiles = (p.M + BM - 1) / BM;
-  const int n_tiles = (p.N + BN - 1) / BN;
-  const int tiles = m_tiles * n_tiles;
-  const int units = tiles * p.ksplit;
-  const int kblocks = (p.K + BK - 1) / BK;  // TMA zero-fills columns past K
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);
-    }
-    mbar_init(drain, 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
-  }
-  griddep_launch_dependents();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  if (warp == 0) {
-    // ---------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      uint32_t pending = 0;  // stages armed and not yet seen consumed (bit mask)
-      uint32_t armed_parity = 0;
-      // The weights do not come from the previous kernel: the first ring
-      // fill of B is issued before waiting for it, then A follows.
-      int pre = 0;
-      if (static_cast<int>(blockIdx.x) < units) {
-        const Unit w = unit_of<BN>(p, blockIdx.x, m_tiles, kblocks);
-        pre = w.kb1 - w.kb0 < C::STAGES ? w.kb1 - w.kb0 : C::STAGES;
-        for (int i = 0; i < pre; ++i) {
-          mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
-          tma_load_2d(smem + i * C::STAGE_BYTES + C::A_BYTES, &tmB, &full[i], (w.kb0 + i) * BK, w.n_blk * BN);
-        }
-      }
-      griddep_wait();
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = unit_of<BN>(p, u, m_tiles, kblocks);
-        const int m0 = w.m0;
-        const int n0 = w.n_blk * BN;
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          uint8_t* sa = smem + stage * C::STAGE_BYTES;
-          if (u == static_cast<int>(blockIdx.x) && kb - w.kb0 < pre) {
-            // stage armed and its B box issued above (fresh barrier, phase 0)
-            pending |= 1u << stage;
-            tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
-          } else {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
-            pending |= 1u << stage;
-            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-            mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-            tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
-            tma_load_2d(sa + C::A_BYTES, &tmB, &full[stage], kb * BK, n0);
-          }
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (!ok) {
-        // let copies already in flight land before the CTA exits; a stage
-        // whose empty wait succeeded later was consumed, so only the last
-        // STAGES arms can be outstanding
-        for (int s = 0; s < C::STAGES; ++s)
-          if (pending & (1u << s)) mbar_drain(&full[s], (armed_parity >> s) & 1u);
-      }
-    }
-    if (lane != 0) griddep_wait();
-  } else if (warp == 1) {
-    griddep_wait();
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
-      int stage = 0;
-      uint32_t phase = 0;
-      int t = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++t) {
-        const Unit w = unit_of<BN>(p, u, m_tiles, kblocks);
-        const int acc = t & 1;
-        const uint32_t acc_phase = (t >> 1) & 1;
-        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
-          const uint32_t b_addr = a_addr + C::A_BYTES;
-#pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            mma_bf16(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), kIdesc,
-                     (kb != w.kb0 || k != 0) ? 1u : 0u);
-          }
-          mma_commit(&empty[stage]);
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (ok) mma_commit(&acc_full[acc]);
-      }
-      if (!ok) {
-        // make sure no MMA is still reading shared memory or writing TMEM
-        mma_commit(drain);
-        mbar_drain(drain, 0);
-      }
-    }
-  } else {
-    // ---------------------------------------------------------- epilogue
-    griddep_wait();
-    const int quarter = warp & 3;
-    int t = 0;
-    for (int un = blockIdx.x; un < units; un += gridDim.x, ++t) {
-      const Unit wu = unit_of<BN>(p, un, m_tiles, kblocks);
-      const int acc = t & 1;
-      const uint32_t acc_phase = (t >> 1) & 1;
-      const int m0 = wu.m0;
-      const int n_blk = wu.n_blk;
-      const int rloc = quarter * 32 + lane;  // row within the tile
-      const int row = m0 + rloc;
-      const bool row_ok = row < p.M;
-      // the row's folded RMSNorm factor, read before the accumulator is ready
-      const float scale = (p.norm.ss_in != nullptr && row_ok) ? row_inv_rms(p.norm, row) : 1.f;
-      bool ok = mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.status);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-      if (EPI == HB_EPI_SWIGLU) {
-#pragma unroll 1
-        for (int j = 0; j < BN / 128; ++j) {
-#pragma unroll 1
-          for (int h = 0; h < 2; ++h) {
-            uint32_t g[32], u[32];
-            tmem_ld_32x32b_x32(t_base + j * 128 + h * 32, g);
-            tmem_ld_32x32b_x32(t_base + j * 128 + 64 + h * 32, u);
-            tmem_ld_wait();
-            const int col = n_blk * (BN / 2) + j * 64 + h * 32;
-            if (row_ok && col < p.out_cols) {
-              uint32_t w[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float a0 = silu(__uint_as_float(g[2 * i]) * scale) * (__uint_as_float(u[2 * i]) * scale);
-                const float a1 =
-                    silu(__uint_as_float(g[2 * i + 1]) * scale) * (__uint_as_float(u[2 * i + 1]) * scale);
-                w[i] = pack_bf16x2(a0, a1);
-              }
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) +
-                                                    static_cast<size_t>(row) * p.ldc + col);
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                if (col + 8 * i < p.out_cols) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-            }
-          }
-        }
-      } else {
-        bool finish = true;  // this warp writes the output rows of the tile
-        const float* other = nullptr;
-        if (p.ksplit == 2) {
-          // Split K: publish this half's fp32 partial (column-major, so each
-          // store is one coalesced 128-byte line per warp); the second warp
-          // to arrive for this 32-row slab adds the other half and finishes.
-          // p0 + p1 is commutative, so the result does not depend on which
-          // half arrives last.
-          float* mine = p.part + (static_cast<size_t>(wu.tile) * 2 + wu.half) * BN * BM;
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(t_base + c * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) mine[static_cast<size_t>(c * 32 + j) * BM + rloc] = __uint_as_float(r[j]);
-          }
-          __threadfence();
-          __syncwarp();
-          int last = 0;
-          if (lane == 0) {
-            int* flag = p.flags + wu.tile * 4 + quarter;
-            last = atomicAdd(flag, 1) == 1;
-            if (last) *flag = 0;
-          }
-          finish = __shfl_sync(0xffffffffu, last, 0) != 0;
-          if (finish) {
-            __threadfence();
-            other = p.part + (static_cast<size_t>(wu.tile) * 2 + (1 - wu.half)) * BN * BM;
-          }
-        }
-        if (finish && EPI == HB_EPI_RESIDUAL) {
-          // software-pipelined: the residual (and the other half's partial)
-          // of chunk c + 1 is in flight while chunk c is combined and stored
-          constexpr int NC = BN / 32;
-          uint4 rv[2][4];
-          float ov[2][32];
-          auto fetch = [&](int c, int b) {
-            const int col = n_blk * BN + c * 32;
-            const uint4* res = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.R) +
-                                                              static_cast<size_t>(row) * p.ldc + col);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              rv[b][i] = (row_ok && col + 8 * i < p.out_cols) ? res[i] : make_uint4(0, 0, 0, 0);
-            if (other != nullptr) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) ov[b][j] = __ldcg(other + static_cast<size_t>(c * 32 + j) * BM + rloc);
-            }
-          };
-          fetch(0, 0);
-#pragma unroll
-          for (int c = 0; c < NC; ++c) {
-            const int b = c & 1;
-            if (c + 1 < NC) fetch(c + 1, b ^ 1);
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(t_base + c * 32, r);
-            tmem_ld_wait();
-            if (other != nullptr) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + ov[b][j]);
-            }
-            const int col = n_blk * BN + c * 32;
-            float* ss_dst = p.norm.ss_out != nullptr
-                                ? p.norm.ss_out + static_cast<size_t>(row) * p.norm.parts + col / 32
-                                : nullptr;
-            if (row_ok && col < p.out_cols) residual_chunk(p, row, col, r, rv[b], ss_dst);
-          }
-        } else if (finish) {
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(t_base + c * 32, r);
-            tmem_ld_wait();
-            const int col = n_blk * BN + c * 32;
-            if (row_ok && col < p.out_cols) store_chunk<EPI>(p, row, col, r, scale);
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
-  }
-}
-
-template <int BN, int EPI>
-hb_status launch(const DeviceCtx& ctx, const void* A, int lda, const void* B, void* Cp, int ldc, const void* R, int M,
-                 int N, int K, const GemmNorm* norm, const GemmSplit* split, cudaStream_t stream) {
-  using C = Cfg<BN>;
-  CUtensorMap tmA, tmB;
-  hb_status st = encode_tmap_2d(&tmA, A, K, M, static_cast<uint64_t>(lda) * 2, BK, BM, true);
-  if (st != HB_OK) return st;
-  st = encode_tmap_2d(&tmB, B, K, N, static_cast<uint64_t>(K) * 2, BK, BN, true);
-  if (st != HB_OK) return st;
-  static bool attr_set[64] = {};
-  if (!attr_set[ctx.device]) {
-    st = cuda_status(cudaFuncSetAttribute(gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM),
-                     "cudaFuncSetAttribute(gemm)");
-    if (st != HB_OK) return st;
-    attr_set[ctx.device] = true;
-  }
-  Params p;
-  p.M = M;
-  p.N = N;
-  p.K = K;
-  p.C = Cp;
-  p.R = R;
-  p.ldc = ldc;
-  p.out_cols = EPI == HB_EPI_SWIGLU ? N / 2 : N;
-  p.status = ctx.status;
-  p.norm = norm ? *norm : GemmNorm{};
-  p.ksplit = split ? 2 : 1;
-  p.part = split ? split->part : nullptr;
-  p.flags = split ? split->flags : nullptr;
-  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const int units = tiles * p.ksplit;
-  const int grid = units < ctx.num_sms ? units : ctx.num_sms;
-  return launch_pdl(gemm_kernel<BN, EPI>, grid, kThreads, C::SMEM, stream, "gemm_kernel launch", tmA, tmB, p);
-}
-
-// Tile width: fewest waves of tiles over the SMs, weighted by a per-tile
-// cost that grows with BN (plus a fixed per-tile overhead).
-int choose_bn(int M, int N, int epi, int num_sms) {
-  const int cands_swiglu[2] = {256, 128};
-  const int cands[3] = {256, 192, 128};
-  const int* c = epi == HB_EPI_SWIGLU ? cands_swiglu : cands;
-  const int nc = epi == HB_EPI_SWIGLU ? 2 : 3;
-  const int m_tiles = (M + BM - 1) / BM;
-  int best = 128;
-  double best_cost = 1e30;
-  for (int i = 0; i < nc; ++i) {
-    const int bn = c[i];
-    if (epi == HB_EPI_SWIGLU ? N % bn != 0 : (N % bn != 0 && bn != 128)) continue;
-    const int tiles = m_tiles * ((N + bn - 1) / bn);
-    const int waves = (tiles + num_sms - 1) / num_sms;
-    const double cost = waves * (bn + 32.0);
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best = bn;
-    }
-  }
-  return best;
-}
-
-}  // namespace
 
 bool gemm_split_k(int N, int K, int epi) {
   // a function of the shape alone, never of M: a row's result must not
@@ -520,8 +24,9 @@ hb_status gemm_launch(const DeviceCtx& ctx, const void* A, int lda, const void* 
   if (split != nullptr && !gemm_split_k(N, K, epi)) split = nullptr;
   // split-K units use the widest tile (N = 256 MMAs run near the tensor peak)
   const int bn = split ? 256 : choose_bn(M, N, epi, ctx.num_sms);
-#define HB_GEMM_CASE(BN_, EPI_) \
-  if (bn == BN_ && epi == EPI_) return launch<BN_, EPI_>(ctx, A, lda, B, C, ldc, R, M, N, K, norm, split, stream);
+#define HB_GEMM_CASE(BN_, EPI_)                                                                                \
+  if (bn == BN_ && epi == EPI_)                                                                                \
+    return launch<BN_, EPI_, false>(ctx, A, lda, nullptr, B, nullptr, C, ldc, R, M, N, K, norm, split, stream);
   HB_GEMM_CASE(256, HB_EPI_STORE)
   HB_GEMM_CASE(192, HB_EPI_STORE)
   HB_GEMM_CASE(128, HB_EPI_STORE)
@@ -550,6 +55,7 @@ hb_status gemm_check(const void* A, const void* B, void* C, const void* R, int M
   return HB_OK;
 }
 
+namespace {
 // ---------------------------------------------------------------- weight prep
 // w_gu row 128*b + e holds gate row 64*b + e (e < 64) or up row 64*b + e - 64;
 // rows past F (when F % 64 != 0) are zero.
@@ -565,6 +71,7 @@ __global__ void interleave_gate_up_kernel(const uint4* __restrict__ wg, const ui
     out[i] = src < F ? (e < 64 ? wg : wu)[static_cast<size_t>(src) * d8 + c] : make_uint4(0, 0, 0, 0);
   }
 }
+}  // namespace
 
 }  // namespace hb
 

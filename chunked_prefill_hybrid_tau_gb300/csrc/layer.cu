@@ -12,6 +12,13 @@
 // projection's epilogue (rmsnorm2, no separate pass).  Every stage is one
 // kernel launch on the caller's stream (attention: two, see attention.cu);
 // the workspace is carved into 256-byte aligned regions.
+//
+// E4M3 weights (FP8 projections, reading notes section 7.7): each
+// projection's input is quantized per token right before it (x together
+// with its row statistics, then o, h and the SwiGLU output), and the
+// projections run on the tensor cores' FP8 path with the per-row scales of
+// both operands applied in the epilogue; the 1/rms factors still come from
+// the bf16 rows.
 #include <cuda_runtime.h>
 
 #include "runtime.h"
@@ -25,7 +32,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline int ffn_pad(const hb_layer_dims& dm) { return (dm.d_ff + 63) / 64 * 64; }
 
 struct LayerWs {
-  size_t ss_x, ss_h, qkv, q, o, h, a, part_o, part_d, flags, attn, total;
+  size_t ss_x, ss_h, qkv, q, o, h, a, part_o, part_d, flags, q8_x, q8_o, q8_h, q8_a, s8, attn, total;
 };
 
 LayerWs layer_ws(const hb_layer_dims& dm, int T, int S, int max_kv_len) {
@@ -42,6 +49,12 @@ LayerWs layer_ws(const hb_layer_dims& dm, int T, int S, int max_kv_len) {
   w.part_o = off; off += align256(gemm_split_part_bytes(T, dm.d_model));
   w.part_d = off; off += align256(gemm_split_part_bytes(T, dm.d_model));
   w.flags = off;  off += align256(static_cast<size_t>(2) * gemm_split_flags(T, dm.d_model) * 4);
+  // E4M3 operands of the four projections and their per-token scales
+  w.q8_x = off; off += align256(t * dm.d_model);
+  w.q8_o = off; off += align256(t * dm.n_q * dm.d_head);
+  w.q8_h = off; off += align256(t * dm.d_model);
+  w.q8_a = off; off += align256(t * ffn_pad(dm));
+  w.s8 = off;   off += 4 * align256(t * 4);
   w.attn = off; off += align256(attention_workspace_bytes(dm, S, max_kv_len));
   w.total = off;
   return w;
@@ -66,6 +79,13 @@ extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_
   if (st != HB_OK) return st;
   HB_REQUIRE(w && plan, "hb_layer_forward: null weights or plan");
   HB_REQUIRE(w->w_qkv && w->w_o && w->w_gu && w->w_d, "hb_layer_forward: null weight");
+  HB_REQUIRE(w->format == HB_WEIGHTS_BF16 || w->format == HB_WEIGHTS_E4M3, "hb_layer_forward: unknown format %d",
+             w->format);
+  const bool f8 = w->format == HB_WEIGHTS_E4M3;
+  HB_REQUIRE(!f8 || (w->s_qkv && w->s_o && w->s_gu && w->s_d), "hb_layer_forward: E4M3 weights need scales");
+  HB_REQUIRE(!f8 || (aligned16(w->s_qkv) && aligned16(w->s_o) && aligned16(w->s_gu) && aligned16(w->s_d)),
+             "hb_layer_forward: E4M3 scales must be 16-byte aligned");
+  HB_REQUIRE(!f8 || dims->d_ff % 16 == 0, "hb_layer_forward: E4M3 weights need d_ff %% 16 == 0");
   HB_REQUIRE(x_in && x_out && k_cache && v_cache && rope, "hb_layer_forward: null pointer");
   HB_REQUIRE(plan->n_rows >= 0 && plan->n_seqs >= 0, "hb_layer_forward: bad plan sizes");
   HB_REQUIRE(plan->n_rows == 0 || (plan->row_pos && plan->slot_mapping && plan->seq_q_start && plan->seq_kv_len &&
@@ -127,6 +147,37 @@ extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_
   split_d.part = reinterpret_cast<float*>(ws + lw.part_d);
   split_o.flags = reinterpret_cast<int*>(ws + lw.flags);
   split_d.flags = split_o.flags + n_flags;
+  if (f8) {
+    uint8_t* xq = ws + lw.q8_x;
+    uint8_t* oq = ws + lw.q8_o;
+    uint8_t* hq = ws + lw.q8_h;
+    uint8_t* aq = ws + lw.q8_a;
+    float* sx = reinterpret_cast<float*>(ws + lw.s8);
+    float* so = sx + align256(static_cast<size_t>(T) * 4) / 4;
+    float* sh = so + align256(static_cast<size_t>(T) * 4) / 4;
+    float* sa = sh + align256(static_cast<size_t>(T) * 4) / 4;
+    HB_STEP(0, quant_rows_launch(ctx, x_in, xq, sx, T, d, ss_x, split_o.flags, 2 * n_flags, s));
+    HB_STEP(1, gemm_e4m3_launch(ctx, xq, d, sx, w->w_qkv, w->s_qkv, qkv, qkv_cols, nullptr, T, qkv_cols, d,
+                                HB_EPI_STORE, s, &norm_x));
+    HB_STEP(2, kv_append_launch(ctx, qkv, T, plan->row_pos, plan->slot_mapping, rope, max_pos, dm, q, k_cache,
+                                v_cache, num_pages, s));
+    HB_STEP(3, attention_launch(ctx, q, k_cache, v_cache, num_pages, *plan, dm, max_kv_len, o, aws,
+                                lw.total - lw.attn, s));
+    HB_STEP(4, quant_rows_launch(ctx, o, oq, so, T, hd, nullptr, nullptr, 0, s));
+    st = gemm_e4m3_launch(ctx, oq, hd, so, w->w_o, w->s_o, h, d, x_in, T, d, hd, HB_EPI_RESIDUAL, s, &norm_h_out,
+                          &split_o);
+    if (st != HB_OK) return st;
+    HB_STEP(5, HB_OK);
+    HB_STEP(6, quant_rows_launch(ctx, h, hq, sh, T, d, nullptr, nullptr, 0, s));
+    st = gemm_e4m3_launch(ctx, hq, d, sh, w->w_gu, w->s_gu, a, fp, nullptr, T, 2 * fp, d, HB_EPI_SWIGLU, s,
+                          &norm_h_in);
+    if (st != HB_OK) return st;
+    HB_STEP(7, quant_rows_launch(ctx, a, aq, sa, T, fp, nullptr, nullptr, 0, s));
+    st = gemm_e4m3_launch(ctx, aq, fp, sa, w->w_d, w->s_d, x_out, d, h, T, d, dm.d_ff, HB_EPI_RESIDUAL, s, nullptr,
+                          &split_d);
+    if (st != HB_OK) return st;
+    return mark(HB_LAYER_STAGES);
+  }
   HB_STEP(0, row_sumsq_launch(ctx, x_in, ss_x, T, d, split_o.flags, 2 * n_flags, s));
   HB_STEP(1, gemm_launch(ctx, x_in, d, w->w_qkv, qkv, qkv_cols, nullptr, T, qkv_cols, d, HB_EPI_STORE, s, &norm_x));
   HB_STEP(2, kv_append_launch(ctx, qkv, T, plan->row_pos, plan->slot_mapping, rope, max_pos, dm, q, k_cache, v_cache,

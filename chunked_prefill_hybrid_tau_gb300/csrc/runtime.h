@@ -19,10 +19,12 @@ hb_status device_context(DeviceCtx* ctx);
 hb_status cuda_status(cudaError_t e, const char* what);
 hb_status launch_status(const char* what);
 
-// 2D bf16 tensor map: `outer` rows of `inner` elements, rows `row_stride_bytes`
-// apart; box of box_inner x box_outer elements.
+// 2D tensor map of bf16 (elem_bytes 2) or byte (elem_bytes 1: E4M3 codes)
+// elements: `outer` rows of `inner` elements, rows `row_stride_bytes` apart;
+// box of box_inner x box_outer elements.
 hb_status encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128);
+                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128,
+                         int elem_bytes = 2);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -88,6 +90,22 @@ struct GemmSplit {
 bool gemm_split_k(int N, int K, int epi);
 size_t gemm_split_part_bytes(int M, int N);  // fp32 partial tiles
 int gemm_split_flags(int M, int N);          // arrival counters (ints)
+
+// E4M3 projections: A [M][K] and B [N][K] codes (row stride lda bytes for A,
+// K for B) with per-row fp32 scales sa [M] and sb [N]; the epilogues are the
+// bf16 ones applied to sa[m] sb[n] acc.
+hb_status gemm_e4m3_launch(const DeviceCtx& ctx, const void* A, int lda, const float* sa, const void* B,
+                           const float* sb, void* C, int ldc, const void* R, int M, int N, int K, int epi,
+                           cudaStream_t stream, const GemmNorm* norm = nullptr, const GemmSplit* split = nullptr);
+hb_status gemm_e4m3_check(const void* A, const float* sa, const void* B, const float* sb, void* C, const void* R,
+                          int M, int N, int K, int epi);
+
+// Per-row E4M3 quantization of bf16 rows x [rows][cols] (row stride cols):
+// codes q [rows][cols], scales [rows]; with ss != nullptr also the row
+// statistics of x in the GemmNorm layout (cols % 32 == 0), and n_zero ints
+// at `zero` cleared (as row_sumsq_launch).
+hb_status quant_rows_launch(const DeviceCtx& ctx, const void* x, void* q, float* scale, int rows, int cols,
+                            float* ss, int* zero, int n_zero, cudaStream_t stream);
 
 // A [M][K] with row stride lda, B [N][K], C/R with row stride ldc (elements).
 hb_status gemm_launch(const DeviceCtx& ctx, const void* A, int lda, const void* B, void* C, int ldc, const void* R,

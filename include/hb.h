@@ -322,6 +322,34 @@ typedef enum hb_epilogue {
 hb_status hb_gemm(const void* A, const void* B, void* C, const void* R, int32_t M, int32_t N, int32_t K,
                   int32_t epilogue, void* stream);
 
+/* ------------------------------------------------------------------------
+ * hb_quantize_e4m3 - per-row FP8 quantization, the operand preparation of
+ * the E4M3 projections (FP8 doubles the FLOPs per byte of the linear layers
+ * and moves their knee to the right: Sarathi-Serve reading notes, section
+ * 7.7).  Format: OCP E4M3 (largest finite magnitude 448).  For each row r of
+ * x [rows][cols] (device bf16):
+ *   amax = max_c |x[r][c]|, inv = 448 / amax, scale[r] = amax / 448
+ *   (correctly rounded fp32 divisions),
+ *   q[r][c] = E4M3(fp32(x[r][c] * inv)), nearest-even, saturating to +-448;
+ * an all-zero row gets scale 0 and zero codes.  q: device bytes
+ * [rows][cols]; scale: device fp32 [rows].  cols % 16 == 0 and cols <= 32768,
+ * x and q 16-byte aligned.  Asynchronous on stream.  Used for weights (rows =
+ * output channels) and for activations (rows = tokens).
+ * ---------------------------------------------------------------------- */
+hb_status hb_quantize_e4m3(const void* x, void* q, float* scale, int32_t rows, int32_t cols, void* stream);
+
+/* ------------------------------------------------------------------------
+ * hb_gemm_e4m3 - C = epilogue(s_a[m] s_b[n] (A B^T)) with E4M3 operands on
+ * the tensor cores (kind::f8f6f4, fp32 accumulate): A [M][K] codes with
+ * per-row scales s_a [M], B [N][K] codes with per-row scales s_b [N] (both
+ * from hb_quantize_e4m3).  The epilogues are hb_gemm's, applied to the
+ * scaled accumulator (SWIGLU: s_b holds the scales of the interleaved rows).
+ * K % 16 == 0, N % 8 == 0 (N % 128 for SWIGLU); A, B, C, R and s_b 16-byte
+ * aligned.
+ * ---------------------------------------------------------------------- */
+hb_status hb_gemm_e4m3(const void* A, const float* s_a, const void* B, const float* s_b, void* C, const void* R,
+                       int32_t M, int32_t N, int32_t K, int32_t epilogue, void* stream);
+
 /* Weight preparation: w_gu[2 Fp][d], Fp = F rounded up to a multiple of 64,
  * from w_gate[F][d] and w_up[F][d] (device bf16): rows interleaved in blocks
  * of 64 ([gate 0..63, up 0..63, gate 64..127, ...]); rows of the padding
@@ -344,11 +372,14 @@ hb_status hb_fold_gamma(const void* w, const void* gamma, void* out, int32_t row
  *   x_out = h + (silu(hn W_g^T) * hn W_u^T) W_d^T
  * the "run_iteration(B)" step of the scheduling loop (Sarathi-Serve reading
  * notes, section 3.4) for one layer.
- *   w      : device bf16 weights, prepared once (see hb_layer_weights):
- *            both RMSNorm gains folded in, gate/up interleaved.  The norms
- *            run inside the projections: (x * r * g) W^T = r * x (W diag g)^T
+ *   w      : device weights, prepared once (see hb_layer_weights): both
+ *            RMSNorm gains folded in, gate/up interleaved.  The norms run
+ *            inside the projections: (x * r * g) W^T = r * x (W diag g)^T
  *            with r = 1/sqrt(mean(x^2) + eps) applied per row in fp32 to the
- *            accumulators of the QKV and gate/up GEMMs.
+ *            accumulators of the QKV and gate/up GEMMs.  HB_WEIGHTS_E4M3:
+ *            x, o, h and the SwiGLU output are quantized per token
+ *            (hb_quantize_e4m3's rule, r still from the bf16 rows) and the
+ *            projections run as hb_gemm_e4m3; d_ff % 16 == 0 required.
  *   plan   : device plan; rope: table from hb_rope_table with max_pos rows
  *   x_in   : device bf16 [T][d_model]; x_out may alias x_in
  *   caches : updated in place with this iteration's K/V
@@ -357,14 +388,27 @@ hb_status hb_fold_gamma(const void* w, const void* gamma, void* out, int32_t row
  *            on `stream` before stage k and events[HB_LAYER_STAGES] after the
  *            last, stages = rmsnorm1 (row statistics of x), qkv, rope+kv,
  *            attention, o+residual (+ statistics of h), rmsnorm2 (no launch:
- *            folded), gate/up+swiglu, down+residual.
+ *            folded), gate/up+swiglu, down+residual.  HB_WEIGHTS_E4M3: the
+ *            quantization of a projection's input is part of the stage of
+ *            that projection (rmsnorm1 quantizes x).
  * ---------------------------------------------------------------------- */
+typedef enum hb_weight_format {
+  HB_WEIGHTS_BF16 = 0, /* bf16 matrices */
+  HB_WEIGHTS_E4M3 = 1  /* each matrix as E4M3 codes of its bf16 form (hb_quantize_e4m3) with per-row scales;
+                          the four projection inputs are quantized per token inside the layer */
+} hb_weight_format;
+
 typedef struct hb_layer_weights {
-  const void* w_qkv;  /* bf16 [(n_q + 2 n_kv) d_head][d_model] = W_qkv diag(g1) (hb_fold_gamma) */
-  const void* w_o;    /* bf16 [d_model][n_q d_head] */
-  const void* w_gu;   /* bf16 [2 Fp][d_model]: hb_interleave_gate_up of W_g, W_u (Fp = d_ff rounded up to
+  const void* w_qkv;  /* [(n_q + 2 n_kv) d_head][d_model] = W_qkv diag(g1) (hb_fold_gamma) */
+  const void* w_o;    /* [d_model][n_q d_head] */
+  const void* w_gu;   /* [2 Fp][d_model]: hb_interleave_gate_up of W_g, W_u (Fp = d_ff rounded up to
                          64), then hb_fold_gamma with g2 */
-  const void* w_d;    /* bf16 [d_model][d_ff] */
+  const void* w_d;    /* [d_model][d_ff] */
+  const float* s_qkv; /* HB_WEIGHTS_E4M3: per-row scales of the four matrices (16-byte aligned); */
+  const float* s_o;   /* NULL for HB_WEIGHTS_BF16 */
+  const float* s_gu;
+  const float* s_d;
+  int32_t format;     /* hb_weight_format */
 } hb_layer_weights;
 
 #define HB_LAYER_STAGES 8

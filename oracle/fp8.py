@@ -133,7 +133,11 @@ def prepare_weights(w):
         "u": ol.round_bf16(np.asarray(w["w_u"], f32) * np.asarray(w["g2"], f32)[None, :]),
         "d": np.asarray(w["w_d"], f32),
     }
-    return {k: quantize_rows(v) for k, v in fold.items()}
+    def by_rows(m, block=2048):  # rows are independent; blocks only bound the memory in use
+        parts = [quantize_rows(m[i:i + block]) for i in range(0, m.shape[0], block)]
+        return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts])
+
+    return {k: by_rows(v) for k, v in fold.items()}
 
 
 def layer_forward(wq, dims, plan, x, k_pool, v_pool, cos, sin, storage=None, dtype=np.float32,

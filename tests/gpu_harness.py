@@ -63,9 +63,10 @@ def plan_both(st: wl.State, tau: int, chunk: int, max_pages=None):
 class GpuLayer:
     """One layer's weights, caches and RoPE table on the device."""
 
-    def __init__(self, w: dict, dims, k_pool: np.ndarray, v_pool: np.ndarray, max_pos: int, device="cuda"):
+    def __init__(self, w: dict, dims, k_pool: np.ndarray, v_pool: np.ndarray, max_pos: int, device="cuda",
+                 fmt="bf16"):
         self.dims = dims
-        self.w = wd.layer_weights_device(w, dims, device)
+        self.w = wd.layer_weights_device(w, dims, device, fmt=fmt)
         self.k = wd.bf16_tensor(k_pool, device)
         self.v = wd.bf16_tensor(v_pool, device)
         self.max_pos = max_pos

@@ -24,12 +24,12 @@ def to_numpy(t) -> np.ndarray:
     return t.detach().float().cpu().numpy()
 
 
-def layer_weights_device(w: dict, dims, device="cuda"):
+def layer_weights_device(w: dict, dims, device="cuda", fmt="bf16"):
     """Upload one layer's weights and prepare them with the library (gains
-    folded, gate/up interleaved)."""
+    folded, gate/up interleaved; fmt="e4m3": then quantized per row)."""
     import chunked_prefill_hybrid_tau_gb300 as hb
     return hb.prepare_layer_weights(*[bf16_tensor(w[k], device) for k in ("w_qkv", "w_o", "w_g", "w_u", "w_d",
-                                                                          "g1", "g2")])
+                                                                          "g1", "g2")], fmt=fmt)
 
 
 def rope_table_device(max_pos: int, dims, device="cuda"):
@@ -76,14 +76,14 @@ def _layer_draws(dims, seed, device):
     return w_qkv, w_o, w_g, w_u, w_d
 
 
-def layer_weights_random(dims, seed, device="cuda"):
+def layer_weights_random(dims, seed, device="cuda", fmt="bf16"):
     """One layer's weights on the device from `seed`: N(0, 0.02) projections,
-    gains 1, prepared by the library."""
+    gains 1, prepared by the library (fmt as in layer_weights_device)."""
     import torch
     import chunked_prefill_hybrid_tau_gb300 as hb
     w_qkv, w_o, w_g, w_u, w_d = _layer_draws(dims, seed, device)
     ones = torch.ones(dims.d_model, dtype=torch.bfloat16, device=device)
-    return hb.prepare_layer_weights(w_qkv, w_o, w_g, w_u, w_d, ones, ones)
+    return hb.prepare_layer_weights(w_qkv, w_o, w_g, w_u, w_d, ones, ones, fmt=fmt)
 
 
 def host_layer_weights(dims, seed, device="cuda") -> dict:
