@@ -30,7 +30,7 @@ namespace {
 using namespace dev;
 
 constexpr int SPLIT = 1024;                 // keys per decode split
-constexpr int HALF_BYTES = 16 * 128;        // one TMA box: 16 keys x 64 dims (128-byte rows)
+constexpr int HALF_BYTES = 16 * 128;        // one 64-dim half of a page: 16 keys x 128-byte rows
 constexpr int MAX_SEQS = 1024;
 
 struct Params {
@@ -263,19 +263,18 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
     }
     __syncwarp();
 
-    // page b of this unit into slot b % DR: lane 0 arms the slot, lanes
-    // 0 .. 2*(D/64)-1 then issue one TMA box each (K or V, one 64-dim half)
+    // page b of this unit into slot b % DR: lane 0 arms the slot, lanes 0
+    // and 1 then issue one TMA box each (the whole K or V page, both halves)
     auto issue = [&](int b) {
       const int slot = b % DR;
       uint8_t* dst = ring + slot * STAGE_BYTES;
       if (lane == 0) mbar_arrive_expect_tx(&full[slot], STAGE_BYTES);
       __syncwarp();
-      if (lane < 2 * (D / 64)) {
+      if (lane < 2) {
         const int page = btc[b];
         const int y = (page * p.n_kv + g) * 16;
-        const int hf = lane >> 1;
         const bool is_v = lane & 1;
-        tma_load_2d(dst + (is_v ? PAGE_BYTES : 0) + hf * HALF_BYTES, is_v ? &tmV : &tmK, &full[slot], hf * 64, y);
+        tma_load_3d(dst + (is_v ? PAGE_BYTES : 0), is_v ? &tmV : &tmK, &full[slot], 0, y, 0);
       }
     };
     for (int b = 0; b < min(DR, npages); ++b) issue(b);
@@ -506,7 +505,8 @@ int chunk_sms(const DeviceCtx& ctx, const hb_device_plan& plan, const hb_layer_d
 
 template <int D>
 hb_status attention_launch_d(const DeviceCtx& ctx, const void* q, const hb_device_plan& plan, const hb_layer_dims& dm,
-                             const CUtensorMap& tmK, const CUtensorMap& tmV, Params p, cudaStream_t stream) {
+                             const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmK3,
+                             const CUtensorMap& tmV3, Params p, cudaStream_t stream) {
   static bool attr_set[64] = {};
   if (!attr_set[ctx.device]) {
     hb_status st = cuda_status(
@@ -521,7 +521,7 @@ hb_status attention_launch_d(const DeviceCtx& ctx, const void* q, const hb_devic
     hb_status st =
         chunk_tc_launch(ctx, q, tmK, tmV, plan, dm, p.num_pages, p.max_kv_len, p.out, p.work_counter, ctx.num_sms, stream);
     if (st != HB_OK) return st;
-    decode_kernel<D><<<ctx.num_sms, kDecWarps * 32, DC<D>::SMEM, stream>>>(tmK, tmV, p);
+    decode_kernel<D><<<ctx.num_sms, kDecWarps * 32, DC<D>::SMEM, stream>>>(tmK3, tmV3, p);
     return launch_status("decode_kernel launch");
   }
   SideStream* ss = nullptr;
@@ -533,7 +533,7 @@ hb_status attention_launch_d(const DeviceCtx& ctx, const void* q, const hb_devic
   if (st != HB_OK) return st;
   st = chunk_tc_launch(ctx, q, tmK, tmV, plan, dm, p.num_pages, p.max_kv_len, p.out, p.work_counter, nc, ss->stream);
   if (st != HB_OK) return st;
-  decode_kernel<D><<<ctx.num_sms - nc, kDecWarps * 32, DC<D>::SMEM, stream>>>(tmK, tmV, p);
+  decode_kernel<D><<<ctx.num_sms - nc, kDecWarps * 32, DC<D>::SMEM, stream>>>(tmK3, tmV3, p);
   st = launch_status("decode_kernel launch");
   if (st != HB_OK) return st;
   st = cuda_status(cudaEventRecord(ss->join, ss->stream), "cudaEventRecord(join)");
@@ -566,11 +566,15 @@ hb_status attention_launch(const DeviceCtx& ctx, const void* q, const void* k_ca
   HB_REQUIRE(ws != nullptr && ws_bytes >= need, "hb_attention: workspace of %zu bytes needed, %zu given", need,
              ws_bytes);
   HB_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "hb_attention: workspace must be 256-byte aligned");
-  CUtensorMap tmK, tmV;
+  CUtensorMap tmK, tmV, tmK3, tmV3;  // 2-D half-page boxes (chunk kernel), 3-D whole pages (decode kernel)
   const uint64_t rows = static_cast<uint64_t>(num_pages) * dm.n_kv * 16;
   hb_status st = encode_tmap_2d(&tmK, k_cache, dm.d_head, rows, dm.d_head * 2, 64, 16, true);
   if (st != HB_OK) return st;
   st = encode_tmap_2d(&tmV, v_cache, dm.d_head, rows, dm.d_head * 2, 64, 16, true);
+  if (st != HB_OK) return st;
+  st = encode_tmap_kv_pages(&tmK3, k_cache, rows, dm.d_head);
+  if (st != HB_OK) return st;
+  st = encode_tmap_kv_pages(&tmV3, v_cache, rows, dm.d_head);
   if (st != HB_OK) return st;
   const size_t counters = counter_bytes(dm, plan.n_seqs);
   st = cuda_status(cudaMemsetAsync(ws, 0, counters, stream), "cudaMemsetAsync(attention counters)");
@@ -595,8 +599,8 @@ hb_status attention_launch(const DeviceCtx& ctx, const void* q, const void* k_ca
   p.combine_counters = reinterpret_cast<int*>(w8 + 256);
   p.partials = reinterpret_cast<float*>(w8 + counters);
   p.status = ctx.status;
-  return dm.d_head == 128 ? attention_launch_d<128>(ctx, q, plan, dm, tmK, tmV, p, stream)
-                          : attention_launch_d<64>(ctx, q, plan, dm, tmK, tmV, p, stream);
+  return dm.d_head == 128 ? attention_launch_d<128>(ctx, q, plan, dm, tmK, tmV, tmK3, tmV3, p, stream)
+                          : attention_launch_d<64>(ctx, q, plan, dm, tmK, tmV, tmK3, tmV3, p, stream);
 }
 
 }  // namespace hb

@@ -12,10 +12,12 @@
 //
 // Warp roles (352 threads, one CTA per SM):
 //   warps 0, 10  TMA producers: warp 0 loads the unit's Q tile (3-D box over
-//            [T][n_q][D]) and each block's 8 K pages into a 2-stage K ring,
+//            [T][n_q][D]) and each block's 8 K pages into a 3-stage K ring,
 //            warp 10 the V pages into a 2-stage V ring (16 keys x 64 dims per
 //            box, 128-byte swizzle).  A K stage is released when its S block
-//            is computed, a V stage when its PV block is;
+//            is computed, a V stage when its PV block is.  Block-table entries
+//            are read four blocks ahead and checked when used, so the issue
+//            cadence is not bound by the latency of those loads;
 //   warp 1   MMA issuer (one thread), issuing whichever is ready first:
 //            S_j = Q K_j^T into one of two TMEM S buffers (K-major operands),
 //            or O += P_j V_j with P read from one of two TMEM P buffers and V
@@ -42,7 +44,8 @@ using namespace dev;
 
 constexpr int TQ = 128;           // query rows per unit (MMA M)
 constexpr int TK = 128;           // keys per block (MMA N of S, K of PV)
-constexpr int NSTAGE = 2;
+constexpr int KSTAGE = 3;         // K ring depth: S blocks wait on K loads, so K runs deeper
+constexpr int VSTAGE = 2;         // V ring depth
 constexpr int MAX_SEQS = 1024;
 constexpr int kSoftWarps = 8;                // two threads per query row (column halves)
 constexpr int kVWarp = 2 + kSoftWarps;        // the V producer
@@ -56,14 +59,15 @@ struct TC {
   static constexpr int Q_BYTES = HALVES * HALF_TILE;     // Q tile
   static constexpr int KV_BYTES = HALVES * HALF_TILE;    // K (or V) block of 128 keys
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = Q_BYTES;                  // K ring [NSTAGE]
-  static constexpr int OFF_V = OFF_K + NSTAGE * KV_BYTES;  // V ring [NSTAGE]
-  static constexpr int OFF_BAR = OFF_V + NSTAGE * KV_BYTES;
-  static constexpr int BAR_BYTES = 256;
+  static constexpr int OFF_K = Q_BYTES;                  // K ring [KSTAGE]
+  static constexpr int OFF_V = OFF_K + KSTAGE * KV_BYTES;  // V ring [VSTAGE]
+  static constexpr int OFF_BAR = OFF_V + VSTAGE * KV_BYTES;
+  static constexpr int BAR_BYTES = 512;
   static constexpr int OFF_XCH = OFF_BAR + BAR_BYTES;    // row maxima / sums exchanged by the two halves
   static constexpr int XCH_BYTES = (2 * 2 * 128 + 2 * 128) * 4;
   static constexpr int OFF_PRE = OFF_XCH + XCH_BYTES;
   static constexpr int SMEM = OFF_PRE + (MAX_SEQS + 1) * 4 + 1024;
+  static_assert(SMEM <= 232448, "shared memory");
   static constexpr uint32_t TMEM_COLS = 512;             // S0 | S1 | O | P0 | P1
   static constexpr uint32_t COL_O = 256;
   static constexpr uint32_t COL_P = 384;                 // P_b (bf16, 2 keys per column) at COL_P + 64 b
@@ -109,15 +113,6 @@ __device__ __forceinline__ TcUnit tc_unit(const TcParams& p, const int* pre, int
   w.pos0 = p.kv_len[s] - qlen + t * TQ;
   w.nblk = (w.pos0 + w.nrows + TK - 1) / TK;
   return w;
-}
-
-__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
-                                            int32_t y, int32_t z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-      "[%5];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-      : "memory");
 }
 
 // O (+)= A B^T with A (M x K bf16) read from tensor memory, B a shared-memory
@@ -173,24 +168,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* k_full = bar;                   // [NSTAGE]
-  uint64_t* k_empty = bar + 2;              // [NSTAGE]
-  uint64_t* q_full = bar + 4;
-  uint64_t* q_empty = bar + 5;
-  uint64_t* s_full = bar + 6;               // [2]
-  uint64_t* s_empty = bar + 8;              // [2]
-  uint64_t* p_full = bar + 25;              // [2] P_b stored (8 warps), once per use of buffer b
-  uint64_t* pv_done = bar + 27;             // [2] the PV that read P_b has completed
-  uint64_t* o_empty = bar + 12;
-  uint64_t* uq_full = bar + 13;             // [2]
-  uint64_t* uq_empty = bar + 15;            // [2]
-  uint64_t* drain = bar + 17;
-  uint64_t* xbar = bar + 18;                // [2] row maxima exchanged (block parity)
-  uint64_t* xsbar = bar + 20;               // row sums exchanged (once per unit)
-  uint64_t* v_full = bar + 21;              // [NSTAGE]
-  uint64_t* v_empty = bar + 23;             // [NSTAGE]
-  int* uq = reinterpret_cast<int*>(bar + 29);  // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(uq + 2);
+  uint64_t* k_full = bar;                   // [KSTAGE]
+  uint64_t* k_empty = bar + 4;              // [KSTAGE]
+  uint64_t* v_full = bar + 8;               // [VSTAGE]
+  uint64_t* v_empty = bar + 12;             // [VSTAGE]
+  uint64_t* q_full = bar + 16;
+  uint64_t* q_empty = bar + 17;
+  uint64_t* s_full = bar + 18;              // [2]
+  uint64_t* s_empty = bar + 20;             // [2]
+  uint64_t* o_empty = bar + 22;
+  uint64_t* uq_full = bar + 23;             // [2]
+  uint64_t* uq_empty = bar + 25;            // [2]
+  uint64_t* drain = bar + 27;
+  uint64_t* xbar = bar + 28;                // [2] row maxima exchanged (block parity)
+  uint64_t* xsbar = bar + 30;               // row sums exchanged (once per unit)
+  uint64_t* p_full = bar + 31;              // [2] P_b stored (8 warps), once per use of buffer b
+  uint64_t* pv_done = bar + 33;             // [2] the PV that read P_b has completed
+  int* uq = reinterpret_cast<int*>(bar + 35);  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 36);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* xmax = reinterpret_cast<float*>(smem + C::OFF_XCH);  // [2 parity][2 half][128 rows]
   float* xsum = xmax + 2 * 2 * 128;                             // [2 half][128 rows]
@@ -210,9 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     pre[s + 1] = c;
   }
   if (tid == 0) {
-    for (int i = 0; i < NSTAGE; ++i) {
+    for (int i = 0; i < KSTAGE; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < VSTAGE; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
@@ -268,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ring = kside ? sK : sV;
     uint64_t* full = kside ? k_full : v_full;
     uint64_t* empty = kside ? k_empty : v_empty;
+    const int nst = kside ? KSTAGE : VSTAGE;
     int qs = 0, stage = 0, nunit = 0;
     uint32_t qph = 0, kph = 0;
     uint32_t pending = 0, armed = 0;
@@ -315,23 +313,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int* bt = p.block_table + static_cast<size_t>(w.seq) * p.max_pages;
       const int key_end = w.pos0 + w.nrows;
       const int my_pg = lane / C::HALVES, my_hf = lane % C::HALVES;
-      // this lane's page id of block j, validated (one block ahead)
-      auto fetch_page = [&](int j) {
-        const int npg = min(8, (key_end - j * TK + 15) / 16);
-        int page = 0;
-        if (my_pg < npg) {
-          page = __ldg(bt + j * 8 + my_pg);
-          if (page < 0 || page >= p.num_pages) {
-            flag_error(p.status, kStatusIndex);
-            page = 0;
-          }
-        }
-        return page;
+      // this lane's raw page id of block j (0 past the last block), loaded
+      // four blocks ahead and checked at use
+      auto load_page = [&](int j) {
+        const int npg = j < w.nblk ? min(8, (key_end - j * TK + 15) / 16) : 0;
+        return my_pg < npg ? __ldg(bt + j * 8 + my_pg) : 0;
       };
-      int nxt = fetch_page(0);
+      int pf0 = load_page(0), pf1 = load_page(1), pf2 = load_page(2), pf3 = load_page(3);
       for (int j = 0; j < w.nblk; ++j) {
-        const int cur = nxt;
-        if (j + 1 < w.nblk) nxt = fetch_page(j + 1);
+        int cur = pf0;
+        pf0 = pf1;
+        pf1 = pf2;
+        pf2 = pf3;
+        pf3 = load_page(j + 4);
+        if (cur < 0 || cur >= p.num_pages) {
+          flag_error(p.status, kStatusIndex);
+          cur = 0;
+        }
         const int npg = min(8, (key_end - j * TK + 15) / 16);
         bool eok = true;
         if (lane == 0) {
@@ -350,14 +348,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* dst = ring + stage * C::KV_BYTES + my_hf * C::HALF_TILE + my_pg * 2048;
           tma_load_2d(dst, tm, &full[stage], my_hf * 64, (cur * p.n_kv + g) * 16);
         }
-        if (++stage == NSTAGE) {
+        if (++stage == nst) {
           stage = 0;
           kph ^= 1u;
         }
       }
     }
     if (!ok && lane == 0)
-      for (int s = 0; s < NSTAGE; ++s)
+      for (int s = 0; s < nst; ++s)
         if (pending & (1u << s)) mbar_drain(&full[s], (armed >> s) & 1u);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -389,8 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (ok && jp < w.nblk) {
           bool progressed = false;
           if (js < w.nblk) {
-            const int gk = J + js, b = gk & 1, st = gk % NSTAGE;
-            if (mbar_test(&k_full[st], (gk / NSTAGE) & 1) && mbar_test(&s_empty[b], ((gk >> 1) & 1) ^ 1u)) {
+            const int gk = J + js, b = gk & 1, st = gk % KSTAGE;
+            if (mbar_test(&k_full[st], (gk / KSTAGE) & 1) && mbar_test(&s_empty[b], ((gk >> 1) & 1) ^ 1u)) {
               tc_fence_after();
               const uint32_t k_addr = smem_u32(sK + st * C::KV_BYTES);
 #pragma unroll
@@ -407,11 +405,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (jp < js) {
-            const int gv = J + jp, st = gv % NSTAGE;
+            const int gv = J + jp, st = gv % VSTAGE;
             // O of the previous unit has been read by the epilogue before the first PV
             if (!o_free) o_free = mbar_test(o_empty, (nunit & 1) ^ 1u);
             const int pb = gv & 1;  // P buffer of this block; its use number is gv >> 1
-            if (o_free && mbar_test(&p_full[pb], (gv >> 1) & 1) && mbar_test(&v_full[st], (gv / NSTAGE) & 1)) {
+            if (o_free && mbar_test(&p_full[pb], (gv >> 1) & 1) && mbar_test(&v_full[st], (gv / VSTAGE) & 1)) {
               tc_fence_after();
               const uint32_t v_addr = smem_u32(sV + st * C::KV_BYTES);
 #pragma unroll
@@ -567,8 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // keys past key_end may hold uninitialised memory: zero their V rows
           // once the V block has landed (its stage cannot be refilled before
           // this block's PV, which waits for p_full below)
-          const int gv = J + j, stage = gv % NSTAGE;
-          bool vok = mbar_wait(&v_full[stage], (gv / NSTAGE) & 1, abort_flag, p.status);
+          const int gv = J + j, stage = gv % VSTAGE;
+          bool vok = mbar_wait(&v_full[stage], (gv / VSTAGE) & 1, abort_flag, p.status);
           if (!__all_sync(0xffffffffu, vok)) {
             ok = false;
             break;

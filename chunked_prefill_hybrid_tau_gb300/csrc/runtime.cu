@@ -125,6 +125,24 @@ hb_status encode_tmap_q3d(CUtensorMap* map, const void* q, int T, int n_q, int d
   return HB_OK;
 }
 
+hb_status encode_tmap_kv_pages(CUtensorMap* map, const void* pool, uint64_t rows, int d_head) {
+  hb_status st = resolve_encode();
+  if (st != HB_OK) return st;
+  const cuuint32_t halves = static_cast<cuuint32_t>(d_head / 64);
+  cuuint64_t dims[3] = {64, rows, halves};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d_head) * 2, 128};
+  cuuint32_t box[3] = {64, 16, halves};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (res != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled (kv pages, 3-D) failed (%d)", static_cast<int>(res));
+    return HB_ERR_INVALID_ARG;
+  }
+  return HB_OK;
+}
+
 hb_status launch_status(const char* what) { return cuda_status(cudaGetLastError(), what); }
 
 }  // namespace hb

@@ -52,6 +52,12 @@ hb_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 hb_status encode_tmap_q3d(CUtensorMap* map, const void* q, int T, int n_q, int d_head);
+// 3-D map over a paged K or V pool [page][n_kv][16][d_head] bf16 seen as
+// (64 dims, rows = (page * n_kv + head) * 16 + key, d_head / 64 halves): one
+// box of 64 x 16 x (d_head / 64) loads a whole 16-key page of one kv head as
+// [half][key][128 bytes] with the 128-byte swizzle, the layout of two
+// separate 64-dim boxes placed 2 KB apart.
+hb_status encode_tmap_kv_pages(CUtensorMap* map, const void* pool, uint64_t rows, int d_head);
 hb_status chunk_tc_launch(const DeviceCtx& ctx, const void* q, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const hb_device_plan& plan, const hb_layer_dims& dims, int num_pages, int max_kv_len,
                           void* out, int* work_counter, int grid, cudaStream_t stream);
