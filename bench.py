@@ -403,30 +403,63 @@ def run_hb(args, world, rank, local):
     stage_ms /= len(ev)
 
     # ---- end to end through the C ABI with host buffers ------------------
+    # Every step uploads its input from pinned host memory and reads its
+    # output back.  The copies run on their own streams with two device
+    # buffers each way, so step i + 1's upload and step i's download overlap
+    # step i's compute; a buffer is reused only after the step that last used
+    # it (layer or copy) has finished with it.
     x_host = torch.from_numpy(wd.to_numpy(x_dev).astype(np.float32)).to(torch.bfloat16).pin_memory()
-    out_host = torch.empty_like(x_host).pin_memory()
-    x_in2 = torch.empty_like(x_dev)
+    out_host = [torch.empty_like(x_host).pin_memory() for _ in range(2)]
+    x_in = [torch.empty_like(x_dev) for _ in range(2)]
+    y_out = [torch.empty_like(x_dev) for _ in range(2)]
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     e_steps = max(1, min(args.steps, 1000))
-    for _ in range(min(args.warmup, 5)):
-        with torch.cuda.stream(stream):
-            x_in2.copy_(x_host, non_blocking=True)
-        layer(runner.step(stream), x_in2, out_dev)
-        with torch.cuda.stream(stream):
-            out_host.copy_(out_dev, non_blocking=True)
-    stream.synchronize()
+
+    def e2e_run(n, e0=None):
+        if n == 0:
+            return
+        uploaded, computed, fetched = ([torch.cuda.Event(), torch.cuda.Event()] for _ in range(3))
+        if e0 is not None:
+            up.wait_event(e0)
+            down.wait_event(e0)
+
+        def upload(i):
+            b = i % 2
+            if i >= 2:
+                up.wait_event(computed[b])  # the layer of step i - 2 has read x_in[b]
+            with torch.cuda.stream(up):
+                x_in[b].copy_(x_host, non_blocking=True)
+            uploaded[b].record(up)
+
+        upload(0)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:
+                upload(i + 1)
+            stream.wait_event(uploaded[b])
+            if i >= 2:
+                stream.wait_event(fetched[b])  # step i - 2's output has been read back
+            layer(runner.step(stream), x_in[b], y_out[b])
+            computed[b].record(stream)
+            down.wait_event(computed[b])
+            with torch.cuda.stream(down):
+                out_host[b].copy_(y_out[b], non_blocking=True)
+            fetched[b].record(down)
+        stream.wait_event(fetched[(n - 1) % 2])
+        if n >= 2:
+            stream.wait_event(fetched[(n - 2) % 2])
+
+    e2e_run(min(args.warmup, 5))
+    torch.cuda.synchronize(dev)
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e_steps):
-        with torch.cuda.stream(stream):
-            x_in2.copy_(x_host, non_blocking=True)
-        layer(runner.step(stream), x_in2, out_dev)
-        with torch.cuda.stream(stream):
-            out_host.copy_(out_dev, non_blocking=True)
+    e2e_run(e_steps, e0)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     hb.hb_check_status(stream)
+    out_host = out_host[0]
     t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
     e2e = {"value": world * T * e_steps / t_e2e, "unit": "tokens/s",
            "h2d_bytes_per_step": int(x_host.numel() * 2 + runner.h2d_bytes),
