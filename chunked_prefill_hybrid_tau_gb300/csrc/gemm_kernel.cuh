@@ -182,6 +182,131 @@ __device__ __forceinline__ void scale_cols(uint32_t (&r)[32], float rowf, const 
   }
 }
 
+// Epilogue of one 128 x BN accumulator block in TMEM (t_base: this warp's
+// 32 lanes) for output row `row` of the warp's thread: SwiGLU, residual (with
+// the split-K exchange on 128-row tile `stile`, K half `half`) or store.
+// scale: the row's folded RMSNorm factor; rowf: scale times the row's E4M3
+// scale (F8).
+template <int BN, int EPI, bool F8>
+__device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_base, int row, bool row_ok, int rloc,
+                                              int n_blk, int stile, int half, int quarter, int lane, float scale,
+                                              float rowf) {
+  if (EPI == HB_EPI_SWIGLU) {
+#pragma unroll 1
+    for (int j = 0; j < BN / 128; ++j) {
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        uint32_t g[32], u[32];
+        tmem_ld_32x32b_x32(t_base + j * 128 + h * 32, g);
+        tmem_ld_32x32b_x32(t_base + j * 128 + 64 + h * 32, u);
+        tmem_ld_wait();
+        const int col = n_blk * (BN / 2) + j * 64 + h * 32;
+        if (row_ok && col < p.out_cols) {
+          if constexpr (F8) {
+            // gate and up rows of w_gu have their own scales
+            const int bcol = n_blk * BN + j * 128 + h * 32;
+            scale_cols(g, rowf, p.sb, bcol, p.N);
+            scale_cols(u, rowf, p.sb, bcol + 64, p.N);
+          }
+          const float sc = F8 ? 1.f : scale;
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a0 = silu(__uint_as_float(g[2 * i]) * sc) * (__uint_as_float(u[2 * i]) * sc);
+            const float a1 = silu(__uint_as_float(g[2 * i + 1]) * sc) * (__uint_as_float(u[2 * i + 1]) * sc);
+            w[i] = pack_bf16x2(a0, a1);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) +
+                                                static_cast<size_t>(row) * p.ldc + col);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (col + 8 * i < p.out_cols) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+    }
+  } else {
+    bool finish = true;  // this warp writes the output rows of the tile
+    const float* other = nullptr;
+    if (p.ksplit == 2) {
+      // Split K: publish this half's fp32 partial (column-major, so each
+      // store is one coalesced 128-byte line per warp); the second warp
+      // to arrive for this 32-row slab adds the other half and finishes.
+      // p0 + p1 is commutative, so the result does not depend on which
+      // half arrives last.
+      float* mine = p.part + (static_cast<size_t>(stile) * 2 + half) * BN * BM;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_base + c * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) mine[static_cast<size_t>(c * 32 + j) * BM + rloc] = __uint_as_float(r[j]);
+      }
+      __threadfence();
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) {
+        int* flag = p.flags + stile * 4 + quarter;
+        last = atomicAdd(flag, 1) == 1;
+        if (last) *flag = 0;
+      }
+      finish = __shfl_sync(0xffffffffu, last, 0) != 0;
+      if (finish) {
+        __threadfence();
+        other = p.part + (static_cast<size_t>(stile) * 2 + (1 - half)) * BN * BM;
+      }
+    }
+    if (finish && EPI == HB_EPI_RESIDUAL) {
+      // software-pipelined: the residual (and the other half's partial)
+      // of chunk c + 1 is in flight while chunk c is combined and stored
+      constexpr int NC = BN / 32;
+      uint4 rv[2][4];
+      float ov[2][32];
+      auto fetch = [&](int c, int b) {
+        const int col = n_blk * BN + c * 32;
+        const uint4* res = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.R) +
+                                                          static_cast<size_t>(row) * p.ldc + col);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          rv[b][i] = (row_ok && col + 8 * i < p.out_cols) ? res[i] : make_uint4(0, 0, 0, 0);
+        if (other != nullptr) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ov[b][j] = __ldcg(other + static_cast<size_t>(c * 32 + j) * BM + rloc);
+        }
+      };
+      fetch(0, 0);
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        const int b = c & 1;
+        if (c + 1 < NC) fetch(c + 1, b ^ 1);
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_base + c * 32, r);
+        tmem_ld_wait();
+        if (other != nullptr) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + ov[b][j]);
+        }
+        const int col = n_blk * BN + c * 32;
+        if constexpr (F8) scale_cols(r, rowf, p.sb, col, p.N);
+        float* ss_dst = p.norm.ss_out != nullptr
+                            ? p.norm.ss_out + static_cast<size_t>(row) * p.norm.parts + col / 32
+                            : nullptr;
+        if (row_ok && col < p.out_cols) residual_chunk(p, row, col, r, rv[b], ss_dst);
+      }
+    } else if (finish) {
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_base + c * 32, r);
+        tmem_ld_wait();
+        const int col = n_blk * BN + c * 32;
+        if constexpr (F8) scale_cols(r, rowf, p.sb, col, p.N);
+        if (row_ok && col < p.out_cols) store_chunk<EPI>(p, row, col, r, F8 ? 1.f : scale);
+      }
+    }
+  }
+}
+
 template <int BN, int EPI, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
@@ -355,120 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-      if (EPI == HB_EPI_SWIGLU) {
-#pragma unroll 1
-        for (int j = 0; j < BN / 128; ++j) {
-#pragma unroll 1
-          for (int h = 0; h < 2; ++h) {
-            uint32_t g[32], u[32];
-            tmem_ld_32x32b_x32(t_base + j * 128 + h * 32, g);
-            tmem_ld_32x32b_x32(t_base + j * 128 + 64 + h * 32, u);
-            tmem_ld_wait();
-            const int col = n_blk * (BN / 2) + j * 64 + h * 32;
-            if (row_ok && col < p.out_cols) {
-              if constexpr (F8) {
-                // gate and up rows of w_gu have their own scales
-                const int bcol = n_blk * BN + j * 128 + h * 32;
-                scale_cols(g, rowf, p.sb, bcol, p.N);
-                scale_cols(u, rowf, p.sb, bcol + 64, p.N);
-              }
-              const float sc = F8 ? 1.f : scale;
-              uint32_t w[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float a0 = silu(__uint_as_float(g[2 * i]) * sc) * (__uint_as_float(u[2 * i]) * sc);
-                const float a1 = silu(__uint_as_float(g[2 * i + 1]) * sc) * (__uint_as_float(u[2 * i + 1]) * sc);
-                w[i] = pack_bf16x2(a0, a1);
-              }
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) +
-                                                    static_cast<size_t>(row) * p.ldc + col);
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                if (col + 8 * i < p.out_cols) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-            }
-          }
-        }
-      } else {
-        bool finish = true;  // this warp writes the output rows of the tile
-        const float* other = nullptr;
-        if (p.ksplit == 2) {
-          // Split K: publish this half's fp32 partial (column-major, so each
-          // store is one coalesced 128-byte line per warp); the second warp
-          // to arrive for this 32-row slab adds the other half and finishes.
-          // p0 + p1 is commutative, so the result does not depend on which
-          // half arrives last.
-          float* mine = p.part + (static_cast<size_t>(wu.tile) * 2 + wu.half) * BN * BM;
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(t_base + c * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) mine[static_cast<size_t>(c * 32 + j) * BM + rloc] = __uint_as_float(r[j]);
-          }
-          __threadfence();
-          __syncwarp();
-          int last = 0;
-          if (lane == 0) {
-            int* flag = p.flags + wu.tile * 4 + quarter;
-            last = atomicAdd(flag, 1) == 1;
-            if (last) *flag = 0;
-          }
-          finish = __shfl_sync(0xffffffffu, last, 0) != 0;
-          if (finish) {
-            __threadfence();
-            other = p.part + (static_cast<size_t>(wu.tile) * 2 + (1 - wu.half)) * BN * BM;
-          }
-        }
-        if (finish && EPI == HB_EPI_RESIDUAL) {
-          // software-pipelined: the residual (and the other half's partial)
-          // of chunk c + 1 is in flight while chunk c is combined and stored
-          constexpr int NC = BN / 32;
-          uint4 rv[2][4];
-          float ov[2][32];
-          auto fetch = [&](int c, int b) {
-            const int col = n_blk * BN + c * 32;
-            const uint4* res = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.R) +
-                                                              static_cast<size_t>(row) * p.ldc + col);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              rv[b][i] = (row_ok && col + 8 * i < p.out_cols) ? res[i] : make_uint4(0, 0, 0, 0);
-            if (other != nullptr) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) ov[b][j] = __ldcg(other + static_cast<size_t>(c * 32 + j) * BM + rloc);
-            }
-          };
-          fetch(0, 0);
-#pragma unroll
-          for (int c = 0; c < NC; ++c) {
-            const int b = c & 1;
-            if (c + 1 < NC) fetch(c + 1, b ^ 1);
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(t_base + c * 32, r);
-            tmem_ld_wait();
-            if (other != nullptr) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + ov[b][j]);
-            }
-            const int col = n_blk * BN + c * 32;
-            if constexpr (F8) scale_cols(r, rowf, p.sb, col, p.N);
-            float* ss_dst = p.norm.ss_out != nullptr
-                                ? p.norm.ss_out + static_cast<size_t>(row) * p.norm.parts + col / 32
-                                : nullptr;
-            if (row_ok && col < p.out_cols) residual_chunk(p, row, col, r, rv[b], ss_dst);
-          }
-        } else if (finish) {
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(t_base + c * 32, r);
-            tmem_ld_wait();
-            const int col = n_blk * BN + c * 32;
-            if constexpr (F8) scale_cols(r, rowf, p.sb, col, p.N);
-            if (row_ok && col < p.out_cols) store_chunk<EPI>(p, row, col, r, F8 ? 1.f : scale);
-          }
-        }
-      }
+      epilogue_tile<BN, EPI, F8>(p, t_base, row, row_ok, rloc, n_blk, wu.tile, wu.half, quarter, lane, scale, rowf);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
@@ -481,6 +493,269 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
+}
+
+// ---------------------------------------------------------------- CTA pairs
+// A cluster of two CTAs on neighbouring SMs computes 256 x 256 tiles with
+// tcgen05.mma.cta_group::2: each CTA holds its 128 rows of A and its 128 of
+// the tile's 256 B rows (the even CTA the first 128) in shared memory, the
+// even CTA's MMA thread issues M = 256, N = 256 MMAs, and each CTA's tensor
+// memory receives its own 128 accumulator rows.  Every SM then streams 32 KB
+// per k-block for the FLOPs a 128 x 256 tile streams 48 KB for.
+//   * both CTAs' TMA loads of a stage complete on the even CTA's `full`
+//     barrier (armed once with both CTAs' bytes); the MMA commit frees the
+//     stage in both CTAs (multicast), and after a tile's last k-block it
+//     signals both CTAs' accumulator barriers;
+//   * the epilogue warps of both CTAs hand the accumulator buffer back on the
+//     even CTA's `acc_empty` (count 8);
+//   * a tile of the pair covers 128-row tiles 2 pm and 2 pm + 1 of the
+//     single-CTA numbering, so split-K partials and counters are shared with
+//     gemm_kernel's layout.
+constexpr int kPairBN = 256;
+struct CfgPair {
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = (kPairBN / 2) * 128;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = 6;
+  static constexpr int TMEM_COLS = 512;  // two 256-column accumulators
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+};
+
+struct PairUnit {
+  int pm, n_blk, half, kb0, kb1;
+};
+
+__device__ __forceinline__ PairUnit pair_unit_of(const Params& p, int u, int pm_tiles, int kblocks) {
+  PairUnit w;
+  const int tile = u / p.ksplit;
+  w.half = u - tile * p.ksplit;
+  w.pm = tile % pm_tiles;
+  w.n_blk = tile / pm_tiles;
+  const int per = (kblocks + p.ksplit - 1) / p.ksplit;
+  w.kb0 = w.half * per;
+  w.kb1 = w.kb0 + per < kblocks ? w.kb0 + per : kblocks;
+  return w;
+}
+
+template <int EPI, bool F8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
+  using C = CfgPair;
+  constexpr int BN = kPairBN;
+  constexpr int BK = bk_elems<F8>();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);  // even CTA's are used
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint64_t* acc_empty = acc_full + 2;  // even CTA's are used
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int m_tiles = (p.M + BM - 1) / BM;
+  const int pm_tiles = (m_tiles + 1) / 2;
+  const int n_tiles = (p.N + BN - 1) / BN;
+  const int units = pm_tiles * n_tiles * p.ksplit;
+  const int kblocks = (p.K + BK - 1) / BK;
+  const int cluster = static_cast<int>(blockIdx.x >> 1);
+  const int n_clusters = static_cast<int>(gridDim.x >> 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 8);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  griddep_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers exist before anything arrives on them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    griddep_wait();
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      uint32_t pending = 0, armed_parity = 0;  // stages loaded and not yet seen released
+      for (int u = cluster; u < units && ok; u += n_clusters) {
+        const PairUnit w = pair_unit_of(p, u, pm_tiles, kblocks);
+        const int m0 = (2 * w.pm + static_cast<int>(rank)) * BM;
+        const int n0 = w.n_blk * BN + static_cast<int>(rank) * (BN / 2);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          pending |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          uint8_t* sa = smem + stage * C::STAGE_BYTES;
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);  // both CTAs' boxes
+          const uint32_t fb = cluster_addr(&full[stage], 0);
+          tma_load_2d_pair(sa, &tmA, fb, kb * BK, m0);
+          tma_load_2d_pair(sa + C::A_BYTES, &tmB, fb, kb * BK, n0);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Normally every loaded stage is consumed by a pair MMA before the MMA
+      // thread drains, and the final cluster barrier follows that drain.
+      // After an expired wait, let the boxes still in flight land (their
+      // stage is released once consumed; a short bounded wait otherwise).
+      if (!ok)
+        for (int s2 = 0; s2 < C::STAGES; ++s2)
+          if (pending & (1u << s2)) mbar_drain(&empty[s2], (armed_parity >> s2) & 1u);
+    }
+  } else if (warp == 1) {
+    griddep_wait();
+    // ---------------------------------------------------------- MMA issuer (even CTA)
+    if (leader && lane == 0) {
+      constexpr uint32_t kIdesc = F8 ? idesc_e4m3_f32(2 * BM, BN) : idesc_bf16_f32(2 * BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int t = 0;
+      bool ok = true;
+      for (int u = cluster; u < units && ok; u += n_clusters, ++t) {
+        const PairUnit w = pair_unit_of(p, u, pm_tiles, kblocks);
+        const int acc = t & 1;
+        const uint32_t acc_phase = (t >> 1) & 1;
+        if (!mbar_wait_cluster(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!mbar_wait_cluster(&full[stage], phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + C::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if constexpr (F8)
+              mma_e4m3_pair(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), kIdesc,
+                            (kb != w.kb0 || k != 0) ? 1u : 0u);
+            else
+              mma_bf16_pair(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), kIdesc,
+                            (kb != w.kb0 || k != 0) ? 1u : 0u);
+          }
+          mma_commit_pair(&empty[stage], 3);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) mma_commit_pair(&acc_full[acc], 3);
+      }
+      // no pair MMA may still read either CTA's shared memory or write its
+      // tensor memory when the CTAs leave
+      mma_commit_pair(drain, 1);
+      mbar_drain(drain, 0);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue (both CTAs)
+    griddep_wait();
+    const int quarter = warp & 3;
+    int t = 0;
+    for (int un = cluster; un < units; un += n_clusters, ++t) {
+      const PairUnit wu = pair_unit_of(p, un, pm_tiles, kblocks);
+      const int acc = t & 1;
+      const uint32_t acc_phase = (t >> 1) & 1;
+      const int mt = 2 * wu.pm + static_cast<int>(rank);  // this CTA's 128-row tile
+      const int rloc = quarter * 32 + lane;
+      const int row = mt * BM + rloc;
+      const bool row_ok = row < p.M;
+      const float scale = (p.norm.ss_in != nullptr && row_ok) ? row_inv_rms(p.norm, row) : 1.f;
+      const float rowf = F8 && row_ok ? scale * p.sa[row] : scale;
+      bool ok = mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      if (mt < m_tiles) {  // a 128-row tile wholly past M (odd tile count) has nothing to write
+        const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+        epilogue_tile<BN, EPI, F8>(p, t_base, row, row_ok, rloc, wu.n_blk, mt + m_tiles * wu.n_blk, wu.half,
+                                   quarter, lane, scale, rowf);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(cluster_addr(&acc_empty[acc], 0));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int EPI, bool F8>
+hb_status launch_pair(const DeviceCtx& ctx, const void* A, int lda, const float* sa, const void* B, const float* sb,
+                      void* Cp, int ldc, const void* R, int M, int N, int K, const GemmNorm* norm,
+                      const GemmSplit* split, cudaStream_t stream) {
+  using C = CfgPair;
+  constexpr int BK = bk_elems<F8>();
+  constexpr int ESZ = F8 ? 1 : 2;
+  CUtensorMap tmA, tmB;
+  hb_status st = encode_tmap_2d(&tmA, A, K, M, static_cast<uint64_t>(lda) * ESZ, BK, BM, true, ESZ);
+  if (st != HB_OK) return st;
+  st = encode_tmap_2d(&tmB, B, K, N, static_cast<uint64_t>(K) * ESZ, BK, kPairBN / 2, true, ESZ);
+  if (st != HB_OK) return st;
+  static bool attr_set[64] = {};
+  if (!attr_set[ctx.device]) {
+    st = cuda_status(cudaFuncSetAttribute(gemm_pair_kernel<EPI, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          C::SMEM),
+                     "cudaFuncSetAttribute(gemm pair)");
+    if (st != HB_OK) return st;
+    attr_set[ctx.device] = true;
+  }
+  Params p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.C = Cp;
+  p.R = R;
+  p.ldc = ldc;
+  p.out_cols = EPI == HB_EPI_SWIGLU ? N / 2 : N;
+  p.status = ctx.status;
+  p.norm = norm ? *norm : GemmNorm{};
+  p.ksplit = split ? 2 : 1;
+  p.part = split ? split->part : nullptr;
+  p.flags = split ? split->flags : nullptr;
+  p.sa = sa;
+  p.sb = sb;
+  const int m_tiles = (M + BM - 1) / BM;
+  const int units = ((m_tiles + 1) / 2) * ((N + kPairBN - 1) / kPairBN) * p.ksplit;
+  const int pairs = ctx.num_sms / 2;
+  const int grid = 2 * (units < pairs ? units : pairs);
+  return launch_pdl(gemm_pair_kernel<EPI, F8>, grid, kThreads, C::SMEM, stream, "gemm_pair_kernel launch", tmA, tmB,
+                    p);
 }
 
 // A [M][K] (row stride lda elements), B [N][K]; sa/sb: E4M3 scales (F8 only).

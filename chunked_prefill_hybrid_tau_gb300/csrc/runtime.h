@@ -94,6 +94,8 @@ struct GemmSplit {
   int* flags = nullptr;
 };
 bool gemm_split_k(int N, int K, int epi);
+// Whether a projection runs on 256 x 256 CTA-pair tiles (tcgen05 cta_group::2).
+bool gemm_use_pair(int M, int N, int epi, bool split);
 size_t gemm_split_part_bytes(int M, int N);  // fp32 partial tiles
 int gemm_split_flags(int M, int N);          // arrival counters (ints)
 

@@ -75,7 +75,8 @@ GEMM_CASES = [
     (333, 1024, 640, L.HB_EPI_STORE),        # ragged M
     (68, 200, 688, L.HB_EPI_STORE),          # N not a multiple of 32, K not of 128
     (512, 4096, 4096, L.HB_EPI_RESIDUAL),
-    (512, 4096, 14336, L.HB_EPI_RESIDUAL),   # split K
+    (512, 4096, 14336, L.HB_EPI_RESIDUAL),   # split K (CTA pairs)
+    (333, 4096, 8192, L.HB_EPI_RESIDUAL),    # split K, odd number of 128-row tiles
     (70, 768, 192, L.HB_EPI_RESIDUAL),
     (300, 1024, 384, L.HB_EPI_SWIGLU),
     (512, 28672, 4096, L.HB_EPI_SWIGLU),

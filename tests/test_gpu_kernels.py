@@ -77,6 +77,7 @@ GEMM_CASES = [
     (300, 1024, 384, L.HB_EPI_SWIGLU),
     (128, 25600, 256, L.HB_EPI_SWIGLU),      # 256-wide tiles
     (512, 28672, 4096, L.HB_EPI_SWIGLU),
+    (333, 4096, 8192, L.HB_EPI_RESIDUAL),   # split K on CTA pairs, odd number of 128-row tiles
     (65, 32000, 4096, L.HB_EPI_F32),
     (3, 640, 128, L.HB_EPI_F32),
     (68, 200, 688, L.HB_EPI_STORE),          # K and N not multiples of 64 / 32
@@ -118,6 +119,34 @@ def test_gemm(M, N, K, epi):
         assert_close(got, ref, "gemm f32", atol=1e-3, rtol=1e-3, rel_l2=1e-4)
     else:
         assert_close(got, ref, f"gemm epi={epi}")
+
+
+@pytest.mark.parametrize("N,K,epi", [(1024, 512, L.HB_EPI_SWIGLU), (28672, 4096, L.HB_EPI_SWIGLU),
+                                     (4096, 8192, L.HB_EPI_RESIDUAL)])
+def test_gemm_pair_tiles_match_single_cta_tiles_bitwise(N, K, epi):
+    """Projections with more than one 128-row tile run on 256 x 256 CTA-pair
+    tiles, a single 128-row tile on one CTA: a row's result must not depend on
+    which, so 128 rows computed alone equal the same rows computed inside a
+    512-row batch bit for bit."""
+    rng = np.random.default_rng(N + K)
+    A = wl.bf16_round(rng.standard_normal((512, K), dtype=np.float32))
+    W = wl.bf16_round(rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02))
+    Wt = wd.bf16_tensor(W)
+    if epi == L.HB_EPI_SWIGLU:
+        Wgu = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+        hb.hb_interleave_gate_up(wd.bf16_tensor(W[:N // 2]), wd.bf16_tensor(W[N // 2:]), Wgu)
+        Wt = Wgu
+    cols = N // 2 if epi == L.HB_EPI_SWIGLU else N
+    R = wl.bf16_round(rng.standard_normal((512, cols), dtype=np.float32))
+    outs = []
+    for M in (512, 128):
+        At = wd.bf16_tensor(A[:M])
+        out = wd.bf16_tensor(R[:M]) if epi == L.HB_EPI_RESIDUAL else torch.empty((M, cols), dtype=torch.bfloat16,
+                                                                                  device="cuda")
+        hb.hb_gemm(At, Wt, out, out if epi == L.HB_EPI_RESIDUAL else None, epi)
+        hb.hb_check_status()
+        outs.append(out[:128])
+    assert torch.equal(outs[0], outs[1])
 
 
 @pytest.mark.parametrize("n_q,n_kv,d_head", [(8, 2, 128), (4, 2, 64), (14, 2, 128)])
