@@ -426,15 +426,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_empty[b]);
-        // mask and scale (base 2), this half's row maximum, then the full row's
+        // this half's row maximum of the raw scores (the scale is positive),
+        // masked keys set to -inf; only a block crossing this row's last key
+        // needs the mask; then the full row's maximum in base-2 units
         const int key0 = j * TK + half * HK;
         float mx = -INFINITY;
+        if (key0 + HK - 1 <= lim) {
 #pragma unroll
-        for (int c = 0; c < HK; ++c) {
-          const float v = key0 + c <= lim ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
-          sv[c] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
+          for (int c = 0; c < HK; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < HK; ++c) {
+            const float s = key0 + c <= lim ? __uint_as_float(sv[c]) : -INFINITY;
+            sv[c] = __float_as_uint(s);
+            mx = fmaxf(mx, s);
+          }
         }
+        mx *= p.scale_log2;
         // exchange with the other half of the row (mbarrier per block parity;
         // a phase cannot run ahead: it needs every softmax warp's arrival)
         float* xm = xmax + ((J + j) & 1) * 256;
@@ -475,12 +483,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = m_new;
         l *= alpha;
         // P = 2^(s - m) as bf16: this thread's 64 keys are row r of P half `half`
+        // P = 2^(s scale - m) (one rounding for the exponent argument)
         float rs = 0.f;
         uint32_t pk[HK / 2];
+        const float neg_m = -m_used;
 #pragma unroll
         for (int c = 0; c < HK / 2; ++c) {
-          const float a0 = ex2_approx(__uint_as_float(sv[2 * c]) - m_used);
-          const float a1 = ex2_approx(__uint_as_float(sv[2 * c + 1]) - m_used);
+          const float a0 = ex2_approx(fmaf(__uint_as_float(sv[2 * c]), p.scale_log2, neg_m));
+          const float a1 = ex2_approx(fmaf(__uint_as_float(sv[2 * c + 1]), p.scale_log2, neg_m));
           rs += a0 + a1;
           pk[c] = pack_bf16x2(a0, a1);
         }
