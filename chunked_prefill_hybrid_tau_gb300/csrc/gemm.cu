@@ -21,7 +21,9 @@ int gemm_split_flags(int M, int N) { return ((M + BM - 1) / BM) * ((N + 255) / 2
 
 bool gemm_use_pair(int M, int N, int epi, bool split) {
   // 256 x 256 pair tiles for the wide projections with more than one
-  // 128-row tile: gate/up (SwiGLU) and the split-K residual ones
+  // 128-row tile: gate/up (SwiGLU) and the split-K residual ones.  (The QKV
+  // and O projections at M = 512 gain nothing from pairs: one tile per CTA,
+  // bound by the ring fill and the epilogue, not by the shared-memory fill.)
   return M > BM && N % kPairBN == 0 && (epi == HB_EPI_SWIGLU || (epi == HB_EPI_RESIDUAL && split));
 }
 
@@ -30,8 +32,10 @@ hb_status gemm_launch(const DeviceCtx& ctx, const void* A, int lda, const void* 
   if (split != nullptr && !gemm_split_k(N, K, epi)) split = nullptr;
   if (gemm_use_pair(M, N, epi, split != nullptr)) {
     if (epi == HB_EPI_SWIGLU)
-      return launch_pair<HB_EPI_SWIGLU, false>(ctx, A, lda, nullptr, B, nullptr, C, ldc, R, M, N, K, norm, split, stream);
-    return launch_pair<HB_EPI_RESIDUAL, false>(ctx, A, lda, nullptr, B, nullptr, C, ldc, R, M, N, K, norm, split, stream);
+      return launch_pair<kPairBN, HB_EPI_SWIGLU, false>(ctx, A, lda, nullptr, B, nullptr, C, ldc, R, M, N, K, norm, split,
+                                                      stream);
+    return launch_pair<kPairBN, HB_EPI_RESIDUAL, false>(ctx, A, lda, nullptr, B, nullptr, C, ldc, R, M, N, K, norm, split,
+                                                      stream);
   }
   // split-K units use the widest tile (N = 256 MMAs run near the tensor peak)
   const int bn = split ? 256 : choose_bn(M, N, epi, ctx.num_sms);

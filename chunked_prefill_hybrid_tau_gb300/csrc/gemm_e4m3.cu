@@ -19,8 +19,10 @@ hb_status gemm_e4m3_launch(const DeviceCtx& ctx, const void* A, int lda, const f
   if (split != nullptr && !gemm_split_k(N, K, epi)) split = nullptr;
   if (gemm_use_pair(M, N, epi, split != nullptr)) {
     if (epi == HB_EPI_SWIGLU)
-      return launch_pair<HB_EPI_SWIGLU, true>(ctx, A, lda, sa, B, sb, C, ldc, R, M, N, K, norm, split, stream);
-    return launch_pair<HB_EPI_RESIDUAL, true>(ctx, A, lda, sa, B, sb, C, ldc, R, M, N, K, norm, split, stream);
+      return launch_pair<kPairBN, HB_EPI_SWIGLU, true>(ctx, A, lda, sa, B, sb, C, ldc, R, M, N, K, norm, split,
+                                                      stream);
+    return launch_pair<kPairBN, HB_EPI_RESIDUAL, true>(ctx, A, lda, sa, B, sb, C, ldc, R, M, N, K, norm, split,
+                                                      stream);
   }
   const int bn = split ? 256 : choose_bn(M, N, epi, ctx.num_sms);
 #define HB_GEMM_CASE(BN_, EPI_) \

@@ -496,12 +496,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- CTA pairs
-// A cluster of two CTAs on neighbouring SMs computes 256 x 256 tiles with
-// tcgen05.mma.cta_group::2: each CTA holds its 128 rows of A and its 128 of
-// the tile's 256 B rows (the even CTA the first 128) in shared memory, the
-// even CTA's MMA thread issues M = 256, N = 256 MMAs, and each CTA's tensor
-// memory receives its own 128 accumulator rows.  Every SM then streams 32 KB
-// per k-block for the FLOPs a 128 x 256 tile streams 48 KB for.
+// A cluster of two CTAs on neighbouring SMs computes 256 x BN tiles with
+// tcgen05.mma.cta_group::2: each CTA holds its 128 rows of A and its BN / 2
+// of the tile's BN B rows (the even CTA the first half) in shared memory, the
+// even CTA's MMA thread issues M = 256, N = BN MMAs, and each CTA's tensor
+// memory receives its own 128 accumulator rows.  At BN = 256 every SM streams
+// 32 KB per k-block for the FLOPs a one-CTA 128 x 256 tile streams 48 KB for.
 //   * both CTAs' TMA loads of a stage complete on the even CTA's `full`
 //     barrier (armed once with both CTAs' bytes); the MMA commit frees the
 //     stage in both CTAs (multicast), and after a tile's last k-block it
@@ -511,13 +511,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   * a tile of the pair covers 128-row tiles 2 pm and 2 pm + 1 of the
 //     single-CTA numbering, so split-K partials and counters are shared with
 //     gemm_kernel's layout.
-constexpr int kPairBN = 256;
+constexpr int kPairBN = 256;  // the tile width of split-K pair projections
+template <int BN>
 struct CfgPair {
   static constexpr int A_BYTES = BM * 128;
-  static constexpr int B_BYTES = (kPairBN / 2) * 128;
+  static constexpr int B_BYTES = (BN / 2) * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = 6;
-  static constexpr int TMEM_COLS = 512;  // two 256-column accumulators
+  static constexpr int STAGES = BN == 256 ? 6 : (BN == 192 ? 7 : 8);
+  static constexpr int TMEM_COLS = 512;  // two BN-column accumulators
+  static_assert(BN == 128 || BN == 192 || BN == 256, "pair tile width");
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
@@ -539,11 +541,10 @@ __device__ __forceinline__ PairUnit pair_unit_of(const Params& p, int u, int pm_
   return w;
 }
 
-template <int EPI, bool F8>
+template <int BN, int EPI, bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
-  using C = CfgPair;
-  constexpr int BN = kPairBN;
+  using C = CfgPair<BN>;
   constexpr int BK = bk_elems<F8>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -715,21 +716,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int EPI, bool F8>
+template <int BN, int EPI, bool F8>
 hb_status launch_pair(const DeviceCtx& ctx, const void* A, int lda, const float* sa, const void* B, const float* sb,
                       void* Cp, int ldc, const void* R, int M, int N, int K, const GemmNorm* norm,
                       const GemmSplit* split, cudaStream_t stream) {
-  using C = CfgPair;
+  using C = CfgPair<BN>;
   constexpr int BK = bk_elems<F8>();
   constexpr int ESZ = F8 ? 1 : 2;
   CUtensorMap tmA, tmB;
   hb_status st = encode_tmap_2d(&tmA, A, K, M, static_cast<uint64_t>(lda) * ESZ, BK, BM, true, ESZ);
   if (st != HB_OK) return st;
-  st = encode_tmap_2d(&tmB, B, K, N, static_cast<uint64_t>(K) * ESZ, BK, kPairBN / 2, true, ESZ);
+  st = encode_tmap_2d(&tmB, B, K, N, static_cast<uint64_t>(K) * ESZ, BK, BN / 2, true, ESZ);
   if (st != HB_OK) return st;
   static bool attr_set[64] = {};
   if (!attr_set[ctx.device]) {
-    st = cuda_status(cudaFuncSetAttribute(gemm_pair_kernel<EPI, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    st = cuda_status(cudaFuncSetAttribute(gemm_pair_kernel<BN, EPI, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           C::SMEM),
                      "cudaFuncSetAttribute(gemm pair)");
     if (st != HB_OK) return st;
@@ -751,10 +752,10 @@ hb_status launch_pair(const DeviceCtx& ctx, const void* A, int lda, const float*
   p.sa = sa;
   p.sb = sb;
   const int m_tiles = (M + BM - 1) / BM;
-  const int units = ((m_tiles + 1) / 2) * ((N + kPairBN - 1) / kPairBN) * p.ksplit;
+  const int units = ((m_tiles + 1) / 2) * ((N + BN - 1) / BN) * p.ksplit;
   const int pairs = ctx.num_sms / 2;
   const int grid = 2 * (units < pairs ? units : pairs);
-  return launch_pdl(gemm_pair_kernel<EPI, F8>, grid, kThreads, C::SMEM, stream, "gemm_pair_kernel launch", tmA, tmB,
+  return launch_pdl(gemm_pair_kernel<BN, EPI, F8>, grid, kThreads, C::SMEM, stream, "gemm_pair_kernel launch", tmA, tmB,
                     p);
 }
 

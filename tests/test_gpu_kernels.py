@@ -122,7 +122,8 @@ def test_gemm(M, N, K, epi):
 
 
 @pytest.mark.parametrize("N,K,epi", [(1024, 512, L.HB_EPI_SWIGLU), (28672, 4096, L.HB_EPI_SWIGLU),
-                                     (4096, 8192, L.HB_EPI_RESIDUAL)])
+                                     (4096, 8192, L.HB_EPI_RESIDUAL), (4096, 4096, L.HB_EPI_RESIDUAL),
+                                     (6144, 4096, L.HB_EPI_STORE), (512, 256, L.HB_EPI_STORE)])
 def test_gemm_pair_tiles_match_single_cta_tiles_bitwise(N, K, epi):
     """Projections with more than one 128-row tile run on 256 x 256 CTA-pair
     tiles, a single 128-row tile on one CTA: a row's result must not depend on
