@@ -123,11 +123,13 @@ __device__ __forceinline__ void warp_page(uint32_t k_base, uint32_t v_base, int 
     mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
   }
   float alpha[2], muse[2];
+  bool grew = false;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const float mn = fmaxf(m[h], mx[h]);
     muse[h] = mn == -INFINITY ? 0.f : mn;
-    alpha[h] = exp2f(m[h] - muse[h]);
+    grew |= mn > m[h];
+    alpha[h] = ex2_approx(m[h] - muse[h]);  // 1 when the maximum did not grow
     m[h] = mn;
   }
   float rs[2] = {0.f, 0.f};
@@ -135,19 +137,22 @@ __device__ __forceinline__ void warp_page(uint32_t k_base, uint32_t v_base, int 
   for (int j = 0; j < 2; ++j) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float pv = exp2f(s[j][e] - muse[e >> 1]);
+      const float pv = ex2_approx(s[j][e] - muse[e >> 1]);
       s[j][e] = pv;
       rs[e >> 1] += pv;
     }
   }
   l[0] = l[0] * alpha[0] + rs[0];
   l[1] = l[1] * alpha[1] + rs[1];
+  // rescale O only when some row's maximum grew (else alpha = 1 exactly)
+  if (__any_sync(0xffffffffu, grew)) {
 #pragma unroll
-  for (int j = 0; j < D / 8; ++j) {
-    o[j][0] *= alpha[0];
-    o[j][1] *= alpha[0];
-    o[j][2] *= alpha[1];
-    o[j][3] *= alpha[1];
+    for (int j = 0; j < D / 8; ++j) {
+      o[j][0] *= alpha[0];
+      o[j][1] *= alpha[0];
+      o[j][2] *= alpha[1];
+      o[j][3] *= alpha[1];
+    }
   }
   uint32_t pa[4];
   pa[0] = pack_bf16x2(s[0][0], s[0][1]);
