@@ -223,7 +223,10 @@ def attention_case(dims, dec_ctx, prefills, tau, chunk, seed, poison=True):
 DEC_CTX = [0, 1, 15, 16, 17, 63, 64, 511, 512, 513, 1500, 2047]
 
 
-@pytest.mark.parametrize("n_q,n_kv,d_head", [(8, 2, 128), (14, 2, 128), (4, 2, 64), (32, 8, 128)])
+# (8, 2, 128), (32, 8, 128), (6, 3, 128): chunk rows on CTA pairs (an even number
+# of q heads per kv head; 6 q heads = 3 head pairs); (14, 2, 128) odd group and
+# (4, 2, 64) d_head 64: one CTA per unit
+@pytest.mark.parametrize("n_q,n_kv,d_head", [(8, 2, 128), (14, 2, 128), (4, 2, 64), (32, 8, 128), (6, 3, 128)])
 def test_attention_hybrid(n_q, n_kv, d_head):
     dims = wl.Dims(d_model=256, n_q=n_q, n_kv=n_kv, d_head=d_head, d_ff=64)
     got, ref, hp = attention_case(dims, DEC_CTX, [(600, 100)], len(DEC_CTX) + 130, 130, seed=n_q + d_head)
