@@ -264,6 +264,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (lane == 0 && *abort_flag) raise_peer_abort(abort_flag, static_cast<uint32_t>(rank));
     if (!ok && lane == 0)
       for (int s = 0; s < nst; ++s)
         if (pending & (1u << s)) mbar_drain(&empty[s], (armed >> s) & 1u);
@@ -332,6 +333,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         J += w.nblk;
         ++nunit;
       }
+      if (*abort_flag) raise_peer_abort(abort_flag, static_cast<uint32_t>(rank));
       // no pair MMA may still read either CTA's shared memory or write its
       // tensor memory when the CTAs leave
       mma_commit_pair(drain, 1);
@@ -508,6 +510,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive_cluster_relaxed(cluster_addr(o_empty, 0));  // O was read into registers
       ++nunit;
     }
+    if (lane == 0 && *abort_flag) raise_peer_abort(abort_flag, static_cast<uint32_t>(rank));
   }
 
   tc_fence_before();

@@ -136,6 +136,15 @@ __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t caddr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
 
+// Raise the abort flag of the pair's other CTA (the same shared-memory
+// variable there), so that its bounded waits give up at once instead of each
+// running to its time limit.  Both CTAs of a pair meet at a cluster barrier
+// before either exits, so the peer is still resident.
+__device__ __forceinline__ void raise_peer_abort(volatile int* abort_flag, uint32_t rank) {
+  const uint32_t a = cluster_addr(const_cast<int*>(abort_flag), rank ^ 1u);
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(1) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

@@ -628,6 +628,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // thread drains, and the final cluster barrier follows that drain.
       // After an expired wait, let the boxes still in flight land (their
       // stage is released once consumed; a short bounded wait otherwise).
+      if (*abort_flag) raise_peer_abort(abort_flag, rank);
       if (!ok)
         for (int s2 = 0; s2 < C::STAGES; ++s2)
           if (pending & (1u << s2)) mbar_drain(&empty[s2], (armed_parity >> s2) & 1u);
@@ -673,6 +674,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (ok) mma_commit_pair(&acc_full[acc], 3);
       }
+      if (*abort_flag) raise_peer_abort(abort_flag, rank);
       // no pair MMA may still read either CTA's shared memory or write its
       // tensor memory when the CTAs leave
       mma_commit_pair(drain, 1);
@@ -705,6 +707,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(cluster_addr(&acc_empty[acc], 0));
     }
+    if (lane == 0 && *abort_flag) raise_peer_abort(abort_flag, rank);
   }
 
   tc_fence_before();
