@@ -1,0 +1,49 @@
+"""The bench's cost model (chunked_prefill_hybrid_tau_gb300/costs.py) against
+closed forms: the projections' FLOPs are 2 T Psi (Sarathi-Serve reading
+notes, section 1.6), attention's are 4 n_q d_head sum(p + 1) over the rows
+(section 7.5b), E4M3 weights are read at one byte per parameter, and the FP8
+roofline halves the projections' tensor time (section 7.7)."""
+import numpy as np
+import pytest
+
+import oracle.plan as op
+import workloads as wl
+from chunked_prefill_hybrid_tau_gb300 import costs
+
+
+@pytest.fixture(scope="module")
+def plan():
+    rng = np.random.default_rng(12)
+    dims = wl.MISTRAL
+    st = wl.make_state(rng, dims, [int(c) for c in rng.integers(100, 3000, 24)], [(4096, 1024)], slack_pages=64,
+                       fill_kv=False)
+    p = op.plan_batch([r.done for r in st.decodes], [r.pages for r in st.decodes],
+                      [r.prompt_len for r in st.prefills], [r.done for r in st.prefills],
+                      [r.pages for r in st.prefills], st.free_pool, 512, 512, dims.page)
+    return dims, p
+
+
+def test_flops_closed_forms(plan):
+    dims, p = plan
+    sc = costs.stage_costs(dims, p.row_pos, p.seq_q_start, p.seq_kv_len)
+    T = len(p.row_pos)
+    linear = sum(sc[k][0] for k in ("qkv", "o_proj", "gate_up", "down"))
+    assert linear == 2.0 * T * dims.params_per_layer
+    assert sc["attention"][0] == 4.0 * dims.n_q * dims.d_head * float(np.sum(np.asarray(p.row_pos) + 1))
+
+
+def test_e4m3_weight_bytes_and_roofline(plan):
+    dims, p = plan
+    s2 = costs.stage_costs(dims, p.row_pos, p.seq_q_start, p.seq_kv_len)
+    s1 = costs.stage_costs(dims, p.row_pos, p.seq_q_start, p.seq_kv_len, weight_bytes=1)
+    b2 = sum(v[1] for v in s2.values())
+    b1 = sum(v[1] for v in s1.values())
+    assert b2 - b1 == dims.params_per_layer  # one byte less per weight
+    # math-bound (infinite bandwidth): the projections take half as long with FP8
+    tf = 1000.0
+    t16 = costs.roofline_time(s2, tf, 1e30, f8=False)
+    t8 = costs.roofline_time(s1, tf, 1e30, f8=True)
+    proj = sum(s2[k][0] for k in ("qkv", "o_proj", "gate_up", "down")) / (tf * 1e12)
+    assert t16 - t8 == pytest.approx(proj / 2, rel=1e-12)
+    # memory-bound (infinite FLOP rate): bytes over bandwidth
+    assert costs.roofline_time(s1, 1e30, 1000.0, f8=True) == pytest.approx(b1 / 1e12, rel=1e-12)
