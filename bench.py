@@ -96,8 +96,9 @@ def make_workload(tau: int, n_dec: int):
 
 
 class PlanRunner:
-    """Per-step planning through the C ABI into pinned staging buffers and one
-    host-to-device copy of the kernel-facing plan arrays."""
+    """Per-step planning through the C ABI into pinned staging buffers, and
+    one host-to-device copy per step of the kernel-facing plan arrays on a
+    copy stream of its own, so the upload overlaps the previous step."""
 
     def __init__(self, lib, st, tau, chunk, device):
         import torch
@@ -127,17 +128,26 @@ class PlanRunner:
         self.host_only = {k: np.zeros(n, np.int32) for k, n in
                           (("row_seq", rc), ("seq_pos0", sc), ("seq_kind", sc), ("seq_req", sc),
                            ("pf_take", max(self.n_pf, 1)), ("pf_finished", max(self.n_pf, 1)))}
+        # two pinned staging buffers and two device copies: step k's plan is
+        # uploaded on a copy stream into dev[k % 2] while step k - 1 computes
         self.pinned = [torch.zeros(self.dev_ints, dtype=torch.int32).pin_memory() for _ in range(2)]
+        self.dev = [torch.zeros(self.dev_ints, dtype=torch.int32, device=device) for _ in range(2)]
         self.copied = [torch.cuda.Event(), torch.cuda.Event()]
-        self.dev = torch.zeros(self.dev_ints, dtype=torch.int32, device=device)
+        self.released = [torch.cuda.Event(), torch.cuda.Event()]
+        self.copy_stream = torch.cuda.Stream(device=device)
         self.k = 0
         self.h2d_bytes = 0
 
     def step(self, stream):
-        """Plan the iteration on the host and enqueue its upload on `stream`.
-        Returns the hb_device_plan struct."""
+        """Plan the iteration on the host, upload it on the copy stream and
+        make `stream` wait for the upload.  Returns the hb_device_plan struct.
+        The caller enqueues one layer forward on `stream` between two calls:
+        that layer is the last reader of its device plan."""
+        import torch
         L = self.L
         b = self.k & 1
+        if self.k >= 1:
+            self.released[b ^ 1].record(stream)  # end of the previous step's layer
         self.copied[b].synchronize()  # the copy that last read this staging buffer is done
         stage = self.pinned[b].numpy()
         for i in range(self.n_dec):
@@ -159,14 +169,17 @@ class PlanRunner:
                                     C.byref(P))
         if st != 0:
             raise RuntimeError(f"hb_plan_batch failed: {self.lib.hb_last_error().decode()}")
-        import torch
-        with torch.cuda.stream(stream):
-            self.dev.copy_(self.pinned[b], non_blocking=True)
-            self.copied[b].record(stream)
+        cs = self.copy_stream
+        if self.k >= 2:
+            cs.wait_event(self.released[b])  # the layer of step k - 2 has read dev[b]
+        with torch.cuda.stream(cs):
+            self.dev[b].copy_(self.pinned[b], non_blocking=True)
+        self.copied[b].record(cs)
+        stream.wait_event(self.copied[b])
         self.h2d_bytes = self.dev_ints * 4
         self.k += 1
         self.n_rows, self.n_seqs = P.n_rows, P.n_seqs
-        d = self.dev.data_ptr()
+        d = self.dev[b].data_ptr()
         return L.hb_device_plan(P.n_rows, P.n_seqs, self.max_pages, *[d + 4 * int(self.off[i]) for i in range(5)],
                                 P.decode_pairs, P.chunk_pairs, P.chunk_rows)
 
