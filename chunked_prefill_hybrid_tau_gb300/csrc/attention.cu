@@ -383,8 +383,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
     if (!last) continue;
     __threadfence();
     // combine the splits of this (row, kv head) in split order: lane r < grp
-    // finds row r's max and sum over splits, then each lane owns 4 columns of
-    // every row and issues all its split loads before accumulating
+    // finds row r's max and sum over splits; then each lane owns 4 columns
+    // of up to four rows at a time and issues the split loads of all of
+    // them before accumulating (one round trip to L2 per group of four
+    // rows, not one per row: this combine ends the kernel's longest units)
     const float* rec0 = p.partials + static_cast<size_t>(u - split * p.n_kv) * REC_FLOATS;
     const size_t rstride = static_cast<size_t>(p.n_kv) * REC_FLOATS;
     float Mr = -INFINITY, Lr = 0.f;
@@ -397,24 +399,42 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
         Lr += __ldcg(rs + 16 * D + 16 + lane) * exp2f(__ldcg(rs + 16 * D + lane) - Mr);
       }
     }
-    for (int r = 0; r < p.grp; ++r) {
-      const float M = __shfl_sync(0xffffffffu, Mr, r);
-      const float L = __shfl_sync(0xffffffffu, Lr, r);
-      const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int r0 = 0; r0 < p.grp; r0 += 4) {
+      const int nr = min(4, p.grp - r0);
+      float M[4], inv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        M[i] = __shfl_sync(0xffffffffu, Mr, r0 + i);  // r0 + i < 16: rows past grp are never used
+        const float L = __shfl_sync(0xffffffffu, Lr, r0 + i);
+        inv[i] = L > 0.f ? 1.f / L : 0.f;
+      }
       for (int c4 = lane; c4 < D / 4; c4 += 32) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 acc[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
         for (int sp = 0; sp < nsplit; ++sp) {
           const float* rs = rec0 + sp * rstride;
-          const float wgt = exp2f(__ldcg(rs + 16 * D + r) - M);
-          const float4 ov = __ldcg(reinterpret_cast<const float4*>(rs + r * D) + c4);
-          acc.x += wgt * ov.x;
-          acc.y += wgt * ov.y;
-          acc.z += wgt * ov.z;
-          acc.w += wgt * ov.w;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (i < nr) {
+              const int r = r0 + i;
+              const float wgt = exp2f(__ldcg(rs + 16 * D + r) - M[i]);
+              const float4 ov = __ldcg(reinterpret_cast<const float4*>(rs + r * D) + c4);
+              acc[i].x += wgt * ov.x;
+              acc[i].y += wgt * ov.y;
+              acc[i].z += wgt * ov.z;
+              acc[i].w += wgt * ov.w;
+            }
+          }
         }
-        *reinterpret_cast<uint2*>(orow + r * D + 4 * c4) =
-            make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (i < nr)
+            *reinterpret_cast<uint2*>(orow + (r0 + i) * D + 4 * c4) =
+                make_uint2(pack_bf16x2(acc[i].x * inv[i], acc[i].y * inv[i]),
+                           pack_bf16x2(acc[i].z * inv[i], acc[i].w * inv[i]));
+        }
       }
     }
   }
