@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "runtime.h"
@@ -16,11 +17,14 @@ namespace hb {
 
 namespace {
 constexpr int kMaxDevices = 64;
-int* g_status_ptr[kMaxDevices];
+// Per-device state, filled once under g_mu.  The status pointer is published
+// last with release order: a thread that reads it non-null (acquire) also
+// sees that device's SM count and compute capability.
+std::atomic<int*> g_status_ptr[kMaxDevices];
 int g_num_sms[kMaxDevices];
 int g_cc[kMaxDevices];
 std::mutex g_mu;
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::atomic<PFN_cuTensorMapEncodeTiled_v12000> g_encode{nullptr};
 }  // namespace
 
 hb_status cuda_status(cudaError_t e, const char* what) {
@@ -31,7 +35,7 @@ hb_status cuda_status(cudaError_t e, const char* what) {
 
 static hb_status init_device(int dev) {
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_status_ptr[dev] != nullptr) return HB_OK;
+  if (g_status_ptr[dev].load(std::memory_order_relaxed) != nullptr) return HB_OK;
   void* p = nullptr;
   hb_status st = cuda_status(cudaGetSymbolAddress(&p, g_hb_status_word), "cudaGetSymbolAddress(status word)");
   if (st != HB_OK) return st;
@@ -40,7 +44,7 @@ static hb_status init_device(int dev) {
   if (st != HB_OK) return st;
   g_num_sms[dev] = prop.multiProcessorCount;
   g_cc[dev] = prop.major * 10 + prop.minor;
-  g_status_ptr[dev] = static_cast<int*>(p);
+  g_status_ptr[dev].store(static_cast<int*>(p), std::memory_order_release);
   return HB_OK;
 }
 
@@ -52,9 +56,11 @@ hb_status device_context(DeviceCtx* ctx) {
     set_error("device ordinal %d out of range", dev);
     return HB_ERR_UNSUPPORTED;
   }
-  if (g_status_ptr[dev] == nullptr) {
+  int* status = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (status == nullptr) {
     st = init_device(dev);
     if (st != HB_OK) return st;
+    status = g_status_ptr[dev].load(std::memory_order_acquire);
   }
   if (g_cc[dev] != 103) {
     set_error("the library is built for sm_103a; device %d is sm_%d", dev, g_cc[dev]);
@@ -62,14 +68,14 @@ hb_status device_context(DeviceCtx* ctx) {
   }
   ctx->device = dev;
   ctx->num_sms = g_num_sms[dev];
-  ctx->status = g_status_ptr[dev];
+  ctx->status = status;
   return HB_OK;
 }
 
 static hb_status resolve_encode() {
-  if (g_encode != nullptr) return HB_OK;
+  if (g_encode.load(std::memory_order_acquire) != nullptr) return HB_OK;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_encode != nullptr) return HB_OK;
+  if (g_encode.load(std::memory_order_relaxed) != nullptr) return HB_OK;
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
   hb_status st =
@@ -80,7 +86,7 @@ static hb_status resolve_encode() {
     set_error("cuTensorMapEncodeTiled is not available from the driver");
     return HB_ERR_UNSUPPORTED;
   }
-  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  g_encode.store(reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn), std::memory_order_release);
   return HB_OK;
 }
 
@@ -94,7 +100,7 @@ hb_status encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uin
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = g_encode.load(std::memory_order_acquire)(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE,
                         swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -115,7 +121,7 @@ hb_status encode_tmap_q3d(CUtensorMap* map, const void* q, int T, int n_q, int d
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d_head) * 2, static_cast<cuuint64_t>(n_q) * d_head * 2};
   cuuint32_t box[3] = {64, 1, 128};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+  CUresult res = g_encode.load(std::memory_order_acquire)(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (res != CUDA_SUCCESS) {
@@ -133,7 +139,7 @@ hb_status encode_tmap_kv_pages(CUtensorMap* map, const void* pool, uint64_t rows
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d_head) * 2, 128};
   cuuint32_t box[3] = {64, 16, halves};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
+  CUresult res = g_encode.load(std::memory_order_acquire)(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (res != CUDA_SUCCESS) {
