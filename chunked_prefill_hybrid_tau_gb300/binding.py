@@ -66,6 +66,10 @@ def hb_check_status(stream=None):
     _check(lib().hb_check_status(_stream(stream)), "hb_check_status")
 
 
+def hb_selftest_wait_timeout(timeout_us: int, stream=None):
+    _check(lib().hb_selftest_wait_timeout(int(timeout_us), _stream(stream)), "hb_selftest_wait_timeout")
+
+
 # ---------------------------------------------------------------- planner
 @dataclasses.dataclass
 class HostPlan:

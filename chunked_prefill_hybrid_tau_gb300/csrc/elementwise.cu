@@ -348,3 +348,31 @@ extern "C" hb_status hb_fold_gamma(const void* w, const void* gamma, void* out, 
       static_cast<const uint4*>(w), static_cast<const uint4*>(gamma), static_cast<uint4*>(out), total, cols / 8);
   return hb::launch_status("fold_gamma_kernel launch");
 }
+
+namespace hb {
+namespace {
+// One thread waits on a barrier that nothing ever completes: the bounded
+// wait gives up after timeout_ns and records a timeout in the status word,
+// the path every kernel takes when a copy or a partner never arrives.
+__global__ void wait_selftest_kernel(int* status, unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, nullptr, status, timeout_ns);
+}
+}  // namespace
+}  // namespace hb
+
+extern "C" hb_status hb_selftest_wait_timeout(int32_t timeout_us, void* stream) {
+  hb::clear_error();
+  HB_REQUIRE(timeout_us >= 1 && timeout_us <= 1000000, "hb_selftest_wait_timeout: timeout_us in [1, 1000000]");
+  hb::DeviceCtx ctx;
+  hb_status st = hb::device_context(&ctx);
+  if (st != HB_OK) return st;
+  hb::wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      ctx.status, static_cast<unsigned long long>(timeout_us) * 1000ull);
+  return hb::launch_status("wait_selftest_kernel launch");
+}

@@ -447,6 +447,19 @@ hb_status hb_check_status(void* stream);
 /* Number of SMs of the current device and whether it is sm_103 (1/0). */
 hb_status hb_device_info(int32_t* num_sms, int32_t* is_sm103);
 
+/* ------------------------------------------------------------------------
+ * hb_selftest_wait_timeout - exercise the failure path of the bounded
+ * device waits without faulting the GPU.  The pages define no such
+ * operation: it checks this library's own error reporting.  One thread of
+ * one CTA waits on a shared-memory barrier that nothing completes; after
+ * timeout_us microseconds (1 .. 1 000 000) the wait gives up, records a
+ * timeout in the device status word and the kernel returns.  The next
+ * hb_check_status on `stream` returns HB_ERR_TIMEOUT and clears the word;
+ * the context stays usable.  Argument errors return HB_ERR_INVALID_ARG
+ * before any device work.
+ * ---------------------------------------------------------------------- */
+hb_status hb_selftest_wait_timeout(int32_t timeout_us, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -49,6 +49,9 @@ def test_argument_errors_are_synchronous(lib):
     bad = L.hb_layer_dims(256, 4, 3, 64, 688, 16, 1e-6, 1e4)  # n_q % n_kv != 0
     st = lib.hb_kv_append(None, 0, None, None, None, 1, C.byref(bad), None, None, None, 1, None)
     assert st == L.HB_ERR_INVALID_ARG
+    # the wait self-test checks its limit before touching a device
+    assert lib.hb_selftest_wait_timeout(0, None) == L.HB_ERR_INVALID_ARG
+    assert lib.hb_selftest_wait_timeout(1000001, None) == L.HB_ERR_INVALID_ARG
     with pytest.raises(B.HBError):
         B._check(L.HB_ERR_INVALID_ARG, "x")
 
