@@ -468,6 +468,66 @@ def test_zero_projections_identity():
 
 
 # ----------------------------------------------------------------------------
+# paged K/V store and the LM head
+# ----------------------------------------------------------------------------
+def pin_paged_store(mod=ol):
+    """Tokens written through a scattered block table come back in order,
+    bit for bit, and no other slot changes (16-token pages; the page and
+    offset of a slot are slot // 16 and slot % 16)."""
+    rng = np.random.default_rng(21)
+    page, n_pages, n_kv, d = 16, 40, 2, 8
+    k_pool = rng.standard_normal((n_pages, n_kv, page, d)).astype(np.float32)
+    v_pool = rng.standard_normal((n_pages, n_kv, page, d)).astype(np.float32)
+    k0, v0 = k_pool.copy(), v_pool.copy()
+    for n in (1, 15, 16, 17, 100):
+        table = rng.permutation(n_pages)[: (n + page - 1) // page]
+        slots = np.array([table[t // page] * page + t % page for t in range(n)])
+        k = rng.standard_normal((n, n_kv, d)).astype(np.float32)
+        v = rng.standard_normal((n, n_kv, d)).astype(np.float32)
+        kp, vp = k0.copy(), v0.copy()
+        mod.kv_append(k, v, slots, kp, vp, page)
+        assert np.array_equal(mod.gather_keys(kp, table, n, page), k)
+        assert np.array_equal(mod.gather_keys(vp, table, n, page), v)
+        touched = np.zeros(n_pages * page, bool)
+        touched[slots] = True
+        flat = lambda pool: pool.transpose(0, 2, 1, 3).reshape(n_pages * page, n_kv, d)
+        assert np.array_equal(flat(kp)[~touched], flat(k0)[~touched])
+        assert np.array_equal(flat(vp)[~touched], flat(v0)[~touched])
+
+
+def pin_lm_head(mod=ol):
+    """Closed forms of the final norm + untied head.  A one-hot row a e_j has
+    mean square a^2/d, so its logits are a / sqrt(a^2/d + eps) g_j W[:, j];
+    with W = I the head returns the normalised rows."""
+    rng = np.random.default_rng(22)
+    d, vocab, eps = 16, 24, 1e-6
+    g = (1 + 0.1 * rng.standard_normal(d)).astype(np.float64)
+    w = rng.standard_normal((vocab, d)).astype(np.float64)
+    for j, a in [(0, 3.0), (5, -0.5), (15, 1e-2)]:
+        x = np.zeros((1, d))
+        x[0, j] = a
+        got = mod.lm_head(x, g, w, eps, dtype=np.float64)
+        exp = a / math.sqrt(a * a / d + eps) * g[j] * w[:, j]
+        assert np.allclose(got[0], exp, rtol=1e-12, atol=0)
+    x = rng.standard_normal((5, d))
+    sq = rng.standard_normal((d, d))
+    assert np.allclose(mod.lm_head(x, g, np.eye(d), eps, dtype=np.float64),
+                       mod.rmsnorm(x, g, eps, dtype=np.float64), rtol=1e-13, atol=0)
+    # a square, non-symmetric head tells W from its transpose
+    exp = mod.rmsnorm(x, g, eps, dtype=np.float64) @ sq.T
+    assert np.allclose(mod.lm_head(x, g, sq, eps, dtype=np.float64), exp, rtol=1e-12, atol=1e-12)
+    assert not np.allclose(exp, mod.rmsnorm(x, g, eps, dtype=np.float64) @ sq, rtol=1e-3)
+
+
+def test_paged_store():
+    pin_paged_store()
+
+
+def test_lm_head():
+    pin_lm_head()
+
+
+# ----------------------------------------------------------------------------
 # planted mistakes: each pin must fail on a plausible wrong oracle
 # ----------------------------------------------------------------------------
 _ORIG_ATTENTION = ol.attention
@@ -515,7 +575,20 @@ def _rms_eps_outside(x, g, eps, dtype=np.float32):
     return x / (np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + eps) * np.asarray(g, dtype)
 
 
+def _gather_off_by_one(pool, table_row, n_keys, page):
+    j = np.arange(n_keys)
+    return pool[np.asarray(table_row)[j // page], :, (j + 1) % page, :]
+
+
+def _lm_head_transposed(x_rows, g_f, w_lm, eps, dtype=np.float32):
+    """The head applied as W instead of W^T wherever the shapes allow it."""
+    w = np.asarray(w_lm, dtype)
+    return ol.rmsnorm(x_rows, g_f, eps, dtype) @ (w if w.shape[0] == w.shape[1] else w.T)
+
+
 @pytest.mark.parametrize("pin,name,mutant", [
+    (pin_paged_store, "gather_keys", _gather_off_by_one),
+    (pin_lm_head, "lm_head", _lm_head_transposed),
     (pin_attention_dense, "attention", _attn_gqa_modulo),
     (pin_attention_dense, "attention", _attn_excludes_self),
     (pin_attention_dense, "attention", _attn_noncausal_chunk),
