@@ -116,23 +116,23 @@ __device__ __forceinline__ float row_inv_rms(const GemmNorm& nm, int row) {
 template <int EPI>
 __device__ __forceinline__ void store_chunk(const Params& p, int row, int col, const uint32_t (&r)[32], float scale) {
   const int ncols = p.out_cols;
-  if (EPI == HB_EPI_F32) {
+  if constexpr (EPI == HB_EPI_F32) {
     float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.C) + static_cast<size_t>(row) * p.ldc + col);
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       if (col + 4 * i < ncols)
         dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
                              __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
-    return;
+  } else {
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * scale, __uint_as_float(r[2 * i + 1]) * scale);
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) + static_cast<size_t>(row) * p.ldc + col);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (col + 8 * i < ncols) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
   }
-  uint32_t w[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i)
-    w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * scale, __uint_as_float(r[2 * i + 1]) * scale);
-  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) + static_cast<size_t>(row) * p.ldc + col);
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    if (col + 8 * i < ncols) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
 }
 
 // RESIDUAL: C = R + acc for 32 columns, with the residual already loaded
