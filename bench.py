@@ -208,6 +208,8 @@ class ClockSampler:
 
     def stop(self):
         if self.p is None:
+            self.f.close()
+            os.unlink(self.f.name)
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.p.terminate()
         try:
@@ -230,6 +232,7 @@ class ClockSampler:
             for n, v in zip(names, parts[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
+        self.f.close()
         os.unlink(self.f.name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
