@@ -26,7 +26,10 @@ import oracle.layer as ol  # noqa: E402
 
 
 def test_expired_wait_is_reported_and_the_context_stays_usable():
-    hb.hb_check_status()  # start from a clean status word
+    try:
+        hb.hb_check_status()  # start from a clean status word, whatever an earlier test left
+    except hb.HBError:
+        pass
     for timeout_us in (2000, 20000):
         t0 = time.perf_counter()
         hb.hb_selftest_wait_timeout(timeout_us)
