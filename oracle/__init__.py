@@ -28,8 +28,13 @@ Parity status per function (what pins it, in tests/test_oracle_pins.py):
   layer.rope             identity at position 0, pair-norm preservation,
                          relative-position property
   layer.silu             logistic-function identity (scipy.special.expit)
-  layer.layer_forward    chunked == unchunked; decode batch independence;
-                         identity when the output projections are zero
+  layer.layer_forward    closed forms of a hand-wired layer (single routes
+                         through each projection: q/k/v order and head
+                         layout, GQA groups, W_o orientation, residual
+                         sources, the gains of the two norms, gate versus
+                         up); chunked == unchunked; decode batch
+                         independence; identity when the output
+                         projections are zero
   costs.*                chunked-attention pair-count identity (section
                          7.5b); closed form of I and c* against counters
   sched.SchedLoop        closed form of one request's iterations; token and
@@ -41,6 +46,7 @@ Parity status per function (what pins it, in tests/test_oracle_pins.py):
                          saturation; per-row scaling bounds and invariances;
                          the projection against exact rational sums; the
                          layer's QKV exact on representable inputs, chunked
-                         == unchunked, and within E4M3's error of the bf16
-                         layer
+                         == unchunked, within E4M3's error of the bf16
+                         layer, and within E4M3's error of the hand-wired
+                         layer's closed forms
 """

@@ -198,8 +198,33 @@ def pin_layer_chunk_invariant(m=of):
         np.testing.assert_allclose(run(c), one, rtol=1e-5, atol=1e-6)
 
 
+def pin_layer_assembly(m=of):
+    """The FP8 layer's wiring against the closed forms of the hand-wired
+    layer in test_oracle_pins (single routes through each projection).  Its
+    weights and the +-1 inputs are exact in E4M3; the per-token codes of o
+    and h carry up to half an E4M3 step (2^-4 relative) each, so the layer's
+    contribution may move by a few percent, while a swapped gate/up or a
+    residual taken from x moves it by 20% or more."""
+    import test_oracle_pins as tp
+    dims, st, p, x, w, c = tp.assembly_case()
+    w = dict(w, g1=ol.round_bf16(w["g1"]), g2=ol.round_bf16(w["g2"]))
+    exp, k_new, v_new = tp.assembly_expected(dims, st, p, x, w, c)
+    cos, sin = ol.rope_tables(64, dims.d_head, dims.theta)
+    k_pool, v_pool = st.k_pool.astype(np.float64), st.v_pool.astype(np.float64)
+    got = m.layer_forward(m.prepare_weights(w), dims, p, x, k_pool, v_pool, cos, sin, dtype=np.float64)
+    contrib = exp - x
+    assert np.linalg.norm(got - exp) <= 0.06 * np.linalg.norm(contrib)
+    assert np.max(np.abs(got - exp)[:, c["m"]]) <= 0.1 * np.max(np.abs(contrib[:, c["m"]]))
+    # K and V come from exact codes of x: rotated K and V land exactly
+    page = dims.page
+    for r, sl in enumerate(p.slot_mapping):
+        np.testing.assert_allclose(k_pool[sl // page, :, sl % page, :], k_new[r], rtol=1e-6, atol=1e-7)
+        np.testing.assert_allclose(v_pool[sl // page, :, sl % page, :], v_new[r], rtol=1e-6, atol=1e-7)
+
+
 PINS = [pin_table, pin_round_against_library, pin_saturation, pin_quantize_rows, pin_gemm_exact,
-        pin_layer_near_bf16_layer, pin_layer_qkv_exact_when_representable, pin_layer_chunk_invariant]
+        pin_layer_near_bf16_layer, pin_layer_qkv_exact_when_representable, pin_layer_chunk_invariant,
+        pin_layer_assembly]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -253,12 +278,51 @@ def _table_no_subnormals():
     return t
 
 
+def _fp8_layer_variant(mutation):
+    """The FP8 oracle's layer with one wiring mistake (names resolve in the
+    mutated module, like the oracle's own functions)."""
+    def layer_forward(wq, dims, plan, x, k_pool, v_pool, cos, sin, storage=None, dtype=np.float32,
+                      return_parts=False):
+        T = len(plan.row_seq)
+        nq, nkv, dh = dims.n_q, dims.n_kv, dims.d_head
+
+        def inv_rms(v):
+            v = np.asarray(v, dtype)
+            return 1.0 / np.sqrt(np.mean(v * v, axis=-1) + dtype(dims.eps))
+
+        def proj(v, name):
+            qa, sa = of.quantize_rows(v)
+            qb, sb = wq[name]
+            return of.gemm(qa, sa, qb, sb).astype(dtype)
+
+        x = np.asarray(x, dtype)
+        qkv = inv_rms(x)[:, None] * proj(x, "qkv")
+        q = qkv[:, :nq * dh].reshape(T, nq, dh)
+        k = qkv[:, nq * dh:(nq + nkv) * dh].reshape(T, nkv, dh)
+        v = qkv[:, (nq + nkv) * dh:].reshape(T, nkv, dh)
+        pos = np.asarray(plan.row_pos)
+        q, k = ol.rope(q, pos, cos, sin, dtype), ol.rope(k, pos, cos, sin, dtype)
+        ol.kv_append(k, v, plan.slot_mapping, k_pool, v_pool, dims.page)
+        o = ol.attention(q, k_pool, v_pool, plan, nq, nkv, dims.page, dtype)
+        h = x + proj(o.reshape(T, nq * dh), "o")
+        r = inv_rms(h)[:, None]
+        gate, up = r * proj(h, "g"), r * proj(h, "u")
+        if mutation == "gate and up swapped":
+            gate, up = up, gate
+        a = ol.silu(gate) * up
+        out = (x if mutation == "final residual from x" else h) + proj(a, "d")
+        return (out, dict(qkv=qkv, o=o, h=h, a=a)) if return_parts else out
+    return layer_forward
+
+
 MUTATIONS = {
     "truncating round": dict(e4m3_round=_round_truncating),
     "round half up": dict(e4m3_round=_round_half_up),
     "per-tensor scale": dict(quantize_rows=_quant_per_tensor),
     "dropped weight scale": dict(gemm=_gemm_dropped_scale),
     "subnormals decoded as normals": dict(e4m3_table=_table_no_subnormals),
+    "layer: gate and up swapped": dict(layer_forward=_fp8_layer_variant("gate and up swapped")),
+    "layer: final residual from x": dict(layer_forward=_fp8_layer_variant("final residual from x")),
 }
 
 

@@ -468,6 +468,128 @@ def test_zero_projections_identity():
 
 
 # ----------------------------------------------------------------------------
+# the layer's assembly: which projection feeds which, in closed form
+# ----------------------------------------------------------------------------
+def assembly_case():
+    """A hand-wired layer whose output and KV writes have closed forms.
+
+    Tiny shapes (d 32, 4 q / 2 kv heads of 8 dims, d_ff 48); two decodes with
+    contexts 1 and 3 over random cached K/V, plus the first 3 tokens of a
+    fresh prompt.  Inputs are +-1, so every row of x has mean square 1.  The
+    weights are zero except for single routes:
+      * q head 3, dim 0     <- cq * xn[:, jq]      (the only non-zero query)
+      * k head 0, dim 1     <- xn[:, jk]
+      * v head 1, dim 2     <- xn[:, jv]
+      * W_o a non-symmetric permutation (h[:, i] = x[:, i] + o[:, pi(i)])
+      * gate row i0 <- alpha * hn[:, jg], up row i0 <- beta * hn[:, ju],
+        down column i0 -> output column m with weight delta.
+    The rows of W_qkv are ordered q heads, k heads, v heads, each head's
+    d_head rows contiguous (the layout the weights are generated in)."""
+    dims = tiny_dims()
+    d, dh, nq, nkv, f = dims.d_model, dims.d_head, dims.n_q, dims.n_kv, dims.d_ff
+    rng = np.random.default_rng(31)
+    st = tiny_state(rng, dims, [1, 3], [(3, 0)], slack=8)
+    p = plan_from_state(st, 8, 8)
+    x = rng.choice([-1.0, 1.0], (p.n_rows, d)).astype(np.float32)
+    g1 = (1 + 0.25 * rng.standard_normal(d)).astype(np.float32)
+    g2 = (1 + 0.25 * rng.standard_normal(d)).astype(np.float32)
+    c = dict(cq=2.0, jq=3, jk=11, jv=17, alpha=1.5, beta=-0.75, delta=2.0, jg=5, ju=23, i0=7, m=29, shift=5)
+    w = dict(w_qkv=np.zeros((dims.qkv_cols, d), np.float32), w_o=np.zeros((d, nq * dh), np.float32),
+             w_g=np.zeros((f, d), np.float32), w_u=np.zeros((f, d), np.float32),
+             w_d=np.zeros((d, f), np.float32), g1=g1, g2=g2)
+    w["w_qkv"][3 * dh + 0, c["jq"]] = c["cq"]
+    w["w_qkv"][nq * dh + 0 * dh + 1, c["jk"]] = 1.0
+    w["w_qkv"][(nq + nkv) * dh + 1 * dh + 2, c["jv"]] = 1.0
+    for i in range(d):
+        w["w_o"][i, (i + c["shift"]) % d] = 1.0
+    w["w_g"][c["i0"], c["jg"]] = c["alpha"]
+    w["w_u"][c["i0"], c["ju"]] = c["beta"]
+    w["w_d"][c["m"], c["i0"]] = c["delta"]
+    return dims, st, p, x, w, c
+
+
+def assembly_expected(dims, st, p, x, w, c):
+    """Closed forms of assembly_case, in float64, by scalar reasoning on the
+    routes: the RMSNorm of a +-1 row is x g / sqrt(1 + eps); RoPE moves a
+    lone component at dim e < d_head/2 to (e, e + d_head/2) with factors
+    cos(pos theta^(-2e/d_head)), sin(...) (float64, held in float32); a zero query weights its keys
+    uniformly; the only scored head is q head 3 over kv head 1."""
+    dh, half, nq, nkv, eps = dims.d_head, dims.d_head // 2, dims.n_q, dims.n_kv, dims.eps
+    T, d = x.shape
+    x = x.astype(np.float64)
+    xn = x / math.sqrt(1.0 + eps) * w["g1"].astype(np.float64)
+    ang = lambda pos, e: pos * dims.theta ** (-2.0 * e / dh)
+    # the rotation factors are computed in float64 and held in float32
+    cosf = lambda a: np.cos(a).astype(np.float32).astype(np.float64)
+    sinf = lambda a: np.sin(a).astype(np.float32).astype(np.float64)
+    pos = np.asarray(p.row_pos)
+    # new K/V rows of this iteration (rotated K), each [n_kv, d_head]
+    k_new = np.zeros((T, nkv, dh))
+    v_new = np.zeros((T, nkv, dh))
+    k_new[:, 0, 1] = xn[:, c["jk"]] * cosf(ang(pos, 1))
+    k_new[:, 0, 1 + half] = xn[:, c["jk"]] * sinf(ang(pos, 1))
+    v_new[:, 1, 2] = xn[:, c["jv"]]
+    q3 = np.zeros((T, dh))
+    q3[:, 0] = c["cq"] * xn[:, c["jq"]] * cosf(ang(pos, 0))
+    q3[:, half] = c["cq"] * xn[:, c["jq"]] * sinf(ang(pos, 0))
+    o = np.zeros((T, nq, dh))
+    for s in range(len(p.seq_pos0)):
+        rows = list(range(p.seq_q_start[s], p.seq_q_start[s + 1]))
+        n_cached = p.seq_pos0[s]
+        Kc = ol.gather_keys(st.k_pool, p.block_table[s], n_cached, dims.page).astype(np.float64)
+        Vc = ol.gather_keys(st.v_pool, p.block_table[s], n_cached, dims.page).astype(np.float64)
+        Ks = np.concatenate([Kc, k_new[rows]])
+        Vs = np.concatenate([Vc, v_new[rows]])
+        for r in rows:
+            n = pos[r] + 1
+            for hq in range(nq):
+                g = hq * nkv // nq
+                if hq == 3:
+                    sc = Ks[:n, g, :] @ q3[r] / math.sqrt(dh)
+                    wts = np.exp(sc - sc.max())
+                    wts /= wts.sum()
+                else:
+                    wts = np.full(n, 1.0 / n)
+                o[r, hq] = wts @ Vs[:n, g, :]
+    of_ = o.reshape(T, nq * dh)
+    h = x + of_[:, (np.arange(d) + c["shift"]) % d]
+    hn = h / np.sqrt(np.mean(h * h, axis=1, keepdims=True) + eps) * w["g2"].astype(np.float64)
+    gate = c["alpha"] * hn[:, c["jg"]]
+    up = c["beta"] * hn[:, c["ju"]]
+    out = h.copy()
+    out[:, c["m"]] += c["delta"] * gate * scipy_expit(gate) * up
+    return out, k_new, v_new
+
+
+def scipy_expit(z):
+    from scipy.special import expit
+    return expit(z)
+
+
+def pin_layer_assembly(layer=ol):
+    """The layer's wiring against closed forms: q/k/v column order and head
+    layout, GQA groups, RoPE placement, the new token among a decode's keys,
+    causal chunk rows, W_o orientation, residual sources, which gain feeds
+    which norm, and gate versus up in the SwiGLU."""
+    dims, st, p, x, w, c = assembly_case()
+    cos, sin = layer.rope_tables(64, dims.d_head, dims.theta)
+    k_pool, v_pool = st.k_pool.astype(np.float64), st.v_pool.astype(np.float64)
+    got = layer.layer_forward(w, dims, p, x, k_pool, v_pool, cos, sin, np.float64)
+    exp, k_new, v_new = assembly_expected(dims, st, p, x, w, c)
+    np.testing.assert_allclose(got, exp, rtol=1e-12, atol=1e-12)
+    # the decode rows see cached values, so the attention term is non-zero
+    assert np.max(np.abs(exp - x)[: 2]) > 0.1
+    page = dims.page
+    for r, sl in enumerate(p.slot_mapping):
+        np.testing.assert_allclose(k_pool[sl // page, :, sl % page, :], k_new[r], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(v_pool[sl // page, :, sl % page, :], v_new[r], rtol=1e-12, atol=1e-12)
+
+
+def test_layer_assembly_closed_form():
+    pin_layer_assembly()
+
+
+# ----------------------------------------------------------------------------
 # paged K/V store and the LM head
 # ----------------------------------------------------------------------------
 def pin_paged_store(mod=ol):
@@ -600,6 +722,55 @@ def test_planted_mistakes_fail(monkeypatch, pin, name, mutant):
     monkeypatch.setattr(ol, name, mutant)
     with pytest.raises(AssertionError):
         pin()
+
+
+def _layer_variant(mutation):
+    """The oracle's layer assembly with one plausible wiring mistake."""
+    def forward(w, dims, plan, x, k_pool, v_pool, cos, sin, dtype=np.float32, return_parts=False, storage=None):
+        T = len(plan.row_seq)
+        nq, nkv, dh = dims.n_q, dims.n_kv, dims.d_head
+        x = np.asarray(x, dtype)
+        xn = ol.rmsnorm(x, w["g1"], dims.eps, dtype)
+        qkv = xn @ np.asarray(w["w_qkv"], dtype).T
+        a0, a1 = nq * dh, (nq + nkv) * dh
+        if mutation == "qkv order q, v, k":
+            q, v, k = qkv[:, :a0], qkv[:, a0:a1], qkv[:, a1:]
+        else:
+            q, k, v = qkv[:, :a0], qkv[:, a0:a1], qkv[:, a1:]
+        if mutation == "q heads interleaved by dim":
+            q = q.reshape(T, dh, nq).transpose(0, 2, 1)
+        q, k, v = q.reshape(T, nq, dh), k.reshape(T, nkv, dh), v.reshape(T, nkv, dh)
+        pos = np.asarray(plan.row_pos)
+        q, k = ol.rope(q, pos, cos, sin, dtype), ol.rope(k, pos, cos, sin, dtype)
+        ol.kv_append(k, v, plan.slot_mapping, k_pool, v_pool, dims.page)
+        o = ol.attention(q, k_pool, v_pool, plan, nq, nkv, dims.page, dtype).reshape(T, nq * dh)
+        wo = np.asarray(w["w_o"], dtype)
+        h = x + (o @ wo if mutation == "W_o transposed" else o @ wo.T)
+        g2 = w["g1"] if mutation == "second norm with g1" else w["g2"]
+        hn = ol.rmsnorm(x if mutation == "MLP norm of x" else h, g2, dims.eps, dtype)
+        gate, up = hn @ np.asarray(w["w_g"], dtype).T, hn @ np.asarray(w["w_u"], dtype).T
+        if mutation == "gate and up swapped":
+            gate, up = up, gate
+        a = ol.silu(gate) * up
+        return (x if mutation == "final residual from x" else h) + a @ np.asarray(w["w_d"], dtype).T
+    return forward
+
+
+LAYER_MUTATIONS = ["gate and up swapped", "final residual from x", "qkv order q, v, k",
+                   "q heads interleaved by dim", "W_o transposed", "second norm with g1", "MLP norm of x"]
+
+
+def test_layer_variant_without_mutation_passes(monkeypatch):
+    # the mutants differ from the oracle only in their named mistake
+    monkeypatch.setattr(ol, "layer_forward", _layer_variant(None))
+    pin_layer_assembly()
+
+
+@pytest.mark.parametrize("mutation", LAYER_MUTATIONS)
+def test_planted_layer_wiring_mistake_fails(monkeypatch, mutation):
+    monkeypatch.setattr(ol, "layer_forward", _layer_variant(mutation))
+    with pytest.raises(AssertionError):
+        pin_layer_assembly()
 
 
 def test_planted_planner_mistake_fails():
