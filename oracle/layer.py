@@ -24,10 +24,14 @@ rounding; inputs are the bf16-representable values the GPU also sees.
 
 Precision variant (storage="bf16"): the same arithmetic in fp32 but with every
 tensor that a bf16 implementation stores rounded to bf16 (round to nearest
-even) where it is stored: xn, qkv, the rotated q and k, the softmax weights P
-fed to the P V product, o, h, hn, the SwiGLU output a and the layer output.
-It quantifies how far bf16 storage alone moves a result from the fp32 one
-(used to bound deep stacks); the default path never rounds.
+even) where it is stored: qkv, the rotated q and k, the softmax weights P
+fed to the P V product, o, h, the SwiGLU output a and the layer output.  The
+normalised rows xn and hn are never stored: each RMSNorm is applied as
+    RMSNorm(v; g) W^T = (v (W diag g)^T) / sqrt(mean(v^2) + eps),
+the algebraic identity of a per-row scale, with W diag g rounded once to
+bf16 (the prepared weights) and the 1/rms factor applied to the fp32 product.
+It quantifies how far bf16 storage alone moves a result from the fp32 one;
+the default path never rounds.
 """
 from __future__ import annotations
 
@@ -120,8 +124,20 @@ def layer_forward(w, dims, plan, x, k_pool, v_pool, cos, sin, dtype=np.float32,
     nq, nkv, dh = dims.n_q, dims.n_kv, dims.d_head
     st = round_bf16 if storage == "bf16" else (lambda t: t)
     x = np.asarray(x, dtype)
-    xn = st(rmsnorm(x, w["g1"], dims.eps, dtype))
-    qkv = st(xn @ np.asarray(w["w_qkv"], dtype).T)
+
+    def inv_rms(v):
+        return 1.0 / np.sqrt(np.mean(v * v, axis=-1, keepdims=True) + dtype(dims.eps))
+
+    def normed_proj(v, g, w_):
+        """RMSNorm(v; g) W^T: plainly in fp32; with bf16 storage the gain is
+        folded into W (rounded once) and 1/rms scales the product."""
+        if storage == "bf16":
+            wf = round_bf16(np.asarray(w_, np.float32) * np.asarray(g, np.float32)[None, :]).astype(dtype)
+            return (v @ wf.T) * inv_rms(v)
+        return rmsnorm(v, g, dims.eps, dtype) @ np.asarray(w_, dtype).T
+
+    xn = rmsnorm(x, w["g1"], dims.eps, dtype)
+    qkv = st(normed_proj(x, w["g1"], w["w_qkv"]))
     q = qkv[:, :nq * dh].reshape(T, nq, dh)
     k = qkv[:, nq * dh:(nq + nkv) * dh].reshape(T, nkv, dh)
     v = qkv[:, (nq + nkv) * dh:].reshape(T, nkv, dh)
@@ -132,8 +148,8 @@ def layer_forward(w, dims, plan, x, k_pool, v_pool, cos, sin, dtype=np.float32,
     o = st(attention(q, k_pool, v_pool, plan, nq, nkv, dims.page, dtype,
                      round_p=round_bf16 if storage == "bf16" else None))
     h = st(x + o.reshape(T, nq * dh) @ np.asarray(w["w_o"], dtype).T)
-    hn = st(rmsnorm(h, w["g2"], dims.eps, dtype))
-    a = st(silu(hn @ np.asarray(w["w_g"], dtype).T) * (hn @ np.asarray(w["w_u"], dtype).T))
+    hn = rmsnorm(h, w["g2"], dims.eps, dtype)
+    a = st(silu(normed_proj(h, w["g2"], w["w_g"])) * normed_proj(h, w["g2"], w["w_u"]))
     out = st(h + a @ np.asarray(w["w_d"], dtype).T)
     if return_parts:
         return out, dict(xn=xn, qkv=qkv, q=q, k=k, v=v, o=o, h=h, hn=hn, a=a)

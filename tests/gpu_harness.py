@@ -10,34 +10,45 @@ import workloads as wl
 from workloads import device as wd
 
 # Tolerance for bf16 activations and outputs (2e-2 max-abs, 1e-2 relative L2):
-#   kernel outputs (both sides fed the same bf16 inputs):
-#       |gpu - ref| <= 2e-2 + 2e-2 |ref| elementwise (a bf16 value v is itself
-#       rounded by up to 2^-8 |v|, so a purely absolute bound cannot hold for
-#       |v| >= 4), and relative L2 <= 1e-2;
-#   composite outputs (a layer against the fp32 oracle, which rounds nothing
-#   in between): relative L2 <= 1e-2 unchanged, and elementwise
-#       |gpu - ref| <= 2e-2 |ref| + 5e-2 rms(ref),
-#   because bf16 storage of h, hn, a, o and the output adds errors that scale
-#   with the activations, not with one element: the per-element error of the
-#   Mistral-shaped layer is about 0.4% of the rms (relative L2 0.0045) and its
-#   largest of 4-8 M elements reaches 3.3% of the rms (an exact emulation with
-#   bf16 storage reaches 2.4% at 2 M elements).
+#   kernel bound, for a kernel against the oracle fed the same bf16 inputs:
+#   |gpu - ref| <= 2e-2 + 2e-2 |ref| elementwise (a bf16 value v is itself
+#   rounded by up to 2^-9 |v|, and one ulp is 2^-8 |v|, so a purely absolute
+#   bound cannot hold for |v| >= 4) and relative L2 <= 1e-2;
+#   a layer's output against the oracle in fp32 (ref) and in its bf16-storage
+#   variant (emu, which rounds where the GPU stores: qkv, q, k, P, o, h, a and
+#   the output).  Two valid bf16 implementations do not round alike: the
+#   softmax weights P are rounded against a running maximum on the GPU and
+#   against the final one in the oracle, so about half of o's bf16 values
+#   differ by an ulp, and that noise reaches the output (measured on the
+#   Mistral-shaped layer: relative L2 3.2e-3 between GPU and emu, 3.3e-3
+#   between emu and fp32).  The bounds are therefore taken from the oracle's
+#   own rounding noise at the same inputs:
+#     relative L2 (gpu, ref) <= 1.5 x relative L2 (emu, ref), and <= 1e-2;
+#     relative L2 (gpu, emu) <= 1e-2;
+#     elementwise, against either: the kernel bound plus one bf16 ulp of the
+#     stored residual h (2^-7 |h|: out = h + mlp is formed from the stored h,
+#     and a one-ulp flip of h passes into out unchanged even where mlp nearly
+#     cancels it), or 1.5 x the largest |emu - ref|, whichever is larger.
 ATOL = 2e-2
 RTOL = 2e-2
 REL_L2 = 1e-2
 
 
-def assert_close(gpu, ref, what, atol=ATOL, rtol=RTOL, rel_l2=REL_L2, scale=None):
-    """scale=None: kernel bound; scale="rms": composite bound."""
+def assert_close(gpu, ref, what, atol=ATOL, rtol=RTOL, rel_l2=REL_L2, floor=None, extra=None):
+    """Kernel bound by default; `extra` adds an elementwise term (the h ulp
+    of a layer output); `floor` raises the elementwise bound to at least that
+    absolute value (the bf16-storage deviation of a layer)."""
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
     assert gpu.shape == ref.shape, (what, gpu.shape, ref.shape)
     assert np.all(np.isfinite(gpu)), f"{what}: non-finite GPU values"
     err = np.abs(gpu - ref)
     rms = float(np.sqrt(np.mean(ref * ref)))
-    if scale == "rms":
-        atol = 5e-2 * rms
     bound = atol + rtol * np.abs(ref)
+    if extra is not None:
+        bound = bound + np.asarray(extra, np.float64)
+    if floor is not None:
+        bound = np.maximum(bound, floor)
     denom = np.linalg.norm(ref)
     rl2 = float(np.linalg.norm(gpu - ref) / denom) if denom > 0 else 0.0
     worst = int(np.argmax(err - bound))
@@ -47,6 +58,28 @@ def assert_close(gpu, ref, what, atol=ATOL, rtol=RTOL, rel_l2=REL_L2, scale=None
                                   f"{int(np.sum(err > bound))} of {err.size} outside)")
     assert rl2 <= rel_l2, f"{what}: relative L2 {rl2:.4g} > {rel_l2}"
     return float(err.max())
+
+
+H_ULP = 2.0 ** -7  # one bf16 ulp relative to |h|, at most
+
+
+def rel_l2(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+def assert_layer(gpu, ref, emu, h, what):
+    """A layer's output against the oracle in fp32 (ref) and in its
+    bf16-storage variant (emu, with its stored residual h); bounds above."""
+    extra = H_ULP * np.abs(np.asarray(h, np.float64))
+    emax = float(np.max(np.abs(np.asarray(emu, np.float64) - np.asarray(ref, np.float64))))
+    e_rl2 = rel_l2(emu, ref)
+    g_rl2 = rel_l2(gpu, ref)
+    print(f"\n{what}: relL2 gpu/fp32 {g_rl2:.4g} emu/fp32 {e_rl2:.4g} gpu/emu {rel_l2(gpu, emu):.4g}; "
+          f"max abs gpu/fp32 {np.abs(np.asarray(gpu, np.float64) - ref).max():.4g} emu/fp32 {emax:.4g}")
+    assert g_rl2 <= 1.5 * e_rl2, f"{what}: relative L2 {g_rl2:.4g} beyond 1.5 x bf16 storage's {e_rl2:.4g}"
+    assert_close(gpu, emu, what + " (vs bf16-storage oracle)", extra=extra, floor=1.5 * emax)
+    return assert_close(gpu, ref, what + " (vs fp32 oracle)", extra=extra, floor=1.5 * emax)
 
 
 def plan_both(st: wl.State, tau: int, chunk: int, max_pages=None):
@@ -85,6 +118,11 @@ class GpuLayer:
         return wd.to_numpy(xout)
 
 
-def oracle_layer(w, dims, plan, x, k_pool, v_pool, max_pos):
+def oracle_layer_both(w, dims, plan, x, pools32, pools16, max_pos):
+    """The fp32 oracle and its bf16-storage variant on the same rows, each
+    appending to its own (K, V) pools in place -> (ref, emu, h of emu)."""
     cos, sin = ol.rope_tables(max_pos, dims.d_head, dims.theta)
-    return ol.layer_forward(w, dims, plan, x, k_pool, v_pool, cos, sin)
+    ref = ol.layer_forward(w, dims, plan, x, pools32[0], pools32[1], cos, sin)
+    emu, parts = ol.layer_forward(w, dims, plan, x, pools16[0], pools16[1], cos, sin, storage="bf16",
+                                  return_parts=True)
+    return ref, emu, parts["h"]

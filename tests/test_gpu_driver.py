@@ -15,7 +15,7 @@ import oracle.layer as ol
 import oracle.sched as osch
 import workloads as wl
 from workloads import device as wd
-from tests.gpu_harness import GpuLayer, assert_close
+from tests.gpu_harness import GpuLayer, assert_layer
 
 pytestmark = pytest.mark.gpu
 
@@ -43,6 +43,7 @@ def test_driver_stream_matches_oracle_every_iteration():
     k0 = np.zeros((n_pages, dims.n_kv, 16, dims.d_head), np.float32)
     gl = GpuLayer(w, dims, k0, k0.copy(), max_pos)
     k_ref, v_ref = k0.copy(), k0.copy()
+    k_emu, v_emu = k0.copy(), k0.copy()
     cos, sin = ol.rope_tables(max_pos, dims.d_head, dims.theta)
 
     drv = hb.Scheduler(tau, C, pool)
@@ -66,7 +67,8 @@ def test_driver_stream_matches_oracle_every_iteration():
             x = np.stack([x_of[r][p] for r, p in zip(row_req, hp.row_pos)])
             got = gl.forward(hp, x, int(hp.seq_kv_len.max()))
             ref = ol.layer_forward(w, dims, po, x, k_ref, v_ref, cos, sin)
-            assert_close(got, ref, f"iteration {it} ({hp.n_rows} rows)", scale="rms")
+            emu, parts = ol.layer_forward(w, dims, po, x, k_emu, v_emu, cos, sin, storage="bf16", return_parts=True)
+            assert_layer(got, ref, emu, parts["h"], f"iteration {it} ({hp.n_rows} rows)")
         before = [loop.reqs[i]["state"] for i in range(len(loop.reqs))]
         drv.commit()
         loop.commit()

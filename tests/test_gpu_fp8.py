@@ -150,6 +150,17 @@ def test_weight_preparation_codes_bit_exact():
         assert np.array_equal(getattr(lw, sname).cpu().numpy(), s), sname
 
 
+# The two sides quantize activations they computed independently, so a bf16
+# value within an ulp of an E4M3 code boundary can take the neighbouring code
+# (one step, 2^-3 relative) on one side; such flips move single outputs by a
+# few percent of the output's rms (see test_mistral_layer_e4m3_tau512).
+E4M3_FLIP_ATOL = 5e-2
+
+
+def rms(a):
+    return float(np.sqrt(np.mean(np.asarray(a, np.float64) ** 2)))
+
+
 def test_tiny_layer_e4m3_two_iterations():
     w = wl.tiny_layer(seed=0)
     st, dims = w.state, w.dims
@@ -163,7 +174,7 @@ def test_tiny_layer_e4m3_two_iterations():
     hp, o = plan_both(st, 128, 128)
     got = gl.forward(hp, w.x_prompt[:128], 512)
     ref = of.layer_forward(wq, dims, o, w.x_prompt[:128], k_ref, v_ref, cos, sin, storage="bf16")
-    assert_close(got, ref, "tiny e4m3 iteration A", scale="rms")
+    assert_close(got, ref, "tiny e4m3 iteration A", atol=E4M3_FLIP_ATOL * rms(ref))
     for i, r in enumerate(st.prefills):
         r.pages = list(hp.pf_pages[i])
         r.done += int(hp.pf_take[i])
@@ -172,7 +183,7 @@ def test_tiny_layer_e4m3_two_iterations():
     hp, o = plan_both(st, 68, 64)
     got = gl.forward(hp, w.x, 512)
     ref = of.layer_forward(wq, dims, o, w.x, k_ref, v_ref, cos, sin, storage="bf16")
-    assert_close(got, ref, "tiny e4m3 iteration B", scale="rms")
+    assert_close(got, ref, "tiny e4m3 iteration B", atol=E4M3_FLIP_ATOL * rms(ref))
     assert_close(wd.to_numpy(gl.k), k_ref, "tiny e4m3 K cache")
 
 

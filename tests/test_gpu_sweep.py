@@ -16,7 +16,7 @@ import oracle.layer as ol
 import oracle.plan as op
 import workloads as wl
 from workloads import device as wd
-from tests.gpu_harness import GpuLayer, assert_close, oracle_layer, plan_both
+from tests.gpu_harness import GpuLayer, assert_close, assert_layer, oracle_layer_both, plan_both
 
 pytestmark = pytest.mark.gpu
 
@@ -73,23 +73,28 @@ def test_chunked_prefill_2048_against_oracle():
     xp = wl.activations(rng, L, dims.d_model)
     st = wl.make_state(rng, dims, [], [(L, 0)], slack_pages=L // 16 + 4)
     gl = GpuLayer(w, dims, st.k_pool, st.v_pool, L + 1)
-    k_ref, v_ref = st.k_pool.copy(), st.v_pool.copy()
-    outs, refs = [], []
+    p32 = (st.k_pool.copy(), st.v_pool.copy())
+    p16 = (st.k_pool.copy(), st.v_pool.copy())
+    outs, refs, emus, hs = [], [], [], []
     while st.prefills[0].done < L:
         hp, o = plan_both(st, C, C)
         xr = xp[np.asarray(hp.row_pos)]
         outs.append(gl.forward(hp, xr, L))
-        refs.append(oracle_layer(w, dims, o, xr, k_ref, v_ref, L + 1))
+        ref, emu, h = oracle_layer_both(w, dims, o, xr, p32, p16, L + 1)
+        refs.append(ref)
+        emus.append(emu)
+        hs.append(h)
         st.prefills[0].pages = list(hp.pf_pages[0])
         st.prefills[0].done += int(hp.pf_take[0])
         st.free_pool = list(hp.free_pool)
-    assert_close(np.concatenate(outs), np.concatenate(refs), "chunked prefill 2048 / 512", scale="rms")
+    assert_layer(np.concatenate(outs), np.concatenate(refs), np.concatenate(emus), np.concatenate(hs),
+                 "chunked prefill 2048 / 512")
     sl = np.concatenate([[pg * 16 + t for t in range(16)] for pg in st.prefills[0].pages])[:L]
     kg = wd.to_numpy(gl.k)
-    assert_close(kg[sl // 16, :, sl % 16], k_ref[sl // 16, :, sl % 16], "chunked prefill K cache")
+    assert_close(kg[sl // 16, :, sl % 16], p16[0][sl // 16, :, sl % 16], "chunked prefill K cache")
 
 
-@pytest.mark.parametrize("tau", [64, 1024])
+@pytest.mark.parametrize("tau", [64, 1024, 2048, 4096])
 def test_tau_sweep_point_against_oracle(tau):
     w = wl.mistral_layer(seed=7, tau=tau, n_dec=64, ctx_lo=512, ctx_hi=8192, prompt_len=8192, offset=0)
     st, dims = w.state, w.dims
@@ -98,5 +103,6 @@ def test_tau_sweep_point_against_oracle(tau):
     max_pos = 8192 + tau + 1
     gl = GpuLayer(w.weights[0], dims, st.k_pool, st.v_pool, max_pos)
     got = gl.forward(hp, w.x, int(hp.seq_kv_len.max()))
-    ref = oracle_layer(w.weights[0], dims, o, w.x, st.k_pool.copy(), st.v_pool.copy(), max_pos)
-    assert_close(got, ref, f"tau={tau} layer output", scale="rms")
+    ref, emu, h = oracle_layer_both(w.weights[0], dims, o, w.x, (st.k_pool.copy(), st.v_pool.copy()),
+                                 (st.k_pool.copy(), st.v_pool.copy()), max_pos)
+    assert_layer(got, ref, emu, h, f"tau={tau} layer output")

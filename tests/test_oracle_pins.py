@@ -831,6 +831,26 @@ def test_bf16_storage_variant_is_close_to_fp32_and_not_equal():
     assert np.all((b.view(np.uint32) & 0xFFFF) == 0)
 
 
+def test_bf16_storage_variant_without_rounding_is_the_layer(monkeypatch):
+    """With rounding turned into the identity, the variant computes the same
+    function as the plain layer: its folded norms are the identity
+    RMSNorm(v; g) W^T = (v (W diag g)^T) / rms(v), so only the order of
+    float64 operations differs."""
+    rng = np.random.default_rng(12)
+    dims = tiny_dims(d_model=64, d_ff=96)
+    w = wl.layer_weights(rng, dims, gamma_jitter=0.2)
+    st = tiny_state(rng, dims, [9, 30], [(40, 5)])
+    p = plan_from_state(st, 30, 30)
+    cos, sin = ol.rope_tables(64, dims.d_head, dims.theta)
+    x = rng.standard_normal((p.n_rows, dims.d_model))
+    f64 = np.float64
+    a = ol.layer_forward(w, dims, p, x, st.k_pool.astype(f64), st.v_pool.astype(f64), cos, sin, f64)
+    monkeypatch.setattr(ol, "round_bf16", lambda t: np.asarray(t, f64))
+    b = ol.layer_forward(w, dims, p, x, st.k_pool.astype(f64), st.v_pool.astype(f64), cos, sin, f64,
+                         storage="bf16")
+    np.testing.assert_allclose(b, a, rtol=1e-12, atol=1e-12)
+
+
 # ---------------------------------------------------------------- iteration driver
 def _run_loop(loop, arrivals, max_iters=10_000):
     """arrivals: {iteration: [(prompt_len, max_new), ...]}; returns per-iteration (plan, row_req)."""
