@@ -21,13 +21,16 @@ constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
 // stand-in, so its device address is looked up with cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_attention_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices];
+void* g_scratch_ptr[hb::kMaxDevices];
 std::mutex g_scratch_mu;
 
 // Device address of the scratch array on `device` (the current device),
 // looked up once per device.
 hb_status scratch_address(int device, void** out) {
+  if (device < 0 || device >= hb::kMaxDevices) {
+    hb::set_error("hb_attention_noalloc: device ordinal %d out of range", device);
+    return HB_ERR_UNSUPPORTED;
+  }
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (g_scratch_ptr[device] == nullptr) {
     void* p = nullptr;

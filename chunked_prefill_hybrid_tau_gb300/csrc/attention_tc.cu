@@ -604,19 +604,11 @@ hb_status chunk_tc_launch(const DeviceCtx& ctx, const void* q, const CUtensorMap
   p.work_counter = work_counter;
   p.status = ctx.status;
   if (chunk_pair_eligible(dm)) return chunk_pair_launch(ctx, tmQ, tmK, tmV, p, grid, stream);
-  static bool attr_set[2][64] = {};
-  const int di = dm.d_head == 128 ? 1 : 0;
-  if (!attr_set[di][ctx.device]) {
-    st = dm.d_head == 128
-             ? cuda_status(cudaFuncSetAttribute(chunk_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                TC<128>::SMEM),
-                           "cudaFuncSetAttribute(chunk_tc)")
-             : cuda_status(cudaFuncSetAttribute(chunk_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                TC<64>::SMEM),
-                           "cudaFuncSetAttribute(chunk_tc)");
-    if (st != HB_OK) return st;
-    attr_set[di][ctx.device] = true;
-  }
+  static std::atomic<bool> attr_set[2][kMaxDevices];
+  st = dm.d_head == 128
+           ? smem_limit_once(attr_set[1], ctx.device, chunk_tc_kernel<128>, TC<128>::SMEM, "cudaFuncSetAttribute(chunk_tc)")
+           : smem_limit_once(attr_set[0], ctx.device, chunk_tc_kernel<64>, TC<64>::SMEM, "cudaFuncSetAttribute(chunk_tc)");
+  if (st != HB_OK) return st;
   if (dm.d_head == 128)
     chunk_tc_kernel<128><<<grid, kThreads, TC<128>::SMEM, stream>>>(tmQ, tmK, tmV, p);
   else

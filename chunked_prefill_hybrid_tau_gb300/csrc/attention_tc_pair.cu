@@ -528,14 +528,9 @@ bool chunk_pair_eligible(const hb_layer_dims& dm) { return dm.d_head == 128 && (
 
 hb_status chunk_pair_launch(const DeviceCtx& ctx, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const TcParams& p, int grid, cudaStream_t stream) {
-  static bool attr_set[64] = {};
-  if (!attr_set[ctx.device]) {
-    hb_status st = cuda_status(
-        cudaFuncSetAttribute(chunk_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::SMEM),
-        "cudaFuncSetAttribute(chunk_pair)");
-    if (st != HB_OK) return st;
-    attr_set[ctx.device] = true;
-  }
+  static std::atomic<bool> attr_set[kMaxDevices];
+  hb_status st = smem_limit_once(attr_set, ctx.device, chunk_pair_kernel, PC::SMEM, "cudaFuncSetAttribute(chunk_pair)");
+  if (st != HB_OK) return st;
   grid &= ~1;
   if (grid < 2) grid = 2;
   chunk_pair_kernel<<<grid, kThreads, PC::SMEM, stream>>>(tmQ, tmK, tmV, p);

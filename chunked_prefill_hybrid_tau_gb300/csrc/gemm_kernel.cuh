@@ -731,14 +731,9 @@ hb_status launch_pair(const DeviceCtx& ctx, const void* A, int lda, const float*
   if (st != HB_OK) return st;
   st = encode_tmap_2d(&tmB, B, K, N, static_cast<uint64_t>(K) * ESZ, BK, BN / 2, true, ESZ);
   if (st != HB_OK) return st;
-  static bool attr_set[64] = {};
-  if (!attr_set[ctx.device]) {
-    st = cuda_status(cudaFuncSetAttribute(gemm_pair_kernel<BN, EPI, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          C::SMEM),
-                     "cudaFuncSetAttribute(gemm pair)");
-    if (st != HB_OK) return st;
-    attr_set[ctx.device] = true;
-  }
+  static std::atomic<bool> attr_set[kMaxDevices];
+  st = smem_limit_once(attr_set, ctx.device, gemm_pair_kernel<BN, EPI, F8>, C::SMEM, "cudaFuncSetAttribute(gemm pair)");
+  if (st != HB_OK) return st;
   Params p;
   p.M = M;
   p.N = N;
@@ -775,14 +770,9 @@ hb_status launch(const DeviceCtx& ctx, const void* A, int lda, const float* sa, 
   if (st != HB_OK) return st;
   st = encode_tmap_2d(&tmB, B, K, N, static_cast<uint64_t>(K) * ESZ, BK, BN, true, ESZ);
   if (st != HB_OK) return st;
-  static bool attr_set[64] = {};
-  if (!attr_set[ctx.device]) {
-    st = cuda_status(cudaFuncSetAttribute(gemm_kernel<BN, EPI, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          C::SMEM),
-                     "cudaFuncSetAttribute(gemm)");
-    if (st != HB_OK) return st;
-    attr_set[ctx.device] = true;
-  }
+  static std::atomic<bool> attr_set[kMaxDevices];
+  st = smem_limit_once(attr_set, ctx.device, gemm_kernel<BN, EPI, F8>, C::SMEM, "cudaFuncSetAttribute(gemm)");
+  if (st != HB_OK) return st;
   Params p;
   p.M = M;
   p.N = N;

@@ -16,7 +16,6 @@ __device__ int g_hb_status_word;
 namespace hb {
 
 namespace {
-constexpr int kMaxDevices = 64;
 // Per-device state, filled once under g_mu.  The status pointer is published
 // last with release order: a thread that reads it non-null (acquire) also
 // sees that device's SM count and compute capability.

@@ -3,9 +3,14 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "common.h"
 
 namespace hb {
+
+// Device ordinals the per-device state covers (device_context rejects others).
+constexpr int kMaxDevices = 64;
 
 struct DeviceCtx {
   int device;
@@ -27,6 +32,19 @@ hb_status encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uin
                          int elem_bytes = 2);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Raises a kernel's dynamic shared-memory limit once per device.  `done` is
+// that kernel's per-device flag array (kMaxDevices entries, static storage).
+// Host threads that make their first call at the same time may each set the
+// attribute; setting it is idempotent, and the flags are atomics, so this is
+// free of data races.
+template <typename Kernel>
+hb_status smem_limit_once(std::atomic<bool>* done, int device, Kernel kernel, int bytes, const char* what) {
+  if (done[device].load(std::memory_order_acquire)) return HB_OK;
+  hb_status st = cuda_status(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes), what);
+  if (st == HB_OK) done[device].store(true, std::memory_order_release);
+  return st;
+}
 
 // Launch with programmatic stream serialization: the kernel may start while
 // its predecessor on the stream is still running (once every predecessor CTA

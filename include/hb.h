@@ -264,7 +264,7 @@ hb_status hb_kv_append(const void* qkv, int32_t T, const int32_t* row_pos, const
  *   out    : device bf16 [T][n_q * d_head]
  *   workspace: device scratch of hb_attention_workspace_bytes(...) bytes,
  *     256-byte aligned; contents need not be initialised.
- * Requires d_head == 128 and page_size == 16.
+ * Requires d_head == 64 or 128 and page_size == 16.
  * ---------------------------------------------------------------------- */
 size_t hb_attention_workspace_bytes(const hb_layer_dims* dims, int32_t max_rows, int32_t max_seqs,
                                     int32_t max_kv_len);
