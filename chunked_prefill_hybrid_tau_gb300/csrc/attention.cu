@@ -469,7 +469,7 @@ struct SideStream {
   cudaStream_t stream = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
 };
-SideStream g_side[64];
+SideStream g_side[kMaxDevices];
 std::mutex g_side_mu;
 
 hb_status side_stream(int device, SideStream** out) {
@@ -532,14 +532,9 @@ template <int D>
 hb_status attention_launch_d(const DeviceCtx& ctx, const void* q, const hb_device_plan& plan, const hb_layer_dims& dm,
                              const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmK3,
                              const CUtensorMap& tmV3, Params p, cudaStream_t stream) {
-  static bool attr_set[64] = {};
-  if (!attr_set[ctx.device]) {
-    hb_status st = cuda_status(
-        cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DC<D>::SMEM),
-        "cudaFuncSetAttribute(decode)");
-    if (st != HB_OK) return st;
-    attr_set[ctx.device] = true;
-  }
+  static std::atomic<bool> attr_set[kMaxDevices];
+  hb_status st0 = smem_limit_once(attr_set, ctx.device, decode_kernel<D>, DC<D>::SMEM, "cudaFuncSetAttribute(decode)");
+  if (st0 != HB_OK) return st0;
   const int nc = chunk_sms(ctx, plan, dm);
   if (nc == 0) {
     // chunk tiles (tcgen05 path), then decode rows (HBM path), both persistent on all SMs
