@@ -19,7 +19,6 @@
 // (row, kv head).
 #include <cuda_bf16.h>
 
-#include <mutex>
 
 #include "device.cuh"
 #include "runtime.h"
@@ -45,6 +44,11 @@ struct Params {
   int* combine_counters;
   float* partials;
   int* status;
+  // 1 when the chunk kernel precedes this one on the stream: that kernel
+  // waited for the inputs before letting this one start, so the wait here
+  // is deferred to the end (this grid's completion then implies the chunk
+  // kernel's, which the next kernel on the stream relies on)
+  int wait_at_end;
 };
 
 __device__ __forceinline__ int upper_index(const int* pre, int n, int u) {
@@ -208,7 +212,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ga = lane >> 2, t4 = lane & 3;
   griddep_launch_dependents();
-  griddep_wait();
+  if (!p.wait_at_end) griddep_wait();
 
   for (int s = tid; s < p.S; s += blockDim.x) {
     const int q0 = p.q_start[s], q1 = p.q_start[s + 1];
@@ -438,6 +442,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
       }
     }
   }
+  if (p.wait_at_end) griddep_wait();
 }
 
 // ---------------------------------------------------------------- SM split
@@ -464,28 +469,6 @@ constexpr double kBlockUs = 1.5;            // per 128-key block of a chunk unit
 constexpr double kSplitUs = 50.0;           // one full decode split on one warp, d_head 128
 constexpr double kDecodeBwPerSm = 55000.0;  // bytes per us per SM
 constexpr double kDecodeBw = 6.2e6;         // bytes per us, whole GPU
-
-struct SideStream {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-};
-SideStream g_side[kMaxDevices];
-std::mutex g_side_mu;
-
-hb_status side_stream(int device, SideStream** out) {
-  std::lock_guard<std::mutex> lock(g_side_mu);
-  SideStream& ss = g_side[device];
-  if (ss.stream == nullptr) {
-    hb_status st = cuda_status(cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking), "cudaStreamCreate(side)");
-    if (st != HB_OK) return st;
-    st = cuda_status(cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming), "cudaEventCreate(fork)");
-    if (st != HB_OK) return st;
-    st = cuda_status(cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming), "cudaEventCreate(join)");
-    if (st != HB_OK) return st;
-  }
-  *out = &ss;
-  return HB_OK;
-}
 
 // CTAs for the chunk kernel when both paths run concurrently (the decode
 // kernel gets the rest); 0 = run them one after the other on all SMs.
@@ -535,35 +518,24 @@ hb_status attention_launch_d(const DeviceCtx& ctx, const void* q, const hb_devic
   static std::atomic<bool> attr_set[kMaxDevices];
   hb_status st0 = smem_limit_once(attr_set, ctx.device, decode_kernel<D>, DC<D>::SMEM, "cudaFuncSetAttribute(decode)");
   if (st0 != HB_OK) return st0;
+  // Chunk rows first, then decode rows, both on `stream` with programmatic
+  // serialization: the chunk kernel takes nc SMs (all of them when run one
+  // after the other) and the decode kernel starts beside it on the rest as
+  // soon as every chunk CTA has passed its wait for the inputs.  Both are
+  // launched whatever the hints say (a kernel without work exits at once),
+  // so results never depend on the hints.
   const int nc = chunk_sms(ctx, plan, dm);
-  if (nc == 0) {
-    // chunk tiles (tcgen05 path), then decode rows (HBM path), both persistent on all SMs
-    hb_status st =
-        chunk_tc_launch(ctx, q, tmK, tmV, plan, dm, p.num_pages, p.max_kv_len, p.out, p.work_counter, ctx.num_sms, stream);
-    if (st != HB_OK) return st;
-    decode_kernel<D><<<ctx.num_sms, kDecWarps * 32, DC<D>::SMEM, stream>>>(tmK3, tmV3, p);
-    return launch_status("decode_kernel launch");
-  }
-  SideStream* ss = nullptr;
-  hb_status st = side_stream(ctx.device, &ss);
+  hb_status st = chunk_tc_launch(ctx, q, tmK, tmV, plan, dm, p.num_pages, p.max_kv_len, p.out, p.work_counter,
+                                 nc > 0 ? nc : ctx.num_sms, stream);
   if (st != HB_OK) return st;
-  st = cuda_status(cudaEventRecord(ss->fork, stream), "cudaEventRecord(fork)");
-  if (st != HB_OK) return st;
-  st = cuda_status(cudaStreamWaitEvent(ss->stream, ss->fork, 0), "cudaStreamWaitEvent(fork)");
-  if (st != HB_OK) return st;
-  st = chunk_tc_launch(ctx, q, tmK, tmV, plan, dm, p.num_pages, p.max_kv_len, p.out, p.work_counter, nc, ss->stream);
-  if (st != HB_OK) return st;
-  decode_kernel<D><<<ctx.num_sms - nc, kDecWarps * 32, DC<D>::SMEM, stream>>>(tmK3, tmV3, p);
-  st = launch_status("decode_kernel launch");
-  if (st != HB_OK) return st;
-  st = cuda_status(cudaEventRecord(ss->join, ss->stream), "cudaEventRecord(join)");
-  if (st != HB_OK) return st;
-  return cuda_status(cudaStreamWaitEvent(stream, ss->join, 0), "cudaStreamWaitEvent(join)");
+  p.wait_at_end = 1;
+  return launch_pdl(decode_kernel<D>, nc > 0 ? ctx.num_sms - nc : ctx.num_sms, kDecWarps * 32, DC<D>::SMEM, stream,
+                    "decode_kernel launch", tmK3, tmV3, p);
 }
 
 }  // namespace
 
-static size_t counter_bytes(const hb_layer_dims& dm, int n_seqs) {
+size_t attention_counter_bytes(const hb_layer_dims& dm, int n_seqs) {
   const size_t c = 256 + static_cast<size_t>(n_seqs) * dm.n_kv * 4;
   return (c + 255) & ~size_t(255);
 }
@@ -571,12 +543,12 @@ static size_t counter_bytes(const hb_layer_dims& dm, int n_seqs) {
 size_t attention_workspace_bytes(const hb_layer_dims& dm, int max_seqs, int max_kv_len) {
   const size_t splits = (static_cast<size_t>(max_kv_len) + SPLIT - 1) / SPLIT;
   const size_t units = static_cast<size_t>(max_seqs) * dm.n_kv * splits;
-  return counter_bytes(dm, max_seqs) + units * (16 * static_cast<size_t>(dm.d_head) + 32) * 4;
+  return attention_counter_bytes(dm, max_seqs) + units * (16 * static_cast<size_t>(dm.d_head) + 32) * 4;
 }
 
 hb_status attention_launch(const DeviceCtx& ctx, const void* q, const void* k_cache, const void* v_cache,
                            int num_pages, const hb_device_plan& plan, const hb_layer_dims& dm, int max_kv_len,
-                           void* out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                           void* out, void* ws, size_t ws_bytes, cudaStream_t stream, bool counters_zeroed) {
   HB_REQUIRE(dm.d_head == 128 || dm.d_head == 64, "hb_attention: d_head must be 64 or 128");
   HB_REQUIRE(plan.n_seqs <= MAX_SEQS, "hb_attention: at most %d sequences per iteration", MAX_SEQS);
   HB_REQUIRE(plan.n_seqs >= 0 && plan.n_rows >= 0 && plan.max_pages >= 1, "hb_attention: bad plan sizes");
@@ -596,9 +568,11 @@ hb_status attention_launch(const DeviceCtx& ctx, const void* q, const void* k_ca
   if (st != HB_OK) return st;
   st = encode_tmap_kv_pages(&tmV3, v_cache, rows, dm.d_head);
   if (st != HB_OK) return st;
-  const size_t counters = counter_bytes(dm, plan.n_seqs);
-  st = cuda_status(cudaMemsetAsync(ws, 0, counters, stream), "cudaMemsetAsync(attention counters)");
-  if (st != HB_OK) return st;
+  const size_t counters = attention_counter_bytes(dm, plan.n_seqs);
+  if (!counters_zeroed) {
+    st = cuda_status(cudaMemsetAsync(ws, 0, counters, stream), "cudaMemsetAsync(attention counters)");
+    if (st != HB_OK) return st;
+  }
   Params p;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.out = static_cast<__nv_bfloat16*>(out);
@@ -649,5 +623,5 @@ extern "C" hb_status hb_attention(const void* q, const void* k_cache, const void
   st = hb::device_context(&ctx);
   if (st != HB_OK) return st;
   return hb::attention_launch(ctx, q, k_cache, v_cache, num_pages, *plan, *dims, max_kv_len, out, workspace, ws_bytes,
-                              static_cast<cudaStream_t>(stream));
+                              static_cast<cudaStream_t>(stream), false);
 }

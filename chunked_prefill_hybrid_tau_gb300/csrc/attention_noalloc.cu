@@ -70,5 +70,5 @@ extern "C" hb_status hb_attention_noalloc(const void* q, const void* k_cache, co
   st = scratch_address(ctx.device, &scratch);
   if (st != HB_OK) return st;
   return hb::attention_launch(ctx, q, k_cache, v_cache, num_pages, *plan, *dims, max_kv_len, out, scratch,
-                              kNoAllocScratchBytes, static_cast<cudaStream_t>(stream));
+                              kNoAllocScratchBytes, static_cast<cudaStream_t>(stream), false);
 }

@@ -97,8 +97,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, TcParams p) {
   using C = TC<D>;
-  griddep_launch_dependents();
+  // The decode kernel that follows on the stream starts once every CTA here
+  // has passed this wait (so the appended K/V and q are complete) and runs
+  // beside this kernel on the other SMs.
   griddep_wait();
+  griddep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + C::OFF_Q;
@@ -610,10 +613,10 @@ hb_status chunk_tc_launch(const DeviceCtx& ctx, const void* q, const CUtensorMap
            : smem_limit_once(attr_set[0], ctx.device, chunk_tc_kernel<64>, TC<64>::SMEM, "cudaFuncSetAttribute(chunk_tc)");
   if (st != HB_OK) return st;
   if (dm.d_head == 128)
-    chunk_tc_kernel<128><<<grid, kThreads, TC<128>::SMEM, stream>>>(tmQ, tmK, tmV, p);
-  else
-    chunk_tc_kernel<64><<<grid, kThreads, TC<64>::SMEM, stream>>>(tmQ, tmK, tmV, p);
-  return launch_status("chunk_tc_kernel launch");
+    return launch_pdl(chunk_tc_kernel<128>, grid, kThreads, TC<128>::SMEM, stream, "chunk_tc_kernel launch", tmQ, tmK,
+                      tmV, p);
+  return launch_pdl(chunk_tc_kernel<64>, grid, kThreads, TC<64>::SMEM, stream, "chunk_tc_kernel launch", tmQ, tmK, tmV,
+                    p);
 }
 
 }  // namespace hb

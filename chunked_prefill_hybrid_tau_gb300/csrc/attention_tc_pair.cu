@@ -90,8 +90,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     chunk_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, TcParams p) {
   using C = PC;
-  griddep_launch_dependents();
+  // The decode kernel that follows on the stream starts once every CTA here
+  // has passed this wait (so the appended K/V and q are complete) and runs
+  // beside this kernel on the other SMs.
   griddep_wait();
+  griddep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + C::OFF_Q;
@@ -533,8 +536,7 @@ hb_status chunk_pair_launch(const DeviceCtx& ctx, const CUtensorMap& tmQ, const 
   if (st != HB_OK) return st;
   grid &= ~1;
   if (grid < 2) grid = 2;
-  chunk_pair_kernel<<<grid, kThreads, PC::SMEM, stream>>>(tmQ, tmK, tmV, p);
-  return launch_status("chunk_pair_kernel launch");
+  return launch_pdl(chunk_pair_kernel, grid, kThreads, PC::SMEM, stream, "chunk_pair_kernel launch", tmQ, tmK, tmV, p);
 }
 
 }  // namespace hb

@@ -9,7 +9,7 @@ namespace hb {
 bool gemm_split_k(int N, int K, int epi) {
   // a function of the shape alone, never of M: a row's result must not
   // depend on how many rows share the launch
-  return epi == HB_EPI_RESIDUAL && N % 256 == 0 && N <= 8192 && K >= 8192;
+  return epi == HB_EPI_RESIDUAL && N % 256 == 0 && N <= 8192 && K >= 4096;
 }
 
 size_t gemm_split_part_bytes(int M, int N) {
@@ -19,23 +19,48 @@ size_t gemm_split_part_bytes(int M, int N) {
 
 int gemm_split_flags(int M, int N) { return ((M + BM - 1) / BM) * ((N + 255) / 256) * 4; }
 
-bool gemm_use_pair(int M, int N, int epi, bool split) {
-  // 256 x 256 pair tiles for the wide projections with more than one
-  // 128-row tile: gate/up (SwiGLU) and the split-K residual ones.  (The QKV
-  // and O projections at M = 512 gain nothing from pairs: one tile per CTA,
-  // bound by the ring fill and the epilogue, not by the shared-memory fill.)
-  return M > BM && N % kPairBN == 0 && (epi == HB_EPI_SWIGLU || (epi == HB_EPI_RESIDUAL && split));
+int gemm_pair_bn(int M, int N, int epi, bool split, int num_sms) {
+  // CTA-pair tiles (256 rows) once M spans more than one 128-row tile: a
+  // pair streams the same bytes per k-block as a one-CTA 128 x 128 tile for
+  // twice the FLOPs, and the k-block time of both is set by the ring's round
+  // trip, not by the MMAs (about 280 ns either way on GB300).  SwiGLU and the
+  // split-K residual projections take 256-wide tiles; a plain store picks
+  // 192 or 256 for the fewest waves of pair tiles over the SM pairs.
+  if (M <= BM) return 0;
+  if (epi == HB_EPI_SWIGLU || (epi == HB_EPI_RESIDUAL && split)) return N % kPairBN == 0 ? kPairBN : 0;
+  if (epi != HB_EPI_STORE) return 0;
+  const int pm = (M + 2 * BM - 1) / (2 * BM);
+  const int pairs = num_sms / 2;
+  int best = 0;
+  double best_cost = 1e30;
+  for (int bn : {256, 192}) {
+    if (N % bn != 0) continue;
+    const int waves = (pm * (N / bn) + pairs - 1) / pairs;
+    const double cost = waves * (bn + 32.0);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
 }
 
 hb_status gemm_launch(const DeviceCtx& ctx, const void* A, int lda, const void* B, void* C, int ldc, const void* R,
                       int M, int N, int K, int epi, cudaStream_t stream, const GemmNorm* norm, const GemmSplit* split) {
   if (split != nullptr && !gemm_split_k(N, K, epi)) split = nullptr;
-  if (gemm_use_pair(M, N, epi, split != nullptr)) {
+  const int pbn = gemm_pair_bn(M, N, epi, split != nullptr, ctx.num_sms);
+  if (pbn != 0) {
     if (epi == HB_EPI_SWIGLU)
       return launch_pair<kPairBN, HB_EPI_SWIGLU, false>(ctx, A, lda, nullptr, B, nullptr, C, ldc, R, M, N, K, norm, split,
                                                       stream);
-    return launch_pair<kPairBN, HB_EPI_RESIDUAL, false>(ctx, A, lda, nullptr, B, nullptr, C, ldc, R, M, N, K, norm, split,
-                                                      stream);
+    if (epi == HB_EPI_RESIDUAL)
+      return launch_pair<kPairBN, HB_EPI_RESIDUAL, false>(ctx, A, lda, nullptr, B, nullptr, C, ldc, R, M, N, K, norm,
+                                                        split, stream);
+    if (pbn == 192)
+      return launch_pair<192, HB_EPI_STORE, false>(ctx, A, lda, nullptr, B, nullptr, C, ldc, R, M, N, K, norm, split,
+                                                   stream);
+    return launch_pair<256, HB_EPI_STORE, false>(ctx, A, lda, nullptr, B, nullptr, C, ldc, R, M, N, K, norm, split,
+                                                 stream);
   }
   // split-K units use the widest tile (N = 256 MMAs run near the tensor peak)
   const int bn = split ? 256 : choose_bn(M, N, epi, ctx.num_sms);

@@ -17,12 +17,17 @@ hb_status gemm_e4m3_launch(const DeviceCtx& ctx, const void* A, int lda, const f
                            const float* sb, void* C, int ldc, const void* R, int M, int N, int K, int epi,
                            cudaStream_t stream, const GemmNorm* norm, const GemmSplit* split) {
   if (split != nullptr && !gemm_split_k(N, K, epi)) split = nullptr;
-  if (gemm_use_pair(M, N, epi, split != nullptr)) {
+  const int pbn = gemm_pair_bn(M, N, epi, split != nullptr, ctx.num_sms);
+  if (pbn != 0) {
     if (epi == HB_EPI_SWIGLU)
       return launch_pair<kPairBN, HB_EPI_SWIGLU, true>(ctx, A, lda, sa, B, sb, C, ldc, R, M, N, K, norm, split,
                                                       stream);
-    return launch_pair<kPairBN, HB_EPI_RESIDUAL, true>(ctx, A, lda, sa, B, sb, C, ldc, R, M, N, K, norm, split,
-                                                      stream);
+    if (epi == HB_EPI_RESIDUAL)
+      return launch_pair<kPairBN, HB_EPI_RESIDUAL, true>(ctx, A, lda, sa, B, sb, C, ldc, R, M, N, K, norm, split,
+                                                        stream);
+    if (pbn == 192)
+      return launch_pair<192, HB_EPI_STORE, true>(ctx, A, lda, sa, B, sb, C, ldc, R, M, N, K, norm, split, stream);
+    return launch_pair<256, HB_EPI_STORE, true>(ctx, A, lda, sa, B, sb, C, ldc, R, M, N, K, norm, split, stream);
   }
   const int bn = split ? 256 : choose_bn(M, N, epi, ctx.num_sms);
 #define HB_GEMM_CASE(BN_, EPI_) \

@@ -23,7 +23,12 @@
 //   * warps 2-5: epilogue.  tcgen05.ld 32x32b (warp w reads TMEM lanes
 //     32*(w%4)..), fused STORE / RESIDUAL / SWIGLU / F32 epilogue, then the
 //     accumulator buffer is handed back.  Two accumulator buffers let the
-//     epilogue of one tile overlap the main loop of the next.
+//     epilogue of one tile overlap the main loop of the next.  A CTA's last
+//     tile has nothing to overlap, so its epilogue uses the then idle ring:
+//     the residual tile (and a split-K partner's partial) arrive by TMA /
+//     bulk copy, the outputs are staged in 128-byte swizzled rows and leave
+//     by TMA stores, instead of one row per thread through the load/store
+//     units.
 //   * every wait is bounded (device.cuh); on expiry the kernel unwinds.
 #pragma once
 #include <cuda_bf16.h>
@@ -95,7 +100,7 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int u, int m_tiles, int
 // rounding of the result; an IEEE divide here made the SwiGLU epilogue the
 // most expensive part of the gate/up projection.  For g -> -inf the
 // denominator overflows to inf and the quotient is 0, the correct limit.
-__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+__device__ __forceinline__ float silu(float g) { return __fdividef(g, __fadd_rn(1.0f, __expf(-g))); }
 
 // Inverse RMS of one row from its 32-column partial sums of squares, summed
 // in column order: rsqrt(sum / d + eps).
@@ -127,7 +132,7 @@ __device__ __forceinline__ void store_chunk(const Params& p, int row, int col, c
     uint32_t w[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-      w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * scale, __uint_as_float(r[2 * i + 1]) * scale);
+      w[i] = pack_bf16x2(__fmul_rn(__uint_as_float(r[2 * i]), scale), __fmul_rn(__uint_as_float(r[2 * i + 1]), scale));
     uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) + static_cast<size_t>(row) * p.ldc + col);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -148,7 +153,7 @@ __device__ __forceinline__ void residual_chunk(const Params& p, int row, int col
     for (int j = 0; j < 4; ++j) {
       const float2 f = unpack_bf16x2(rr[j]);
       const int e = 8 * i + 2 * j;
-      w[4 * i + j] = pack_bf16x2(f.x + __uint_as_float(r[e]), f.y + __uint_as_float(r[e + 1]));
+      w[4 * i + j] = pack_bf16x2(__fadd_rn(f.x, __uint_as_float(r[e])), __fadd_rn(f.y, __uint_as_float(r[e + 1])));
     }
   }
   if (ss_dst) {
@@ -156,8 +161,8 @@ __device__ __forceinline__ void residual_chunk(const Params& p, int row, int col
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const float2 f = unpack_bf16x2(w[i]);
-      ss += f.x * f.x;
-      ss += f.y * f.y;
+      ss = __fmaf_rn(f.x, f.x, ss);
+      ss = __fmaf_rn(f.y, f.y, ss);
     }
     *ss_dst = ss;
   }
@@ -170,15 +175,17 @@ __device__ __forceinline__ void residual_chunk(const Params& p, int row, int col
 // E4M3 operands: acc * rowf * sb[col + j] for 32 accumulator columns, in
 // place (rowf = the row's scale times its folded RMSNorm factor, if any);
 // columns at or past N get scale 0.
+// The products are rounded explicitly (no contraction into a later add), so
+// every epilogue path produces the same bits.
 __device__ __forceinline__ void scale_cols(uint32_t (&r)[32], float rowf, const float* sb, int col, int N) {
   const float4* s4 = reinterpret_cast<const float4*>(sb + col);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float4 s = col + 4 * i < N ? __ldg(s4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-    r[4 * i] = __float_as_uint(__uint_as_float(r[4 * i]) * rowf * s.x);
-    r[4 * i + 1] = __float_as_uint(__uint_as_float(r[4 * i + 1]) * rowf * s.y);
-    r[4 * i + 2] = __float_as_uint(__uint_as_float(r[4 * i + 2]) * rowf * s.z);
-    r[4 * i + 3] = __float_as_uint(__uint_as_float(r[4 * i + 3]) * rowf * s.w);
+    r[4 * i] = __float_as_uint(__fmul_rn(__fmul_rn(__uint_as_float(r[4 * i]), rowf), s.x));
+    r[4 * i + 1] = __float_as_uint(__fmul_rn(__fmul_rn(__uint_as_float(r[4 * i + 1]), rowf), s.y));
+    r[4 * i + 2] = __float_as_uint(__fmul_rn(__fmul_rn(__uint_as_float(r[4 * i + 2]), rowf), s.z));
+    r[4 * i + 3] = __float_as_uint(__fmul_rn(__fmul_rn(__uint_as_float(r[4 * i + 3]), rowf), s.w));
   }
 }
 
@@ -189,8 +196,8 @@ __device__ __forceinline__ void scale_cols(uint32_t (&r)[32], float rowf, const 
 // scale (F8).
 template <int BN, int EPI, bool F8>
 __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_base, int row, bool row_ok, int rloc,
-                                              int n_blk, int stile, int half, int quarter, int lane, float scale,
-                                              float rowf) {
+                                              int n_blk, int stile, int half, bool leader, volatile int* ep_flag,
+                                              float scale, float rowf) {
   if (EPI == HB_EPI_SWIGLU) {
 #pragma unroll 1
     for (int j = 0; j < BN / 128; ++j) {
@@ -212,8 +219,9 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_base, 
           uint32_t w[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float a0 = silu(__uint_as_float(g[2 * i]) * sc) * (__uint_as_float(u[2 * i]) * sc);
-            const float a1 = silu(__uint_as_float(g[2 * i + 1]) * sc) * (__uint_as_float(u[2 * i + 1]) * sc);
+            const float a0 = __fmul_rn(silu(__fmul_rn(__uint_as_float(g[2 * i]), sc)), __fmul_rn(__uint_as_float(u[2 * i]), sc));
+            const float a1 =
+                __fmul_rn(silu(__fmul_rn(__uint_as_float(g[2 * i + 1]), sc)), __fmul_rn(__uint_as_float(u[2 * i + 1]), sc));
             w[i] = pack_bf16x2(a0, a1);
           }
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) +
@@ -229,10 +237,10 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_base, 
     const float* other = nullptr;
     if (p.ksplit == 2) {
       // Split K: publish this half's fp32 partial (column-major, so each
-      // store is one coalesced 128-byte line per warp); the second warp
-      // to arrive for this 32-row slab adds the other half and finishes.
-      // p0 + p1 is commutative, so the result does not depend on which
-      // half arrives last.
+      // store is one coalesced 128-byte line per warp); the CTA that
+      // arrives second for this 128-row tile adds the other half and
+      // finishes.  p0 + p1 is commutative, so the result does not depend on
+      // which half arrives last.
       float* mine = p.part + (static_cast<size_t>(stile) * 2 + half) * BN * BM;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
@@ -243,14 +251,15 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_base, 
         for (int j = 0; j < 32; ++j) mine[static_cast<size_t>(c * 32 + j) * BM + rloc] = __uint_as_float(r[j]);
       }
       __threadfence();
-      __syncwarp();
-      int last = 0;
-      if (lane == 0) {
-        int* flag = p.flags + stile * 4 + quarter;
-        last = atomicAdd(flag, 1) == 1;
+      named_barrier_sync(1, 128);
+      if (leader) {
+        int* flag = p.flags + stile * 4;  // one counter per 128-row tile
+        const int last = atomicAdd(flag, 1) == 1;
         if (last) *flag = 0;
+        *ep_flag = last;
       }
-      finish = __shfl_sync(0xffffffffu, last, 0) != 0;
+      named_barrier_sync(1, 128);
+      finish = *ep_flag != 0;
       if (finish) {
         __threadfence();
         other = p.part + (static_cast<size_t>(stile) * 2 + (1 - half)) * BN * BM;
@@ -284,7 +293,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_base, 
         tmem_ld_wait();
         if (other != nullptr) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + ov[b][j]);
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fadd_rn(__uint_as_float(r[j]), ov[b][j]));
         }
         const int col = n_blk * BN + c * 32;
         if constexpr (F8) scale_cols(r, rowf, p.sb, col, p.N);
@@ -307,9 +316,200 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_base, 
   }
 }
 
+// Byte offset of 16-byte chunk c (0..7) of row r in a staged slab of 128
+// rows x 128 bytes with the 128-byte swizzle (the TMA box layout).
+__device__ __forceinline__ uint32_t slab_off(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+constexpr int kSlabBytes = 128 * 128;
+
+// Epilogue of a CTA's last 128 x BN accumulator block, staged through the
+// ring (idle once the tile's MMAs are done; at least 192 KB):
+//   STORE / F32 / SWIGLU: outputs into 128-byte slabs, then TMA stores;
+//   RESIDUAL: the residual tile arrives by TMA into the slabs (issued as soon
+//   as the accumulator is ready) and is overwritten in place by the outputs;
+//   with split K, this half's fp32 partial goes out (column-major, coalesced)
+//   and the CTA that arrives second for the tile fetches the other half's
+//   partial with one bulk copy and finishes the tile (p0 + p1 is commutative,
+//   so the result does not depend on which half arrives last).
+// Called by the 128 epilogue threads; `leader` is one of them.  Returns
+// false when a bounded wait expired.
+template <int BN, int EPI, bool F8>
+__device__ __forceinline__ bool epilogue_last(const Params& p, const CUtensorMap* tmC, const CUtensorMap* tmR,
+                                              uint8_t* ring, uint64_t* ep_bar, volatile int* ep_flag, uint32_t t_base,
+                                              int m0, int row, bool row_ok, int rloc, int n_blk, int stile, int half,
+                                              bool leader, float scale, float rowf, volatile int* abort_flag) {
+  if constexpr (EPI == HB_EPI_RESIDUAL) {
+    constexpr int NS = BN / 64;  // 64-column bf16 slabs
+    static_assert(NS * kSlabBytes + (BN * BM * 4) <= 192 * 1024, "ring too small for the split epilogue");
+    uint8_t* part_smem = ring + NS * kSlabBytes;
+    if (leader) {
+      mbar_arrive_expect_tx(&ep_bar[0], NS * kSlabBytes);
+      for (int s = 0; s < NS; ++s) tma_load_2d(ring + s * kSlabBytes, tmR, &ep_bar[0], n_blk * BN + s * 64, m0);
+    }
+    bool finish = true;
+    if (p.ksplit == 2) {
+      float* mine = p.part + (static_cast<size_t>(stile) * 2 + half) * BN * BM;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_base + c * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) mine[static_cast<size_t>(c * 32 + j) * BM + rloc] = __uint_as_float(r[j]);
+      }
+      __threadfence();
+      named_barrier_sync(1, 128);
+      if (leader) {
+        int* flag = p.flags + stile * 4;  // one counter per 128-row tile
+        const int last = atomicAdd(flag, 1) == 1;
+        if (last) {
+          *flag = 0;
+          __threadfence();
+          fence_proxy_async_global();
+          const float* other = p.part + (static_cast<size_t>(stile) * 2 + (1 - half)) * BN * BM;
+          constexpr uint32_t kPiece = BN * BM * 4 / 4;
+          mbar_arrive_expect_tx(&ep_bar[1], 4 * kPiece);
+          for (int i = 0; i < 4; ++i)
+            bulk_load(part_smem + i * kPiece, reinterpret_cast<const uint8_t*>(other) + i * kPiece, kPiece, &ep_bar[1]);
+        }
+        *ep_flag = last;
+      }
+      named_barrier_sync(1, 128);
+      finish = *ep_flag != 0;
+    }
+    // the residual copies land before anything else happens to the ring
+    if (!mbar_wait(&ep_bar[0], 0, abort_flag, p.status)) return false;
+    if (!finish) return true;
+    if (p.ksplit == 2 && !mbar_wait(&ep_bar[1], 0, abort_flag, p.status)) return false;
+    const float* other = reinterpret_cast<const float*>(part_smem);
+#pragma unroll 1
+    for (int s = 0; s < NS; ++s) {
+      uint8_t* slab = ring + s * kSlabBytes;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r[32];
+        const int cl = s * 64 + h * 32;  // accumulator column within the tile
+        tmem_ld_32x32b_x32(t_base + cl, r);
+        tmem_ld_wait();
+        if (p.ksplit == 2) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fadd_rn(__uint_as_float(r[j]), other[(cl + j) * BM + rloc]));
+        }
+        const int col = n_blk * BN + cl;
+        if constexpr (F8) scale_cols(r, rowf, p.sb, col, p.N);
+        float ss = 0.f;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint4* q = reinterpret_cast<uint4*>(slab + slab_off(rloc, h * 4 + c4));
+          const uint4 rv = *q;
+          const uint32_t rr[4] = {rv.x, rv.y, rv.z, rv.w};
+          uint32_t w[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = unpack_bf16x2(rr[j]);
+            const int e = 8 * c4 + 2 * j;
+            w[j] = pack_bf16x2(__fadd_rn(f.x, __uint_as_float(r[e])), __fadd_rn(f.y, __uint_as_float(r[e + 1])));
+            const float2 o = unpack_bf16x2(w[j]);
+            ss = __fmaf_rn(o.x, o.x, ss);
+            ss = __fmaf_rn(o.y, o.y, ss);
+          }
+          *q = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        if (p.norm.ss_out != nullptr && row_ok && col < p.out_cols)
+          p.norm.ss_out[static_cast<size_t>(row) * p.norm.parts + col / 32] = ss;
+      }
+    }
+    fence_proxy_async_smem();
+    named_barrier_sync(1, 128);
+    if (leader) {
+      for (int s = 0; s < NS; ++s) tma_store_2d(tmC, ring + s * kSlabBytes, n_blk * BN + s * 64, m0);
+      bulk_commit_group();
+    }
+    return true;
+  } else if constexpr (EPI == HB_EPI_SWIGLU) {
+    constexpr int NS = BN / 128;  // each 128 accumulator columns (gate 64 | up 64) give a 64-column slab
+#pragma unroll 1
+    for (int s = 0; s < NS; ++s) {
+      uint8_t* slab = ring + s * kSlabBytes;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t g[32], u[32];
+        tmem_ld_32x32b_x32(t_base + s * 128 + h * 32, g);
+        tmem_ld_32x32b_x32(t_base + s * 128 + 64 + h * 32, u);
+        tmem_ld_wait();
+        if constexpr (F8) {
+          const int bcol = n_blk * BN + s * 128 + h * 32;
+          scale_cols(g, rowf, p.sb, bcol, p.N);
+          scale_cols(u, rowf, p.sb, bcol + 64, p.N);
+        }
+        const float sc = F8 ? 1.f : scale;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t w[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int e = 8 * c4 + 2 * j;
+            const float a0 = __fmul_rn(silu(__fmul_rn(__uint_as_float(g[e]), sc)), __fmul_rn(__uint_as_float(u[e]), sc));
+            const float a1 = __fmul_rn(silu(__fmul_rn(__uint_as_float(g[e + 1]), sc)), __fmul_rn(__uint_as_float(u[e + 1]), sc));
+            w[j] = pack_bf16x2(a0, a1);
+          }
+          *reinterpret_cast<uint4*>(slab + slab_off(rloc, h * 4 + c4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    named_barrier_sync(1, 128);
+    if (leader) {
+      for (int s = 0; s < NS; ++s) tma_store_2d(tmC, ring + s * kSlabBytes, n_blk * (BN / 2) + s * 64, m0);
+      bulk_commit_group();
+    }
+    return true;
+  } else {
+    // STORE (bf16, 64 columns per slab) or F32 (fp32, 32 columns per slab)
+    constexpr int SC = EPI == HB_EPI_F32 ? 32 : 64;
+    constexpr int NS = BN / SC;
+#pragma unroll 1
+    for (int s = 0; s < NS; ++s) {
+      uint8_t* slab = ring + s * kSlabBytes;
+#pragma unroll
+      for (int h = 0; h < SC / 32; ++h) {
+        uint32_t r[32];
+        const int cl = s * SC + h * 32;
+        tmem_ld_32x32b_x32(t_base + cl, r);
+        tmem_ld_wait();
+        if constexpr (F8) scale_cols(r, rowf, p.sb, n_blk * BN + cl, p.N);
+        if constexpr (EPI == HB_EPI_F32) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(slab + slab_off(rloc, c)) = make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+        } else {
+          const float sc = F8 ? 1.f : scale;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int e = 8 * c4 + 2 * j;
+              w[j] = pack_bf16x2(__fmul_rn(__uint_as_float(r[e]), sc), __fmul_rn(__uint_as_float(r[e + 1]), sc));
+            }
+            *reinterpret_cast<uint4*>(slab + slab_off(rloc, h * 4 + c4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    named_barrier_sync(1, 128);
+    if (leader) {
+      for (int s = 0; s < NS; ++s) tma_store_2d(tmC, ring + s * kSlabBytes, n_blk * BN + s * SC, m0);
+      bulk_commit_group();
+    }
+    return true;
+  }
+}
+
 template <int BN, int EPI, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR, Params p) {
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -318,8 +518,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* ep_bar = drain + 1;  // last-tile epilogue: residual copies, partner partial
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ep_bar + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* ep_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -340,10 +542,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acc_empty[a], 4);
     }
     mbar_init(drain, 1);
+    mbar_init(&ep_bar[0], 1);
+    mbar_init(&ep_bar[1], 1);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -463,6 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- epilogue
     griddep_wait();
     const int quarter = warp & 3;
+    const bool leader = warp == 2 && lane == 0;
     int t = 0;
     for (int un = blockIdx.x; un < units; un += gridDim.x, ++t) {
       const Unit wu = unit_of<BN>(p, un, m_tiles, kblocks);
@@ -480,11 +686,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-      epilogue_tile<BN, EPI, F8>(p, t_base, row, row_ok, rloc, n_blk, wu.tile, wu.half, quarter, lane, scale, rowf);
+      if (un + static_cast<int>(gridDim.x) >= units) {
+        // the CTA's last tile: the ring is idle, stage through it
+        ok = epilogue_last<BN, EPI, F8>(p, &tmC, &tmR, smem, ep_bar, ep_flag, t_base, m0, row, row_ok, rloc, n_blk,
+                                        wu.tile, wu.half, leader, scale, rowf, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      } else {
+        epilogue_tile<BN, EPI, F8>(p, t_base, row, row_ok, rloc, n_blk, wu.tile, wu.half, leader, ep_flag, scale,
+                                   rowf);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
     }
+    if (leader) bulk_wait_group<0>();  // the TMA stores have left shared memory and are performed
   }
 
   tc_fence_before();
@@ -543,7 +758,8 @@ __device__ __forceinline__ PairUnit pair_unit_of(const Params& p, int u, int pm_
 
 template <int BN, int EPI, bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR, Params p) {
   using C = CfgPair<BN>;
   constexpr int BK = bk_elems<F8>();
   extern __shared__ uint8_t smem_raw[];
@@ -553,8 +769,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + 2;  // even CTA's are used
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* ep_bar = drain + 1;  // last-tile epilogue (this CTA's own): residual copies, partner partial
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ep_bar + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* ep_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -578,10 +796,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&acc_empty[a], 8);
     }
     mbar_init(drain, 1);
+    mbar_init(&ep_bar[0], 1);
+    mbar_init(&ep_bar[1], 1);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
@@ -596,28 +817,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
-    griddep_wait();
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       uint32_t pending = 0, armed_parity = 0;  // stages loaded and not yet seen released
+      // The weights do not come from the previous kernel: the first ring
+      // fill of B is issued before waiting for it, then A follows.
+      int pre = 0;
+      if (cluster < units) {
+        const PairUnit w = pair_unit_of(p, cluster, pm_tiles, kblocks);
+        const int n0 = w.n_blk * BN + static_cast<int>(rank) * (BN / 2);
+        pre = w.kb1 - w.kb0 < C::STAGES ? w.kb1 - w.kb0 : C::STAGES;
+        for (int i = 0; i < pre; ++i) {
+          if (leader) mbar_arrive_expect_tx(&full[i], 2 * C::STAGE_BYTES);  // both CTAs' boxes
+          tma_load_2d_pair(smem + i * C::STAGE_BYTES + C::A_BYTES, &tmB, cluster_addr(&full[i], 0),
+                           (w.kb0 + i) * BK, n0);
+        }
+      }
+      griddep_wait();
       for (int u = cluster; u < units && ok; u += n_clusters) {
         const PairUnit w = pair_unit_of(p, u, pm_tiles, kblocks);
         const int m0 = (2 * w.pm + static_cast<int>(rank)) * BM;
         const int n0 = w.n_blk * BN + static_cast<int>(rank) * (BN / 2);
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          pending |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           uint8_t* sa = smem + stage * C::STAGE_BYTES;
-          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);  // both CTAs' boxes
           const uint32_t fb = cluster_addr(&full[stage], 0);
-          tma_load_2d_pair(sa, &tmA, fb, kb * BK, m0);
-          tma_load_2d_pair(sa + C::A_BYTES, &tmB, fb, kb * BK, n0);
+          if (u == cluster && kb - w.kb0 < pre) {
+            // stage armed and its B box issued above (fresh barriers)
+            pending |= 1u << stage;
+            tma_load_2d_pair(sa, &tmA, fb, kb * BK, m0);
+          } else {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            pending |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);  // both CTAs' boxes
+            tma_load_2d_pair(sa, &tmA, fb, kb * BK, m0);
+            tma_load_2d_pair(sa + C::A_BYTES, &tmB, fb, kb * BK, n0);
+          }
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -684,6 +924,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- epilogue (both CTAs)
     griddep_wait();
     const int quarter = warp & 3;
+    const bool leader_thread = warp == 2 && lane == 0;
     int t = 0;
     for (int un = cluster; un < units; un += n_clusters, ++t) {
       const PairUnit wu = pair_unit_of(p, un, pm_tiles, kblocks);
@@ -700,13 +941,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (mt < m_tiles) {  // a 128-row tile wholly past M (odd tile count) has nothing to write
         const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-        epilogue_tile<BN, EPI, F8>(p, t_base, row, row_ok, rloc, wu.n_blk, mt + m_tiles * wu.n_blk, wu.half,
-                                   quarter, lane, scale, rowf);
+        const int stile = mt + m_tiles * wu.n_blk;
+        if (un + n_clusters >= units) {
+          // the CTA's last tile: its ring is idle, stage through it
+          ok = epilogue_last<BN, EPI, F8>(p, &tmC, &tmR, smem, ep_bar, ep_flag, t_base, mt * BM, row, row_ok, rloc,
+                                          wu.n_blk, stile, wu.half, leader_thread, scale, rowf, abort_flag);
+        } else {
+          epilogue_tile<BN, EPI, F8>(p, t_base, row, row_ok, rloc, wu.n_blk, stile, wu.half, leader_thread, ep_flag,
+                                     scale, rowf);
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(cluster_addr(&acc_empty[acc], 0));
+      if (!__all_sync(0xffffffffu, ok)) break;
     }
+    if (leader_thread) bulk_wait_group<0>();  // the TMA stores have left shared memory and are performed
     if (lane == 0 && *abort_flag) raise_peer_abort(abort_flag, rank);
   }
 
@@ -719,6 +969,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
+// Tensor maps of the output and the residual for the last-tile epilogue:
+// 128-row boxes of one 128-byte row (64 bf16 or 32 fp32 columns), 128-byte
+// swizzle.
+template <int EPI>
+hb_status encode_out_maps(CUtensorMap* tmC, CUtensorMap* tmR, void* Cp, const void* R, int ldc, int M, int out_cols) {
+  const int esz = EPI == HB_EPI_F32 ? 4 : 2;
+  hb_status st = encode_tmap_2d(tmC, Cp, out_cols, M, static_cast<uint64_t>(ldc) * esz, 128 / esz, BM, true, esz);
+  if (st != HB_OK) return st;
+  if (EPI != HB_EPI_RESIDUAL) {
+    *tmR = *tmC;
+    return HB_OK;
+  }
+  return encode_tmap_2d(tmR, R, out_cols, M, static_cast<uint64_t>(ldc) * 2, 64, BM, true, 2);
+}
+
 template <int BN, int EPI, bool F8>
 hb_status launch_pair(const DeviceCtx& ctx, const void* A, int lda, const float* sa, const void* B, const float* sb,
                       void* Cp, int ldc, const void* R, int M, int N, int K, const GemmNorm* norm,
@@ -726,10 +991,12 @@ hb_status launch_pair(const DeviceCtx& ctx, const void* A, int lda, const float*
   using C = CfgPair<BN>;
   constexpr int BK = bk_elems<F8>();
   constexpr int ESZ = F8 ? 1 : 2;
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmC, tmR;
   hb_status st = encode_tmap_2d(&tmA, A, K, M, static_cast<uint64_t>(lda) * ESZ, BK, BM, true, ESZ);
   if (st != HB_OK) return st;
   st = encode_tmap_2d(&tmB, B, K, N, static_cast<uint64_t>(K) * ESZ, BK, BN / 2, true, ESZ);
+  if (st != HB_OK) return st;
+  st = encode_out_maps<EPI>(&tmC, &tmR, Cp, R, ldc, M, EPI == HB_EPI_SWIGLU ? N / 2 : N);
   if (st != HB_OK) return st;
   static std::atomic<bool> attr_set[kMaxDevices];
   st = smem_limit_once(attr_set, ctx.device, gemm_pair_kernel<BN, EPI, F8>, C::SMEM, "cudaFuncSetAttribute(gemm pair)");
@@ -754,7 +1021,7 @@ hb_status launch_pair(const DeviceCtx& ctx, const void* A, int lda, const float*
   const int pairs = ctx.num_sms / 2;
   const int grid = 2 * (units < pairs ? units : pairs);
   return launch_pdl(gemm_pair_kernel<BN, EPI, F8>, grid, kThreads, C::SMEM, stream, "gemm_pair_kernel launch", tmA, tmB,
-                    p);
+                    tmC, tmR, p);
 }
 
 // A [M][K] (row stride lda elements), B [N][K]; sa/sb: E4M3 scales (F8 only).
@@ -765,10 +1032,12 @@ hb_status launch(const DeviceCtx& ctx, const void* A, int lda, const float* sa, 
   using C = Cfg<BN>;
   constexpr int BK = bk_elems<F8>();
   constexpr int ESZ = F8 ? 1 : 2;
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmC, tmR;
   hb_status st = encode_tmap_2d(&tmA, A, K, M, static_cast<uint64_t>(lda) * ESZ, BK, BM, true, ESZ);
   if (st != HB_OK) return st;
   st = encode_tmap_2d(&tmB, B, K, N, static_cast<uint64_t>(K) * ESZ, BK, BN, true, ESZ);
+  if (st != HB_OK) return st;
+  st = encode_out_maps<EPI>(&tmC, &tmR, Cp, R, ldc, M, EPI == HB_EPI_SWIGLU ? N / 2 : N);
   if (st != HB_OK) return st;
   static std::atomic<bool> attr_set[kMaxDevices];
   st = smem_limit_once(attr_set, ctx.device, gemm_kernel<BN, EPI, F8>, C::SMEM, "cudaFuncSetAttribute(gemm)");
@@ -791,7 +1060,8 @@ hb_status launch(const DeviceCtx& ctx, const void* A, int lda, const float* sa, 
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int units = tiles * p.ksplit;
   const int grid = units < ctx.num_sms ? units : ctx.num_sms;
-  return launch_pdl(gemm_kernel<BN, EPI, F8>, grid, kThreads, C::SMEM, stream, "gemm_kernel launch", tmA, tmB, p);
+  return launch_pdl(gemm_kernel<BN, EPI, F8>, grid, kThreads, C::SMEM, stream, "gemm_kernel launch", tmA, tmB, tmC,
+                    tmR, p);
 }
 
 // Tile width: fewest waves of tiles over the SMs, weighted by a per-tile

@@ -48,13 +48,15 @@ LayerWs layer_ws(const hb_layer_dims& dm, int T, int S, int max_kv_len) {
   w.a = off;    off += align256(t * ffn_pad(dm) * 2);
   w.part_o = off; off += align256(gemm_split_part_bytes(T, dm.d_model));
   w.part_d = off; off += align256(gemm_split_part_bytes(T, dm.d_model));
-  w.flags = off;  off += align256(static_cast<size_t>(2) * gemm_split_flags(T, dm.d_model) * 4);
   // E4M3 operands of the four projections and their per-token scales
   w.q8_x = off; off += align256(t * dm.d_model);
   w.q8_o = off; off += align256(t * dm.n_q * dm.d_head);
   w.q8_h = off; off += align256(t * dm.d_model);
   w.q8_a = off; off += align256(t * ffn_pad(dm));
   w.s8 = off;   off += 4 * align256(t * 4);
+  // split-K counters right before the attention workspace, whose counters
+  // come first: the layer's first kernel zeroes both in one range
+  w.flags = off;  off += align256(static_cast<size_t>(2) * gemm_split_flags(T, dm.d_model) * 4);
   w.attn = off; off += align256(attention_workspace_bytes(dm, S, max_kv_len));
   w.total = off;
   return w;
@@ -140,8 +142,10 @@ extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_
     nm->eps = dm.rms_eps;
   }
   // split-K workspaces of the o and down projections: fp32 partial tiles
-  // and arrival counters (zeroed by the row statistics pass, left zero)
+  // and arrival counters, and the attention counters after them: zeroed by
+  // the layer's first kernel (row statistics or the quantization of x)
   const int n_flags = gemm_split_flags(T, d);
+  const int n_zero = static_cast<int>((lw.attn - lw.flags + attention_counter_bytes(dm, plan->n_seqs)) / 4);
   GemmSplit split_o, split_d;
   split_o.part = reinterpret_cast<float*>(ws + lw.part_o);
   split_d.part = reinterpret_cast<float*>(ws + lw.part_d);
@@ -156,13 +160,13 @@ extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_
     float* so = sx + align256(static_cast<size_t>(T) * 4) / 4;
     float* sh = so + align256(static_cast<size_t>(T) * 4) / 4;
     float* sa = sh + align256(static_cast<size_t>(T) * 4) / 4;
-    HB_STEP(0, quant_rows_launch(ctx, x_in, xq, sx, T, d, ss_x, split_o.flags, 2 * n_flags, s));
+    HB_STEP(0, quant_rows_launch(ctx, x_in, xq, sx, T, d, ss_x, split_o.flags, n_zero, s));
     HB_STEP(1, gemm_e4m3_launch(ctx, xq, d, sx, w->w_qkv, w->s_qkv, qkv, qkv_cols, nullptr, T, qkv_cols, d,
                                 HB_EPI_STORE, s, &norm_x));
     HB_STEP(2, kv_append_launch(ctx, qkv, T, plan->row_pos, plan->slot_mapping, rope, max_pos, dm, q, k_cache,
                                 v_cache, num_pages, s));
     HB_STEP(3, attention_launch(ctx, q, k_cache, v_cache, num_pages, *plan, dm, max_kv_len, o, aws,
-                                lw.total - lw.attn, s));
+                                lw.total - lw.attn, s, true));
     HB_STEP(4, quant_rows_launch(ctx, o, oq, so, T, hd, nullptr, nullptr, 0, s));
     st = gemm_e4m3_launch(ctx, oq, hd, so, w->w_o, w->s_o, h, d, x_in, T, d, hd, HB_EPI_RESIDUAL, s, &norm_h_out,
                           &split_o);
@@ -178,12 +182,12 @@ extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_
     if (st != HB_OK) return st;
     return mark(HB_LAYER_STAGES);
   }
-  HB_STEP(0, row_sumsq_launch(ctx, x_in, ss_x, T, d, split_o.flags, 2 * n_flags, s));
+  HB_STEP(0, row_sumsq_launch(ctx, x_in, ss_x, T, d, split_o.flags, n_zero, s));
   HB_STEP(1, gemm_launch(ctx, x_in, d, w->w_qkv, qkv, qkv_cols, nullptr, T, qkv_cols, d, HB_EPI_STORE, s, &norm_x));
   HB_STEP(2, kv_append_launch(ctx, qkv, T, plan->row_pos, plan->slot_mapping, rope, max_pos, dm, q, k_cache, v_cache,
                               num_pages, s));
   HB_STEP(3, attention_launch(ctx, q, k_cache, v_cache, num_pages, *plan, dm, max_kv_len, o, aws,
-                              lw.total - lw.attn, s));
+                              lw.total - lw.attn, s, true));
   HB_STEP(4, gemm_launch(ctx, o, hd, w->w_o, h, d, x_in, T, d, hd, HB_EPI_RESIDUAL, s, &norm_h_out, &split_o));
   HB_STEP(5, HB_OK);  // rmsnorm2: statistics came from the o projection, scaling goes to gate/up
   HB_STEP(6, gemm_launch(ctx, h, d, w->w_gu, a, fp, nullptr, T, 2 * fp, d, HB_EPI_SWIGLU, s, &norm_h_in));

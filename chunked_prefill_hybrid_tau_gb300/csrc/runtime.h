@@ -24,9 +24,9 @@ hb_status device_context(DeviceCtx* ctx);
 hb_status cuda_status(cudaError_t e, const char* what);
 hb_status launch_status(const char* what);
 
-// 2D tensor map of bf16 (elem_bytes 2) or byte (elem_bytes 1: E4M3 codes)
-// elements: `outer` rows of `inner` elements, rows `row_stride_bytes` apart;
-// box of box_inner x box_outer elements.
+// 2D tensor map of bf16 (elem_bytes 2), byte (elem_bytes 1: E4M3 codes) or
+// fp32 (elem_bytes 4) elements: `outer` rows of `inner` elements, rows
+// `row_stride_bytes` apart; box of box_inner x box_outer elements.
 hb_status encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128,
                          int elem_bytes = 2);
@@ -112,8 +112,9 @@ struct GemmSplit {
   int* flags = nullptr;
 };
 bool gemm_split_k(int N, int K, int epi);
-// Whether a projection runs on 256 x 256 CTA-pair tiles (tcgen05 cta_group::2).
-bool gemm_use_pair(int M, int N, int epi, bool split);
+// Tile width of CTA-pair tiles (tcgen05 cta_group::2, 256 rows) for a
+// projection, or 0 for one-CTA tiles.
+int gemm_pair_bn(int M, int N, int epi, bool split, int num_sms);
 size_t gemm_split_part_bytes(int M, int N);  // fp32 partial tiles
 int gemm_split_flags(int M, int N);          // arrival counters (ints)
 
@@ -143,8 +144,13 @@ hb_status gemm_launch(const DeviceCtx& ctx, const void* A, int lda, const void* 
 hb_status row_sumsq_launch(const DeviceCtx& ctx, const void* x, float* ss, int rows, int d, int* zero, int n_zero,
                            cudaStream_t stream);
 size_t attention_workspace_bytes(const hb_layer_dims& dims, int max_seqs, int max_kv_len);
+// Bytes at the start of the attention workspace that must be zero when the
+// attention kernels start (work and combine counters).
+size_t attention_counter_bytes(const hb_layer_dims& dims, int n_seqs);
+// counters_zeroed: the caller has zeroed the counters on the stream (the
+// layer does it in its first kernel), else they are cleared here.
 hb_status attention_launch(const DeviceCtx& ctx, const void* q, const void* k_cache, const void* v_cache,
                            int num_pages, const hb_device_plan& plan, const hb_layer_dims& dims, int max_kv_len,
-                           void* out, void* ws, size_t ws_bytes, cudaStream_t stream);
+                           void* out, void* ws, size_t ws_bytes, cudaStream_t stream, bool counters_zeroed);
 
 }  // namespace hb
