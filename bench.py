@@ -35,6 +35,7 @@ if ROOT not in sys.path:
 
 METRIC = "hybrid-iteration tokens/s and ms/iter vs token budget; % of per-iteration roofline"
 WORKLOAD = "mistral7b_layer_tau512"
+MIN_CLOCK_S = 0.3  # seconds of layer steps the clock sampler sees at least (20 ms period)
 
 
 def parse():
@@ -201,7 +202,7 @@ class ClockSampler:
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             self.p = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={self.QUERY}",
-                                       "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                       "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
                                       stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.p = None
@@ -390,7 +391,9 @@ def run_hb(args, world, rank, local):
     stream.synchronize()
     hb.hb_check_status(stream)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # the clock sampler runs from here through the end-to-end pass
     clocks = ClockSampler(local)
+    t_clock0 = time.perf_counter()
     barrier(world)
     torch.cuda.synchronize(dev)
     start.record(stream)
@@ -399,7 +402,6 @@ def run_hb(args, world, rank, local):
     end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
-    clk = clocks.stop()
     hb.hb_check_status(stream)
     t_dev = max_over_ranks(start.elapsed_time(end) / 1e3, world)
     T = runner.n_rows
@@ -429,7 +431,7 @@ def run_hb(args, world, rank, local):
     x_in = [torch.empty_like(x_dev) for _ in range(2)]
     y_out = [torch.empty_like(x_dev) for _ in range(2)]
     up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    e_steps = max(1, min(args.steps, 1000))
+    e_steps = max(1, args.steps)
 
     def e2e_run(n, e0=None):
         if n == 0:
@@ -465,7 +467,9 @@ def run_hb(args, world, rank, local):
         if n >= 2:
             stream.wait_event(fetched[(n - 2) % 2])
 
-    e2e_run(min(args.warmup, 5))
+    # warm-up of the copy streams and pinned buffers, so the timed steps are
+    # steady state (fill and drain of the copy pipeline are one step each)
+    e2e_run(max(args.warmup, 10))
     torch.cuda.synchronize(dev)
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -475,6 +479,13 @@ def run_hb(args, world, rank, local):
     torch.cuda.synchronize(dev)
     barrier(world)
     hb.hb_check_status(stream)
+    # short runs: keep the layer running (untimed) until the sampler has seen
+    # at least MIN_CLOCK_S of it, so the clock record is never empty
+    while time.perf_counter() - t_clock0 < MIN_CLOCK_S:
+        for _ in range(50):
+            layer(runner.step(stream), x_dev, out_dev)
+        torch.cuda.synchronize(dev)
+    clk = clocks.stop()
     out_host = out_host[0]
     t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
     e2e = {"value": world * T * e_steps / t_e2e, "unit": "tokens/s",
@@ -635,29 +646,85 @@ def run_sweep(args, taus=None, emit=True):
     return records
 
 
+def select_tau(profile, slo_ms):
+    """The pages' calibration rule (profile T(n), take the largest n with
+    T(n) <= T*) on a measured profile [(tau, iteration_ms), ...] in
+    increasing tau.  Returns (tau or None, knee) where the knee is the first
+    tau whose time is 10% above the smallest budget's."""
+    fits = [t for t, ms in profile if ms <= slo_ms]
+    base = profile[0][1]
+    knee = next((t for t, ms in profile if ms >= 1.1 * base), None)
+    return (max(fits) if fits else None), knee
+
+
 def run_calibrate(args):
     """The scheduling method's tau calibration (the Sarathi-Serve reading notes'
-    profiling step): measure the iteration time T(tau) over a range of token
-    budgets, then take the largest tau whose time fits the per-iteration SLO.
-    T(tau) is the measured single-layer time times --layers (the layers are
-    identical in shape).  Prints the profile and one summary line."""
+    profiling step): measure the iteration time T(tau) of a --layers-deep
+    model (distinct random weights and KV pools per layer, every layer through
+    hb_layer_forward) over a range of token budgets, then take the largest
+    tau whose time fits the per-iteration SLO.  The batch at each tau is 64
+    decodes with contexts uniform in [512, 8192] plus a chunk of tau - 64
+    tokens.  Prints the profile and one summary line."""
+    import torch
+    import chunked_prefill_hybrid_tau_gb300 as hb
+    from workloads import device as wd
+    lib = hb.lib()
     taus = [64, 128, 192, 256, 384, 512, 640, 768, 1024, 1536, 2048, 3072, 4096]
-    recs = run_sweep(args, taus, emit=False)
-    prof = [r for r in recs if r["sweep"] == "tau"]
-    c_star = [r for r in recs if r["sweep"] == "c_star"][0]
-    for r in prof:
-        print(json.dumps({"calibrate": "profile", "weights": args.weights, "tau": r["tau"], "layer_ms": r["ms_per_step"],
-                          "iteration_ms": r["ms_per_step"] * args.layers, "tokens_per_s": r["tokens_per_s"],
-                          "roofline_frac": r["roofline_frac"]}), flush=True)
-    fits = [r for r in prof if r["ms_per_step"] * args.layers <= args.calibrate]
-    base = prof[0]["ms_per_step"]
-    knee = next((r["tau"] for r in prof if r["ms_per_step"] >= 1.1 * base), None)
-    best = max(fits, key=lambda r: r["tau"]) if fits else None
-    print(json.dumps({"calibrate": "tau", "slo_ms": args.calibrate, "layers": args.layers,
-                      "tau": best["tau"] if best else None,
-                      "iteration_ms": best["ms_per_step"] * args.layers if best else None,
-                      "tau_knee_10pct": knee, "c_star_tokens": c_star["c_star_tokens"],
-                      "decodes": 64, "weights": args.weights}), flush=True)
+    L = args.layers
+    w = make_workload(max(taus), 64)
+    st, dims = w.state, w.dims
+    max_pos = 8192 + max(taus) + 1
+    fmt = args.weights
+    gen = wd.device_generator(77)
+    layers = [wd.layer_weights_random(dims, 7700 + l, fmt=fmt) for l in range(L)]
+    shape = (st.num_pages, dims.n_kv, 16, dims.d_head)
+    pools = [(wd.randn_bf16(shape, gen), wd.randn_bf16(shape, gen)) for _ in range(L)]
+    rope = wd.rope_table_device(max_pos, dims)
+    x_all = wd.randn_bf16((max(taus), dims.d_model), gen)
+    profile = []
+    for tau in taus:
+        stream = torch.cuda.Stream()
+        runner = PlanRunner(lib, st, tau, tau, "cuda")
+        ws = wd.workspace(hb.hb_layer_workspace_bytes(dims, runner.row_cap, runner.seq_cap, max_pos))
+        x = x_all[:tau].clone()
+        ds = hb.dims_struct(dims)
+        wstructs = [lw.struct() for lw in layers]
+
+        def iteration():
+            dp = runner.step(stream)
+            for l in range(L):
+                k, v = pools[l]
+                rc = lib.hb_layer_forward(C.byref(wstructs[l]), C.byref(ds), C.byref(dp), C.c_void_p(rope.data_ptr()),
+                                          max_pos, C.c_void_p(x.data_ptr()), C.c_void_p(x.data_ptr()),
+                                          C.c_void_p(k.data_ptr()), C.c_void_p(v.data_ptr()), int(k.shape[0]),
+                                          max_pos, C.c_void_p(ws.data_ptr()), ws.numel(),
+                                          C.c_void_p(stream.cuda_stream), None)
+                if rc != 0:
+                    raise RuntimeError(lib.hb_last_error().decode())
+
+        for _ in range(3):
+            iteration()
+        stream.synchronize()
+        n = max(5, min(args.steps, 20))
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(n):
+            iteration()
+        s1.record(stream)
+        stream.synchronize()
+        hb.hb_check_status(stream)
+        ms = s0.elapsed_time(s1) / n
+        T = runner.n_rows
+        profile.append((tau, ms))
+        print(json.dumps({"calibrate": "profile", "weights": fmt, "layers": L, "tau": tau, "rows": T,
+                          "iteration_ms": ms, "layer_ms": ms / L, "tokens_per_s": T / (ms / 1e3)}), flush=True)
+        del ws
+    c_star = [r for r in run_sweep(args, [64], emit=False) if r["sweep"] == "c_star"][0]
+    tau, knee = select_tau(profile, args.calibrate)
+    best = dict(profile).get(tau)
+    print(json.dumps({"calibrate": "tau", "slo_ms": args.calibrate, "layers": L, "tau": tau, "iteration_ms": best,
+                      "tau_knee_10pct": knee, "c_star_tokens": c_star["c_star_tokens"], "decodes": 64,
+                      "weights": fmt}), flush=True)
     return 0
 
 
@@ -673,7 +740,7 @@ def run_chunk_study(args):
     dims = wl.MISTRAL
     lw = wd.layer_weights_random(dims, 4100)
     gen = wd.device_generator(41)
-    for P in (8192, 32768):
+    for P in (8192, 32768, 65536):
         x = wd.randn_bf16((P, dims.d_model), gen)
         out = torch.empty_like(x)
         rope = wd.rope_table_device(P + 1, dims)

@@ -47,3 +47,22 @@ def test_e4m3_weight_bytes_and_roofline(plan):
     assert t16 - t8 == pytest.approx(proj / 2, rel=1e-12)
     # memory-bound (infinite FLOP rate): bytes over bandwidth
     assert costs.roofline_time(s1, 1e30, 1000.0, f8=True) == pytest.approx(b1 / 1e12, rel=1e-12)
+
+
+# ----------------------------------------------------------------------------
+# tau calibration (the scheduling method's profiling step: largest budget n
+# with T(n) <= T*, Sarathi-Serve reading notes section 3.3)
+# ----------------------------------------------------------------------------
+def test_select_tau_takes_the_largest_budget_within_the_slo():
+    import bench
+    # flat up to 512, then linear: T(n) = 10 ms below the knee, 10 + (n - 512) / 100 above
+    prof = [(n, 10.0 if n <= 512 else 10.0 + (n - 512) / 100.0) for n in (64, 128, 256, 512, 1024, 2048, 4096)]
+    assert bench.select_tau(prof, 10.0) == (512, 1024)      # every budget up to the knee fits
+    assert bench.select_tau(prof, 15.2) == (1024, 1024)     # 1024 -> 15.12 ms fits, 2048 -> 25.36 does not
+    assert bench.select_tau(prof, 1e9) == (4096, 1024)
+    assert bench.select_tau(prof, 5.0) == (None, 1024)      # nothing fits a tighter SLO
+    # the knee is the first budget 10% above the smallest budget's time
+    assert bench.select_tau([(64, 1.0), (128, 1.05), (256, 1.1), (512, 2.0)], 10.0) == (512, 256)
+    assert bench.select_tau([(64, 1.0), (128, 1.0)], 10.0) == (128, None)
+    # a non-monotone profile still returns the largest fitting budget
+    assert bench.select_tau([(64, 1.0), (128, 3.0), (256, 2.0)], 2.5)[0] == 256

@@ -5,8 +5,11 @@ through hb_layer_forward and the logits through hb_final_logits (GPU).
 The oracle follows sampled decode rows through every layer from the original
 inputs: a decode row's output depends only on its own hidden state and its
 own KV (prior context + its new token), so the chunk rows, which the CPU
-could not afford at these sizes, are not needed for it.  The last chunk
-row's logits are checked for finiteness.
+could not afford through every layer, are not needed for it.  For the
+32-layer model, layers 0 and 1 are also compared on every row (all 64 decode
+rows and the 1984 chunk rows), each fed the GPU's actual input to that layer
+and its KV pools as they were before it, at the single-layer bounds.  The
+last chunk row's logits are checked for finiteness.
 
 Tolerance of a deep stack: the random-weight stack amplifies any per-layer
 rounding, so the bound is derived from the arithmetic itself: the oracle is
@@ -23,7 +26,7 @@ import oracle.layer as ol
 import oracle.plan as op
 import workloads as wl
 from workloads import device as wd
-from tests.gpu_harness import assert_close
+from tests.gpu_harness import assert_close, assert_layer
 
 pytestmark = pytest.mark.gpu
 
@@ -34,12 +37,16 @@ if not torch.cuda.is_available():
 import chunked_prefill_hybrid_tau_gb300 as hb  # noqa: E402
 
 
-def run_model(dims, tau, dec_ctx, prompt_len, sample, vocab, seed):
+def run_model(dims, tau, dec_ctx, prompt_len, sample, vocab, seed, full_layers=()):
+    """full_layers: layers whose every row (decode and chunk) is compared with
+    the oracle run on the GPU's own input to that layer and the layer's KV
+    pools as they were before it."""
     rng = np.random.default_rng(seed)
     st = wl.make_state(rng, dims, [int(c) for c in dec_ctx], [(prompt_len, 0)],
                        slack_pages=wl.pages_for(tau) + len(dec_ctx) + 8, fill_kv=False)
-    hp = hb.hb_plan_batch([r.done for r in st.decodes], [r.pages for r in st.decodes], [prompt_len], [0], [[]],
-                          st.free_pool, tau, tau)
+    plan_args = ([r.done for r in st.decodes], [r.pages for r in st.decodes], [prompt_len], [0], [[]],
+                 st.free_pool, tau, tau)
+    hp = hb.hb_plan_batch(*plan_args)
     T = hp.n_rows
     n_dec = len(dec_ctx)
     assert T == tau and list(hp.pf_take) == [tau - n_dec]
@@ -60,9 +67,14 @@ def run_model(dims, tau, dec_ctx, prompt_len, sample, vocab, seed):
     remap = {pg: k for k, pg in enumerate(sample_pages)}
     idx = torch.tensor(sample_pages, device="cuda")
     host_kv = [(wd.to_numpy(k[idx]), wd.to_numpy(v[idx])) for k, v in pools]
+    full = {}
     for l in range(dims.n_layers):
         k, v = pools[l]
+        if l in full_layers:
+            full[l] = [wd.to_numpy(x), wd.to_numpy(k), wd.to_numpy(v)]
         hb.hb_layer_forward(layers[l], dims, dp, rope, max_kv + 1, x, x, k, v, max_kv, ws)
+        if l in full_layers:
+            full[l].append(wd.to_numpy(x))
     hb.hb_check_status()
     rows = torch.tensor(list(range(n_dec)) + [T - 1], dtype=torch.int32, device="cuda")
     logits = None
@@ -99,6 +111,16 @@ def run_model(dims, tau, dec_ctx, prompt_len, sample, vocab, seed):
         assert gmax <= max(2e-2, 2.0 * emax), f"{what}: max abs {gmax:.4g} beyond 2 x bf16-storage {emax:.4g}"
 
     check_stack(gpu_rows, xr, xe, f"{dims.n_layers}-layer hidden state of sampled decode rows")
+    if full_layers:
+        # every row of the chosen layers (the chunk rows included), each layer
+        # fed its actual GPU input and KV pools
+        o_full = op.plan_batch(*plan_args, max_pages=hp.max_pages)
+        for l in full_layers:
+            x_in, kp, vp, x_out = full[l]
+            w = wd.host_layer_weights(dims, seed * 1000 + l)
+            ref = ol.layer_forward(w, dims, o_full, x_in, kp.copy(), vp.copy(), cos, sin)
+            emu, parts = ol.layer_forward(w, dims, o_full, x_in, kp, vp, cos, sin, storage="bf16", return_parts=True)
+            assert_layer(x_out, ref, emu, parts["h"], f"layer {l}, all {T} rows")
     if vocab:
         g_f_h = np.ones(dims.d_model, np.float32)
         w_lm_h = wd.to_numpy(w_lm)
@@ -114,7 +136,7 @@ def run_model(dims, tau, dec_ctx, prompt_len, sample, vocab, seed):
 def test_mistral_32_layers_lm_head_tau2048():
     rng = np.random.default_rng(2)
     ctx = rng.integers(1024, 8192, size=64, endpoint=True)
-    run_model(wl.MISTRAL_32L, 2048, ctx, 8192, sample=[0, 21, 63], vocab=32000, seed=2)
+    run_model(wl.MISTRAL_32L, 2048, ctx, 8192, sample=[0, 21, 63], vocab=32000, seed=2, full_layers=(0, 1))
 
 
 def test_yi34b_60_layers_tau1024():
