@@ -71,7 +71,7 @@ struct Params {
   GemmNorm norm;  // folded RMSNorm: row scaling in (STORE, SWIGLU), row statistics out (RESIDUAL)
   int ksplit;     // 1, or 2: each tile's K range in two halves (RESIDUAL only)
   float* part;    // ksplit 2: fp32 partial tiles [tile][half][BN][BM] (column-major)
-  int* flags;     // ksplit 2: per (tile, 32-row slab) arrival counters, zero between launches
+  int* flags;     // ksplit 2: per 128-row tile arrival counters (index 4 x tile), zero at launch
   const float* sa;  // E4M3 operands: per-row scales of A [M] and of B [N] (null for bf16)
   const float* sb;
 };
@@ -189,6 +189,39 @@ __device__ __forceinline__ void scale_cols(uint32_t (&r)[32], float rowf, const 
   }
 }
 
+// Split K: the two halves of a 128-row tile exchange partial sums by
+// columns.  Each CTA has written its fp32 partial of the other half's
+// columns; here it arrives on the tile's counter and waits (bounded) for the
+// partner's arrival, after which the partner's partial of its own columns is
+// in place.  Own + partner is commutative, so either half's sum has the same
+// bits.  The counters must be zero at launch (the layer's first kernel
+// clears them); both halves of a tile run in the same round of the
+// persistent grid (consecutive units on an even number of clusters).
+__device__ __forceinline__ bool split_exchange(const Params& p, int stile, bool leader, volatile int* ep_flag,
+                                               volatile int* abort_flag) {
+  __threadfence();
+  named_barrier_sync(1, 128);
+  if (leader) {
+    int* arrive = p.flags + stile * 4;
+    atomicAdd(arrive, 1);
+    int ok = 1;
+    const uint64_t t0 = globaltimer();
+    while (*reinterpret_cast<volatile int*>(arrive) < 2) {
+      if (*abort_flag || globaltimer() - t0 > kWaitTimeoutNs) {
+        if (!*abort_flag) flag_error(p.status, kStatusTimeout);
+        *abort_flag = 1;
+        ok = 0;
+        break;
+      }
+      __nanosleep(32);
+    }
+    __threadfence();
+    *ep_flag = ok;
+  }
+  named_barrier_sync(1, 128);
+  return *ep_flag != 0;
+}
+
 // Epilogue of one 128 x BN accumulator block in TMEM (t_base: this warp's
 // 32 lanes) for output row `row` of the warp's thread: SwiGLU, residual (with
 // the split-K exchange on 128-row tile `stile`, K half `half`) or store.
@@ -197,7 +230,7 @@ __device__ __forceinline__ void scale_cols(uint32_t (&r)[32], float rowf, const 
 template <int BN, int EPI, bool F8>
 __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_base, int row, bool row_ok, int rloc,
                                               int n_blk, int stile, int half, bool leader, volatile int* ep_flag,
-                                              float scale, float rowf) {
+                                              volatile int* abort_flag, float scale, float rowf) {
   if (EPI == HB_EPI_SWIGLU) {
 #pragma unroll 1
     for (int j = 0; j < BN / 128; ++j) {
@@ -233,42 +266,31 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_base, 
       }
     }
   } else {
-    bool finish = true;  // this warp writes the output rows of the tile
+    // columns this CTA finishes: all, or with split K its half of them (the
+    // other half's partial goes to the partner CTA)
+    constexpr int NC = BN / 32;
+    int c_lo = 0, c_hi = NC;
     const float* other = nullptr;
+    bool finish = true;
     if (p.ksplit == 2) {
-      // Split K: publish this half's fp32 partial (column-major, so each
-      // store is one coalesced 128-byte line per warp); the CTA that
-      // arrives second for this 128-row tile adds the other half and
-      // finishes.  p0 + p1 is commutative, so the result does not depend on
-      // which half arrives last.
+      c_lo = half * (NC / 2);
+      c_hi = c_lo + NC / 2;
       float* mine = p.part + (static_cast<size_t>(stile) * 2 + half) * BN * BM;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < NC; ++c) {
+        if (c >= c_lo && c < c_hi) continue;
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_base + c * 32, r);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; ++j) mine[static_cast<size_t>(c * 32 + j) * BM + rloc] = __uint_as_float(r[j]);
       }
-      __threadfence();
-      named_barrier_sync(1, 128);
-      if (leader) {
-        int* flag = p.flags + stile * 4;  // one counter per 128-row tile
-        const int last = atomicAdd(flag, 1) == 1;
-        if (last) *flag = 0;
-        *ep_flag = last;
-      }
-      named_barrier_sync(1, 128);
-      finish = *ep_flag != 0;
-      if (finish) {
-        __threadfence();
-        other = p.part + (static_cast<size_t>(stile) * 2 + (1 - half)) * BN * BM;
-      }
+      finish = split_exchange(p, stile, leader, ep_flag, abort_flag);
+      other = p.part + (static_cast<size_t>(stile) * 2 + (1 - half)) * BN * BM;
     }
     if (finish && EPI == HB_EPI_RESIDUAL) {
       // software-pipelined: the residual (and the other half's partial)
       // of chunk c + 1 is in flight while chunk c is combined and stored
-      constexpr int NC = BN / 32;
       uint4 rv[2][4];
       float ov[2][32];
       auto fetch = [&](int c, int b) {
@@ -283,11 +305,14 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_base, 
           for (int j = 0; j < 32; ++j) ov[b][j] = __ldcg(other + static_cast<size_t>(c * 32 + j) * BM + rloc);
         }
       };
-      fetch(0, 0);
+      const int n_own = c_hi - c_lo;
+      fetch(c_lo, 0);
 #pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        const int b = c & 1;
-        if (c + 1 < NC) fetch(c + 1, b ^ 1);
+      for (int i = 0; i < NC; ++i) {
+        if (i >= n_own) break;
+        const int c = c_lo + i;
+        const int b = i & 1;
+        if (i + 1 < n_own) fetch(c + 1, b ^ 1);
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_base + c * 32, r);
         tmem_ld_wait();
@@ -326,10 +351,10 @@ constexpr int kSlabBytes = 128 * 128;
 //   STORE / F32 / SWIGLU: outputs into 128-byte slabs, then TMA stores;
 //   RESIDUAL: the residual tile arrives by TMA into the slabs (issued as soon
 //   as the accumulator is ready) and is overwritten in place by the outputs;
-//   with split K, this half's fp32 partial goes out (column-major, coalesced)
-//   and the CTA that arrives second for the tile fetches the other half's
-//   partial with one bulk copy and finishes the tile (p0 + p1 is commutative,
-//   so the result does not depend on which half arrives last).
+//   with split K each of the tile's two CTAs finishes half of the columns:
+//   it writes its fp32 partial of the other half (column-major, coalesced),
+//   meets the partner on the tile's counter and fetches the partner's partial
+//   of its own half with one bulk copy.
 // Called by the 128 epilogue threads; `leader` is one of them.  Returns
 // false when a bounded wait expired.
 template <int BN, int EPI, bool F8>
@@ -338,61 +363,60 @@ __device__ __forceinline__ bool epilogue_last(const Params& p, const CUtensorMap
                                               int m0, int row, bool row_ok, int rloc, int n_blk, int stile, int half,
                                               bool leader, float scale, float rowf, volatile int* abort_flag) {
   if constexpr (EPI == HB_EPI_RESIDUAL) {
-    constexpr int NS = BN / 64;  // 64-column bf16 slabs
-    static_assert(NS * kSlabBytes + (BN * BM * 4) <= 192 * 1024, "ring too small for the split epilogue");
-    uint8_t* part_smem = ring + NS * kSlabBytes;
+    // the columns this CTA finishes: all, or with split K its half (the
+    // other half's partial goes to the partner CTA, whose partial of these
+    // columns comes in by one bulk copy)
+    constexpr int NS_ALL = BN / 64;  // 64-column bf16 slabs
+    const bool split = p.ksplit == 2;
+    const int ns = split ? NS_ALL / 2 : NS_ALL;
+    const int cl0 = split ? half * (BN / 2) : 0;  // first accumulator column finished here
+    static_assert(NS_ALL * kSlabBytes + (BN / 2) * BM * 4 <= 192 * 1024, "ring too small for the split epilogue");
+    uint8_t* part_smem = ring + NS_ALL * kSlabBytes;
     if (leader) {
-      mbar_arrive_expect_tx(&ep_bar[0], NS * kSlabBytes);
-      for (int s = 0; s < NS; ++s) tma_load_2d(ring + s * kSlabBytes, tmR, &ep_bar[0], n_blk * BN + s * 64, m0);
+      mbar_arrive_expect_tx(&ep_bar[0], ns * kSlabBytes);
+      for (int s = 0; s < ns; ++s) tma_load_2d(ring + s * kSlabBytes, tmR, &ep_bar[0], n_blk * BN + cl0 + s * 64, m0);
     }
-    bool finish = true;
-    if (p.ksplit == 2) {
+    if (split) {
       float* mine = p.part + (static_cast<size_t>(stile) * 2 + half) * BN * BM;
+      const int o0 = (1 - half) * (BN / 2);  // the partner's columns
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < BN / 64; ++c) {
         uint32_t r[32];
-        tmem_ld_32x32b_x32(t_base + c * 32, r);
+        tmem_ld_32x32b_x32(t_base + o0 + c * 32, r);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) mine[static_cast<size_t>(c * 32 + j) * BM + rloc] = __uint_as_float(r[j]);
+        for (int j = 0; j < 32; ++j) mine[static_cast<size_t>(o0 + c * 32 + j) * BM + rloc] = __uint_as_float(r[j]);
       }
-      __threadfence();
-      named_barrier_sync(1, 128);
-      if (leader) {
-        int* flag = p.flags + stile * 4;  // one counter per 128-row tile
-        const int last = atomicAdd(flag, 1) == 1;
-        if (last) {
-          *flag = 0;
-          __threadfence();
-          fence_proxy_async_global();
-          const float* other = p.part + (static_cast<size_t>(stile) * 2 + (1 - half)) * BN * BM;
-          constexpr uint32_t kPiece = BN * BM * 4 / 4;
-          mbar_arrive_expect_tx(&ep_bar[1], 4 * kPiece);
-          for (int i = 0; i < 4; ++i)
-            bulk_load(part_smem + i * kPiece, reinterpret_cast<const uint8_t*>(other) + i * kPiece, kPiece, &ep_bar[1]);
-        }
-        *ep_flag = last;
+      const bool ok = split_exchange(p, stile, leader, ep_flag, abort_flag);
+      if (leader && ok) {
+        fence_proxy_async_global();
+        const float* other = p.part + (static_cast<size_t>(stile) * 2 + (1 - half)) * BN * BM + cl0 * BM;
+        constexpr uint32_t kPiece = (BN / 2) * BM * 4 / 2;
+        mbar_arrive_expect_tx(&ep_bar[1], 2 * kPiece);
+        for (int i = 0; i < 2; ++i)
+          bulk_load(part_smem + i * kPiece, reinterpret_cast<const uint8_t*>(other) + i * kPiece, kPiece, &ep_bar[1]);
       }
-      named_barrier_sync(1, 128);
-      finish = *ep_flag != 0;
+      if (!ok) {
+        mbar_wait(&ep_bar[0], 0, nullptr, nullptr);  // the residual copies land before the CTA leaves
+        return false;
+      }
     }
-    // the residual copies land before anything else happens to the ring
     if (!mbar_wait(&ep_bar[0], 0, abort_flag, p.status)) return false;
-    if (!finish) return true;
-    if (p.ksplit == 2 && !mbar_wait(&ep_bar[1], 0, abort_flag, p.status)) return false;
-    const float* other = reinterpret_cast<const float*>(part_smem);
+    if (split && !mbar_wait(&ep_bar[1], 0, abort_flag, p.status)) return false;
+    const float* other = reinterpret_cast<const float*>(part_smem);  // partner's partial of this CTA's columns
 #pragma unroll 1
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < ns; ++s) {
       uint8_t* slab = ring + s * kSlabBytes;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t r[32];
-        const int cl = s * 64 + h * 32;  // accumulator column within the tile
+        const int cl = cl0 + s * 64 + h * 32;  // accumulator column within the tile
         tmem_ld_32x32b_x32(t_base + cl, r);
         tmem_ld_wait();
-        if (p.ksplit == 2) {
+        if (split) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fadd_rn(__uint_as_float(r[j]), other[(cl + j) * BM + rloc]));
+          for (int j = 0; j < 32; ++j)
+            r[j] = __float_as_uint(__fadd_rn(__uint_as_float(r[j]), other[(cl - cl0 + j) * BM + rloc]));
         }
         const int col = n_blk * BN + cl;
         if constexpr (F8) scale_cols(r, rowf, p.sb, col, p.N);
@@ -421,7 +445,7 @@ __device__ __forceinline__ bool epilogue_last(const Params& p, const CUtensorMap
     fence_proxy_async_smem();
     named_barrier_sync(1, 128);
     if (leader) {
-      for (int s = 0; s < NS; ++s) tma_store_2d(tmC, ring + s * kSlabBytes, n_blk * BN + s * 64, m0);
+      for (int s = 0; s < ns; ++s) tma_store_2d(tmC, ring + s * kSlabBytes, n_blk * BN + cl0 + s * 64, m0);
       bulk_commit_group();
     }
     return true;
@@ -692,8 +716,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         wu.tile, wu.half, leader, scale, rowf, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) break;
       } else {
-        epilogue_tile<BN, EPI, F8>(p, t_base, row, row_ok, rloc, n_blk, wu.tile, wu.half, leader, ep_flag, scale,
-                                   rowf);
+        epilogue_tile<BN, EPI, F8>(p, t_base, row, row_ok, rloc, n_blk, wu.tile, wu.half, leader, ep_flag, abort_flag,
+                                   scale, rowf);
       }
       tc_fence_before();
       __syncwarp();
@@ -948,7 +972,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                           wu.n_blk, stile, wu.half, leader_thread, scale, rowf, abort_flag);
         } else {
           epilogue_tile<BN, EPI, F8>(p, t_base, row, row_ok, rloc, wu.n_blk, stile, wu.half, leader_thread, ep_flag,
-                                     scale, rowf);
+                                     abort_flag, scale, rowf);
         }
       }
       tc_fence_before();

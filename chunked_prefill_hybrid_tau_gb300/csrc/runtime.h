@@ -105,8 +105,9 @@ struct GemmNorm {
 };
 
 // Split-K workspace for RESIDUAL projections (fp32 partial tiles and arrival
-// counters; the counters must be zero at launch and are left zero).  Used
-// when gemm_split_k(N, K, epi) holds, which depends on the shape only.
+// counters; the counters must be zero at launch and are not cleared by the
+// kernel: the layer's first kernel zeroes them).  Used when
+// gemm_split_k(N, K, epi) holds, which depends on the shape only.
 struct GemmSplit {
   float* part = nullptr;
   int* flags = nullptr;
