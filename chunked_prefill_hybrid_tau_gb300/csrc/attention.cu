@@ -449,9 +449,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
 // Chunk rows (tensor cores, latency-bound per tile) and decode rows (HBM
 // streaming) cannot share an SM (each kernel fills its shared memory), so
 // when the plan's hints give both kinds of work the SMs are split and the
-// two persistent kernels run at the same time on disjoint SMs: the chunk
-// kernel on a side stream forked from and joined back into the caller's
-// stream.  Cost model (GB300, measured):
+// two persistent kernels run at the same time on disjoint SMs, both on the
+// caller's stream: the decode kernel is a programmatic dependent of the
+// chunk kernel and starts beside it.  Cost model (GB300, measured):
 //   chunk : U = 128-row tiles x q heads units of about kUnitUs + (key blocks
 //           per tile) x kBlockUs each (key blocks over all tiles ~ pairs /
 //           128^2 + rows / 128), taken heaviest first, so on n SMs the
