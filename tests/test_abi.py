@@ -45,7 +45,7 @@ def test_argument_errors_are_synchronous(lib):
     assert st == L.HB_ERR_INVALID_ARG
     assert b"null" in lib.hb_last_error()
     st = lib.hb_gemm(C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), None, 128, 100, 128, 0, None)
-    assert st == L.HB_ERR_INVALID_ARG  # N not a multiple of 64
+    assert st == L.HB_ERR_INVALID_ARG  # N not a multiple of 8
     bad = L.hb_layer_dims(256, 4, 3, 64, 688, 16, 1e-6, 1e4)  # n_q % n_kv != 0
     st = lib.hb_kv_append(None, 0, None, None, None, 1, C.byref(bad), None, None, None, 1, None)
     assert st == L.HB_ERR_INVALID_ARG
@@ -63,3 +63,22 @@ def test_workspace_sizes(lib):
     assert a > 0 and a % 256 == 0
     w = lib.hb_layer_workspace_bytes(C.byref(ds), 512, 33, 4097)
     assert w > a + 512 * 4096 * 2 * 5
+
+
+def test_idle_iteration_is_a_no_op(lib):
+    """An iteration with nothing planned (no decodes, no prompt tokens) is
+    accepted and returns before any device work, so it runs without a GPU;
+    the same call with one row would need the device."""
+    import workloads as wl
+    ds = B.dims_struct(wl.TINY)
+    fake = C.c_void_p(4096)  # never dereferenced
+    w = L.hb_layer_weights(fake, fake, fake, fake, None, None, None, None, L.HB_WEIGHTS_BF16)
+    plan = L.hb_device_plan(0, 0, 1, None, None, None, None, None, 0, 0, 0)
+    st = lib.hb_layer_forward(C.byref(w), C.byref(ds), C.byref(plan), fake, 64, fake, fake, fake, fake, 8, 64,
+                              None, 0, None, None)
+    assert st == L.HB_OK, lib.hb_last_error()
+    # a planned row with null plan arrays is an argument error, found before the device
+    plan.n_rows, plan.n_seqs = 1, 1
+    st = lib.hb_layer_forward(C.byref(w), C.byref(ds), C.byref(plan), fake, 64, fake, fake, fake, fake, 8, 64,
+                              None, 0, None, None)
+    assert st == L.HB_ERR_INVALID_ARG and b"null plan array" in lib.hb_last_error()

@@ -220,7 +220,10 @@ def attention_case(dims, dec_ctx, prefills, tau, chunk, seed, poison=True):
     return wd.to_numpy(out), ref, hp
 
 
-DEC_CTX = [0, 1, 15, 16, 17, 63, 64, 511, 512, 513, 1500, 2047]
+# decode contexts at page edges (16 keys) and at the 1024-key split edges: a
+# decode row's kv_len is its context + 1, so 1023 fills one split exactly,
+# 1024 leaves a one-key last split and 3072 a one-key fourth split
+DEC_CTX = [0, 1, 15, 16, 17, 63, 64, 511, 512, 513, 1023, 1024, 1500, 2047, 3072]
 
 
 # (8, 2, 128), (32, 8, 128), (6, 3, 128): chunk rows on CTA pairs (an even number
