@@ -187,8 +187,12 @@ __global__ void kv_append_kernel(const __nv_bfloat16* __restrict__ qkv, const in
       for (int j = 0; j < 4; ++j) {
         const float4 t2 = cs[j];  // (cos, sin) of element 2j and 2j+1
         const float2 x1 = unpack_bf16x2(aw[j]), x2 = unpack_bf16x2(bw[j]);
-        o1[j] = pack_bf16x2(x1.x * t2.x - x2.x * t2.y, x1.y * t2.z - x2.y * t2.w);
-        o2[j] = pack_bf16x2(x2.x * t2.x + x1.x * t2.y, x2.y * t2.z + x1.y * t2.w);
+        // each product and sum rounded to fp32 (no contraction), as in the
+        // fused QKV epilogue, so both paths give the same bits
+        o1[j] = pack_bf16x2(__fsub_rn(__fmul_rn(x1.x, t2.x), __fmul_rn(x2.x, t2.y)),
+                            __fsub_rn(__fmul_rn(x1.y, t2.z), __fmul_rn(x2.y, t2.w)));
+        o2[j] = pack_bf16x2(__fadd_rn(__fmul_rn(x2.x, t2.x), __fmul_rn(x1.x, t2.y)),
+                            __fadd_rn(__fmul_rn(x2.y, t2.z), __fmul_rn(x1.y, t2.w)));
       }
       __nv_bfloat16* dst;
       if (h < n_q) {

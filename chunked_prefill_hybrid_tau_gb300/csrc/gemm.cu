@@ -19,6 +19,11 @@ size_t gemm_split_part_bytes(int M, int N) {
 
 int gemm_split_flags(int M, int N) { return ((M + BM - 1) / BM) * ((N + 255) / 256) * 4; }
 
+bool gemm_rope_ok(int N, const hb_layer_dims& dims) {
+  // every 128- or 256-column tile holds whole heads
+  return N % 256 == 0 && (dims.d_head == 64 || dims.d_head == 128);
+}
+
 int gemm_pair_bn(int M, int N, int epi, bool split, int num_sms) {
   // CTA-pair tiles (256 rows) once M spans more than one 128-row tile: a
   // pair streams the same bytes per k-block as a one-CTA 128 x 128 tile for
@@ -27,7 +32,8 @@ int gemm_pair_bn(int M, int N, int epi, bool split, int num_sms) {
   // split-K residual projections take 256-wide tiles; a plain store picks
   // 192 or 256 for the fewest waves of pair tiles over the SM pairs.
   if (M <= BM) return 0;
-  if (epi == HB_EPI_SWIGLU || (epi == HB_EPI_RESIDUAL && split)) return N % kPairBN == 0 ? kPairBN : 0;
+  if (epi == HB_EPI_SWIGLU || epi == kEpiRope || (epi == HB_EPI_RESIDUAL && split))
+    return N % kPairBN == 0 ? kPairBN : 0;
   if (epi != HB_EPI_STORE) return 0;
   const int pm = (M + 2 * BM - 1) / (2 * BM);
   const int pairs = num_sms / 2;

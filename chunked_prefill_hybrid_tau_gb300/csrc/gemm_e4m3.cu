@@ -15,9 +15,21 @@ namespace hb {
 
 hb_status gemm_e4m3_launch(const DeviceCtx& ctx, const void* A, int lda, const float* sa, const void* B,
                            const float* sb, void* C, int ldc, const void* R, int M, int N, int K, int epi,
-                           cudaStream_t stream, const GemmNorm* norm, const GemmSplit* split) {
+                           cudaStream_t stream, const GemmNorm* norm, const GemmSplit* split, const GemmRope* rope) {
   if (split != nullptr && !gemm_split_k(N, K, epi)) split = nullptr;
   const int pbn = gemm_pair_bn(M, N, epi, split != nullptr, ctx.num_sms);
+  if (epi == kEpiRope) {
+    if (rope == nullptr || N % 256 != 0) {
+      set_error("gemm_e4m3: the fused RoPE epilogue needs its destinations and N %% 256 == 0");
+      return HB_ERR_UNSUPPORTED;
+    }
+    if (pbn != 0)
+      return launch_pair<kPairBN, kEpiRope, true>(ctx, A, lda, sa, B, sb, C, ldc, R, M, N, K, norm, split, stream,
+                                                  rope);
+    if (choose_bn(M, N, epi, ctx.num_sms) == 256)
+      return launch<256, kEpiRope, true>(ctx, A, lda, sa, B, sb, C, ldc, R, M, N, K, norm, split, stream, rope);
+    return launch<128, kEpiRope, true>(ctx, A, lda, sa, B, sb, C, ldc, R, M, N, K, norm, split, stream, rope);
+  }
   if (pbn != 0) {
     if (epi == HB_EPI_SWIGLU)
       return launch_pair<kPairBN, HB_EPI_SWIGLU, true>(ctx, A, lda, sa, B, sb, C, ldc, R, M, N, K, norm, split,

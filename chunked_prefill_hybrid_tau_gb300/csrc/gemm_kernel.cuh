@@ -74,6 +74,7 @@ struct Params {
   int* flags;     // ksplit 2: per 128-row tile arrival counters (index 4 x tile), zero at launch
   const float* sa;  // E4M3 operands: per-row scales of A [M] and of B [N] (null for bf16)
   const float* sb;
+  GemmRope rope;    // kEpiRope: destinations and RoPE table of the fused QKV epilogue
 };
 
 // Work unit u: tile u / ksplit, K half u % ksplit (k-blocks [kb0, kb1)).
@@ -370,8 +371,12 @@ __device__ __forceinline__ bool epilogue_last(const Params& p, const CUtensorMap
     const bool split = p.ksplit == 2;
     const int ns = split ? NS_ALL / 2 : NS_ALL;
     const int cl0 = split ? half * (BN / 2) : 0;  // first accumulator column finished here
-    static_assert(NS_ALL * kSlabBytes + (BN / 2) * BM * 4 <= 192 * 1024, "ring too small for the split epilogue");
+    constexpr int NP = 2 * NS_ALL;  // 32-column statistics parts of the tile
+    static_assert(NS_ALL * kSlabBytes + (BN / 2) * BM * 4 + BM * NP * 4 <= 192 * 1024,
+                  "ring too small for the split epilogue");
     uint8_t* part_smem = ring + NS_ALL * kSlabBytes;
+    // this thread's row statistics, collected here and written as one vector
+    float* ss_sm = reinterpret_cast<float*>(part_smem + (BN / 2) * BM * 4) + rloc * NP;
     if (leader) {
       mbar_arrive_expect_tx(&ep_bar[0], ns * kSlabBytes);
       for (int s = 0; s < ns; ++s) tma_load_2d(ring + s * kSlabBytes, tmR, &ep_bar[0], n_blk * BN + cl0 + s * 64, m0);
@@ -438,8 +443,20 @@ __device__ __forceinline__ bool epilogue_last(const Params& p, const CUtensorMap
           }
           *q = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        if (p.norm.ss_out != nullptr && row_ok && col < p.out_cols)
-          p.norm.ss_out[static_cast<size_t>(row) * p.norm.parts + col / 32] = ss;
+        ss_sm[2 * s + h] = ss;
+      }
+    }
+    if (p.norm.ss_out != nullptr && row_ok) {
+      // parts (n_blk BN + cl0) / 32 .. + 2 ns - 1 of the row, consecutive
+      const int col0 = n_blk * BN + cl0;
+      float* dst = p.norm.ss_out + static_cast<size_t>(row) * p.norm.parts + col0 / 32;
+      const bool vec = (p.norm.parts % 4) == 0 && (col0 / 32) % 4 == 0 && col0 + 2 * ns * 32 <= p.out_cols;
+      if (vec) {
+        for (int i = 0; i < 2 * ns; i += 4)
+          *reinterpret_cast<float4*>(dst + i) = make_float4(ss_sm[i], ss_sm[i + 1], ss_sm[i + 2], ss_sm[i + 3]);
+      } else {
+        for (int i = 0; i < 2 * ns; ++i)
+          if (col0 + i * 32 < p.out_cols) dst[i] = ss_sm[i];
       }
     }
     fence_proxy_async_smem();
@@ -527,6 +544,94 @@ __device__ __forceinline__ bool epilogue_last(const Params& p, const CUtensorMap
       bulk_commit_group();
     }
     return true;
+  }
+}
+
+// QKV epilogue with RoPE and the KV append (kEpiRope) for one 128 x BN
+// accumulator block whose columns are whole heads (BN a multiple of
+// d_head): per head and per 32 dimensions i of its first half, the thread's
+// row takes accumulator columns i and i + d_head/2, rounds them to bf16 as
+// the STORE epilogue would (the qkv activations), rotates q and k heads by
+// the row's position (rotate-half: x_i cos - x_{i+d/2} sin and
+// x_{i+d/2} cos + x_i sin, each product and sum rounded to fp32 as in
+// kv_append_kernel) and writes q to its row, K and V to the row's slot.
+// An out-of-range position skips the row; an out-of-range slot skips its
+// K/V; both set the status word (as kv_append_kernel).  Each thread writes
+// its own row in 16-byte pieces.  (Staging the rows in the idle ring and
+// writing whole rows per warp measured slower.)
+template <int BN, bool F8>
+__device__ __forceinline__ void epilogue_rope(const Params& p, uint32_t t_base, int row, bool row_ok, int n_blk,
+                                              float scale, float rowf) {
+  const GemmRope& rp = p.rope;
+  const int DH = rp.d_head, HALF = DH / 2;
+  const int pos = row_ok ? __ldg(rp.row_pos + row) : 0;
+  const int slot = row_ok ? __ldg(rp.slots + row) : 0;
+  const bool pos_ok = row_ok && pos >= 0 && pos < rp.max_pos;
+  const bool slot_ok = pos_ok && slot >= 0 && slot < rp.num_slots;
+  if (row_ok && (!pos_ok || slot >= rp.num_slots)) flag_error(p.status, kStatusIndex);
+  const int page = slot / 16, off = slot % 16;
+  const float sc = F8 ? 1.f : scale;
+  auto* q_out = static_cast<__nv_bfloat16*>(rp.q_out);
+  auto* kc = static_cast<__nv_bfloat16*>(rp.k_cache);
+  auto* vc = static_cast<__nv_bfloat16*>(rp.v_cache);
+#pragma unroll 1
+  for (int hb = 0; hb < BN; hb += DH) {
+    const int col0 = n_blk * BN + hb;  // the head's first column
+    const int head = col0 / DH;
+    const bool rot = head < rp.n_q + rp.n_kv;
+    __nv_bfloat16* dst = nullptr;
+    if (head < rp.n_q) {
+      dst = pos_ok ? q_out + (static_cast<size_t>(row) * rp.n_q + head) * DH : nullptr;
+    } else if (rot) {
+      dst = slot_ok ? kc + ((static_cast<size_t>(page) * rp.n_kv + (head - rp.n_q)) * 16 + off) * DH : nullptr;
+    } else {
+      dst = slot_ok ? vc + ((static_cast<size_t>(page) * rp.n_kv + (head - rp.n_q - rp.n_kv)) * 16 + off) * DH
+                    : nullptr;
+    }
+#pragma unroll 1
+    for (int c = 0; c < HALF; c += 32) {
+      // (cos, sin) of dimensions c .. c + 31 at the row's position, all loads
+      // in flight together (the accumulator loads overlap them)
+      float4 cs[16];
+      const float4* csp = reinterpret_cast<const float4*>(rp.rope + static_cast<size_t>(pos) * HALF + c);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) cs[i] = rot && pos_ok ? __ldg(csp + i) : make_float4(1.f, 0.f, 1.f, 0.f);
+      uint32_t r1[32], r2[32];
+      tmem_ld_32x32b_x32(t_base + hb + c, r1);
+      tmem_ld_32x32b_x32(t_base + hb + HALF + c, r2);
+      tmem_ld_wait();
+      if constexpr (F8) {
+        scale_cols(r1, rowf, p.sb, col0 + c, p.N);
+        scale_cols(r2, rowf, p.sb, col0 + HALF + c, p.N);
+      }
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {  // 8 dimensions (one 16-byte piece per half) at a time
+        uint32_t w1[4], w2[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int e = 8 * g + 2 * j;
+          // the bf16 activations of the projection
+          const float2 a = unpack_bf16x2(pack_bf16x2(__fmul_rn(__uint_as_float(r1[e]), sc),
+                                                     __fmul_rn(__uint_as_float(r1[e + 1]), sc)));
+          const float2 b = unpack_bf16x2(pack_bf16x2(__fmul_rn(__uint_as_float(r2[e]), sc),
+                                                     __fmul_rn(__uint_as_float(r2[e + 1]), sc)));
+          if (rot) {
+            const float4 t = cs[e >> 1];  // (cos, sin) of dimensions e and e + 1
+            w1[j] = pack_bf16x2(__fsub_rn(__fmul_rn(a.x, t.x), __fmul_rn(b.x, t.y)),
+                                __fsub_rn(__fmul_rn(a.y, t.z), __fmul_rn(b.y, t.w)));
+            w2[j] = pack_bf16x2(__fadd_rn(__fmul_rn(b.x, t.x), __fmul_rn(a.x, t.y)),
+                                __fadd_rn(__fmul_rn(b.y, t.z), __fmul_rn(a.y, t.w)));
+          } else {
+            w1[j] = pack_bf16x2(a.x, a.y);
+            w2[j] = pack_bf16x2(b.x, b.y);
+          }
+        }
+        if (dst != nullptr) {
+          *reinterpret_cast<uint4*>(dst + c + 8 * g) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+          *reinterpret_cast<uint4*>(dst + HALF + c + 8 * g) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+        }
+      }
+    }
   }
 }
 
@@ -710,7 +815,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-      if (un + static_cast<int>(gridDim.x) >= units) {
+      if constexpr (EPI == kEpiRope) {
+        epilogue_rope<BN, F8>(p, t_base, row, row_ok, n_blk, scale, rowf);
+      } else if (un + static_cast<int>(gridDim.x) >= units) {
         // the CTA's last tile: the ring is idle, stage through it
         ok = epilogue_last<BN, EPI, F8>(p, &tmC, &tmR, smem, ep_bar, ep_flag, t_base, m0, row, row_ok, rloc, n_blk,
                                         wu.tile, wu.half, leader, scale, rowf, abort_flag);
@@ -966,7 +1073,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (mt < m_tiles) {  // a 128-row tile wholly past M (odd tile count) has nothing to write
         const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
         const int stile = mt + m_tiles * wu.n_blk;
-        if (un + n_clusters >= units) {
+        if constexpr (EPI == kEpiRope) {
+          epilogue_rope<BN, F8>(p, t_base, row, row_ok, wu.n_blk, scale, rowf);
+        } else if (un + n_clusters >= units) {
           // the CTA's last tile: its ring is idle, stage through it
           ok = epilogue_last<BN, EPI, F8>(p, &tmC, &tmR, smem, ep_bar, ep_flag, t_base, mt * BM, row, row_ok, rloc,
                                           wu.n_blk, stile, wu.half, leader_thread, scale, rowf, abort_flag);
@@ -1011,7 +1120,7 @@ hb_status encode_out_maps(CUtensorMap* tmC, CUtensorMap* tmR, void* Cp, const vo
 template <int BN, int EPI, bool F8>
 hb_status launch_pair(const DeviceCtx& ctx, const void* A, int lda, const float* sa, const void* B, const float* sb,
                       void* Cp, int ldc, const void* R, int M, int N, int K, const GemmNorm* norm,
-                      const GemmSplit* split, cudaStream_t stream) {
+                      const GemmSplit* split, cudaStream_t stream, const GemmRope* rope = nullptr) {
   using C = CfgPair<BN>;
   constexpr int BK = bk_elems<F8>();
   constexpr int ESZ = F8 ? 1 : 2;
@@ -1020,8 +1129,13 @@ hb_status launch_pair(const DeviceCtx& ctx, const void* A, int lda, const float*
   if (st != HB_OK) return st;
   st = encode_tmap_2d(&tmB, B, K, N, static_cast<uint64_t>(K) * ESZ, BK, BN / 2, true, ESZ);
   if (st != HB_OK) return st;
-  st = encode_out_maps<EPI>(&tmC, &tmR, Cp, R, ldc, M, EPI == HB_EPI_SWIGLU ? N / 2 : N);
-  if (st != HB_OK) return st;
+  if constexpr (EPI == kEpiRope) {
+    tmC = tmA;  // no tiled stores: the fused epilogue writes q, K and V rows itself
+    tmR = tmA;
+  } else {
+    st = encode_out_maps<EPI>(&tmC, &tmR, Cp, R, ldc, M, EPI == HB_EPI_SWIGLU ? N / 2 : N);
+    if (st != HB_OK) return st;
+  }
   static std::atomic<bool> attr_set[kMaxDevices];
   st = smem_limit_once(attr_set, ctx.device, gemm_pair_kernel<BN, EPI, F8>, C::SMEM, "cudaFuncSetAttribute(gemm pair)");
   if (st != HB_OK) return st;
@@ -1040,6 +1154,7 @@ hb_status launch_pair(const DeviceCtx& ctx, const void* A, int lda, const float*
   p.flags = split ? split->flags : nullptr;
   p.sa = sa;
   p.sb = sb;
+  p.rope = rope ? *rope : GemmRope{};
   const int m_tiles = (M + BM - 1) / BM;
   const int units = ((m_tiles + 1) / 2) * ((N + BN - 1) / BN) * p.ksplit;
   const int pairs = ctx.num_sms / 2;
@@ -1052,7 +1167,7 @@ hb_status launch_pair(const DeviceCtx& ctx, const void* A, int lda, const float*
 template <int BN, int EPI, bool F8>
 hb_status launch(const DeviceCtx& ctx, const void* A, int lda, const float* sa, const void* B, const float* sb,
                  void* Cp, int ldc, const void* R, int M, int N, int K, const GemmNorm* norm, const GemmSplit* split,
-                 cudaStream_t stream) {
+                 cudaStream_t stream, const GemmRope* rope = nullptr) {
   using C = Cfg<BN>;
   constexpr int BK = bk_elems<F8>();
   constexpr int ESZ = F8 ? 1 : 2;
@@ -1061,8 +1176,13 @@ hb_status launch(const DeviceCtx& ctx, const void* A, int lda, const float* sa, 
   if (st != HB_OK) return st;
   st = encode_tmap_2d(&tmB, B, K, N, static_cast<uint64_t>(K) * ESZ, BK, BN, true, ESZ);
   if (st != HB_OK) return st;
-  st = encode_out_maps<EPI>(&tmC, &tmR, Cp, R, ldc, M, EPI == HB_EPI_SWIGLU ? N / 2 : N);
-  if (st != HB_OK) return st;
+  if constexpr (EPI == kEpiRope) {
+    tmC = tmA;  // no tiled stores: the fused epilogue writes q, K and V rows itself
+    tmR = tmA;
+  } else {
+    st = encode_out_maps<EPI>(&tmC, &tmR, Cp, R, ldc, M, EPI == HB_EPI_SWIGLU ? N / 2 : N);
+    if (st != HB_OK) return st;
+  }
   static std::atomic<bool> attr_set[kMaxDevices];
   st = smem_limit_once(attr_set, ctx.device, gemm_kernel<BN, EPI, F8>, C::SMEM, "cudaFuncSetAttribute(gemm)");
   if (st != HB_OK) return st;
@@ -1081,6 +1201,7 @@ hb_status launch(const DeviceCtx& ctx, const void* A, int lda, const float* sa, 
   p.flags = split ? split->flags : nullptr;
   p.sa = sa;
   p.sb = sb;
+  p.rope = rope ? *rope : GemmRope{};
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int units = tiles * p.ksplit;
   const int grid = units < ctx.num_sms ? units : ctx.num_sms;
@@ -1093,14 +1214,15 @@ hb_status launch(const DeviceCtx& ctx, const void* A, int lda, const float* sa, 
 inline int choose_bn(int M, int N, int epi, int num_sms) {
   const int cands_swiglu[2] = {256, 128};
   const int cands[3] = {256, 192, 128};
-  const int* c = epi == HB_EPI_SWIGLU ? cands_swiglu : cands;
-  const int nc = epi == HB_EPI_SWIGLU ? 2 : 3;
+  const bool whole = epi == HB_EPI_SWIGLU || epi == kEpiRope;  // tiles of whole 128-column groups
+  const int* c = whole ? cands_swiglu : cands;
+  const int nc = whole ? 2 : 3;
   const int m_tiles = (M + BM - 1) / BM;
   int best = 128;
   double best_cost = 1e30;
   for (int i = 0; i < nc; ++i) {
     const int bn = c[i];
-    if (epi == HB_EPI_SWIGLU ? N % bn != 0 : (N % bn != 0 && bn != 128)) continue;
+    if (whole ? N % bn != 0 : (N % bn != 0 && bn != 128)) continue;
     const int tiles = m_tiles * ((N + bn - 1) / bn);
     const int waves = (tiles + num_sms - 1) / num_sms;
     const double cost = waves * (bn + 32.0);

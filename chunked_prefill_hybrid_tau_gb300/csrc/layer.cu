@@ -132,6 +132,26 @@ extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_
     if (st != HB_OK) return st;  \
   } while (0)
 
+  // RoPE and the KV append in the QKV projection's epilogue (E4M3 weights,
+  // when every projection tile holds whole heads); else a separate
+  // kv_append kernel.  Both give the same bits.  With bf16 weights the
+  // fused path is slower at the benchmark shapes: it needs 256-wide tiles
+  // (48 CTA pairs) where the plain projection runs 192-wide ones on 64
+  // pairs, which costs more than the saved launch.
+  const bool fuse_rope = f8 && gemm_rope_ok(qkv_cols, dm);
+  GemmRope rope_qkv;
+  rope_qkv.rope = static_cast<const float2*>(rope);
+  rope_qkv.row_pos = plan->row_pos;
+  rope_qkv.slots = plan->slot_mapping;
+  rope_qkv.q_out = q;
+  rope_qkv.k_cache = k_cache;
+  rope_qkv.v_cache = v_cache;
+  rope_qkv.n_q = dm.n_q;
+  rope_qkv.n_kv = dm.n_kv;
+  rope_qkv.d_head = dm.d_head;
+  rope_qkv.max_pos = max_pos;
+  rope_qkv.num_slots = static_cast<long long>(num_pages) * 16;
+  const int qkv_epi = fuse_rope ? kEpiRope : HB_EPI_STORE;
   GemmNorm norm_x, norm_h_out, norm_h_in;
   norm_x.ss_in = ss_x;
   norm_h_out.ss_out = ss_h;
@@ -161,10 +181,11 @@ extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_
     float* sh = so + align256(static_cast<size_t>(T) * 4) / 4;
     float* sa = sh + align256(static_cast<size_t>(T) * 4) / 4;
     HB_STEP(0, quant_rows_launch(ctx, x_in, xq, sx, T, d, ss_x, split_o.flags, n_zero, s));
-    HB_STEP(1, gemm_e4m3_launch(ctx, xq, d, sx, w->w_qkv, w->s_qkv, qkv, qkv_cols, nullptr, T, qkv_cols, d,
-                                HB_EPI_STORE, s, &norm_x));
-    HB_STEP(2, kv_append_launch(ctx, qkv, T, plan->row_pos, plan->slot_mapping, rope, max_pos, dm, q, k_cache,
-                                v_cache, num_pages, s));
+    HB_STEP(1, gemm_e4m3_launch(ctx, xq, d, sx, w->w_qkv, w->s_qkv, qkv, qkv_cols, nullptr, T, qkv_cols, d, qkv_epi,
+                                s, &norm_x, nullptr, &rope_qkv));
+    HB_STEP(2, fuse_rope ? HB_OK
+                         : kv_append_launch(ctx, qkv, T, plan->row_pos, plan->slot_mapping, rope, max_pos, dm, q,
+                                            k_cache, v_cache, num_pages, s));
     HB_STEP(3, attention_launch(ctx, q, k_cache, v_cache, num_pages, *plan, dm, max_kv_len, o, aws,
                                 lw.total - lw.attn, s, true));
     HB_STEP(4, quant_rows_launch(ctx, o, oq, so, T, hd, nullptr, nullptr, 0, s));

@@ -113,6 +113,28 @@ struct GemmSplit {
   int* flags = nullptr;
 };
 bool gemm_split_k(int N, int K, int epi);
+
+// QKV projection with the RoPE rotation and the paged KV append in its
+// epilogue (the layer's fused path with E4M3 weights, epilogue id kEpiRope,
+// internal, gemm_e4m3_launch only): the
+// rotated q rows go to q_out [rows][n_q][d_head], the rotated K row and the
+// V row of each token to its slot of the [page][n_kv][16][d_head] pools.
+// rope, row_pos and slots as for kv_append_launch; the arithmetic and the
+// rounding points are those of the projection's STORE epilogue followed by
+// kv_append_kernel, so the fused and the two-kernel paths give the same bits.
+struct GemmRope {
+  const float2* rope = nullptr;
+  const int* row_pos = nullptr;
+  const int* slots = nullptr;
+  void* q_out = nullptr;
+  void* k_cache = nullptr;
+  void* v_cache = nullptr;
+  int n_q = 0, n_kv = 0, d_head = 0, max_pos = 0;
+  long long num_slots = 0;
+};
+constexpr int kEpiRope = 16;
+// The fused path applies when whole heads fall in every 128- and 256-column tile.
+bool gemm_rope_ok(int N, const hb_layer_dims& dims);
 // Tile width of CTA-pair tiles (tcgen05 cta_group::2, 256 rows) for a
 // projection, or 0 for one-CTA tiles.
 int gemm_pair_bn(int M, int N, int epi, bool split, int num_sms);
@@ -124,7 +146,8 @@ int gemm_split_flags(int M, int N);          // arrival counters (ints)
 // bf16 ones applied to sa[m] sb[n] acc.
 hb_status gemm_e4m3_launch(const DeviceCtx& ctx, const void* A, int lda, const float* sa, const void* B,
                            const float* sb, void* C, int ldc, const void* R, int M, int N, int K, int epi,
-                           cudaStream_t stream, const GemmNorm* norm = nullptr, const GemmSplit* split = nullptr);
+                           cudaStream_t stream, const GemmNorm* norm = nullptr, const GemmSplit* split = nullptr,
+                           const GemmRope* rope = nullptr);
 hb_status gemm_e4m3_check(const void* A, const float* sa, const void* B, const float* sb, void* C, const void* R,
                           int M, int N, int K, int epi);
 
