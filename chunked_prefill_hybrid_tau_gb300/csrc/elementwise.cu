@@ -102,11 +102,12 @@ __global__ void __launch_bounds__(kNormWarps * 32)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float2 f = unpack_bf16x2(w[j]);
-      a += f.x * f.x;
-      a += f.y * f.y;
+      a = __fmaf_rn(f.x, f.x, a);
+      a = __fmaf_rn(f.y, f.y, a);
     }
-    a += __shfl_xor_sync(0xffffffffu, a, 1);
-    a += __shfl_xor_sync(0xffffffffu, a, 2);
+    // parts of 32 columns: (lane 4q + lane 4q+1) + (lane 4q+2 + lane 4q+3)
+    a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 2));
     const int i = lane + 32 * k;
     if ((lane & 3) == 0 && i < d8) out[i / 4] = a;
   }

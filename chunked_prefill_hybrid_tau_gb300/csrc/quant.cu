@@ -60,13 +60,13 @@ __global__ void __launch_bounds__(kQuantThreads)
       const float2 f = unpack_bf16x2(w[j]);
       amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
       if (SS) {
-        a += f.x * f.x;
-        a += f.y * f.y;
+        a = __fmaf_rn(f.x, f.x, a);
+        a = __fmaf_rn(f.y, f.y, a);
       }
     }
     if (SS) {
-      a += __shfl_xor_sync(0xffffffffu, a, 1);
-      a += __shfl_xor_sync(0xffffffffu, a, 2);
+      a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 1));
+      a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 2));
       const int i = t + kQuantThreads * k;
       if ((lane & 3) == 0 && i < c8) ss[static_cast<size_t>(r) * (c8 / 4) + i / 4] = a;
     }
