@@ -283,7 +283,11 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
         const int page = btc[b];
         const int y = (page * p.n_kv + g) * 16;
         const bool is_v = lane & 1;
-        tma_load_3d(dst + (is_v ? PAGE_BYTES : 0), is_v ? &tmV : &tmK, &full[slot], 0, y, 0);
+        // each decode K/V byte is read once: first out of L2, so the stream
+        // does not push out what is read again (the chunk rows' prefix K/V,
+        // activations, code)
+        tma_load_3d_hint(dst + (is_v ? PAGE_BYTES : 0), is_v ? &tmV : &tmK, &full[slot], 0, y, 0,
+                         policy_evict_first());
       }
     };
     for (int b = 0; b < min(DR, npages); ++b) issue(b);
