@@ -704,14 +704,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pending = 0;  // stages armed and not yet seen consumed (bit mask)
       uint32_t armed_parity = 0;
       // The weights do not come from the previous kernel: the first ring
-      // fill of B is issued before waiting for it, then A follows.
+      // fill of B is issued before waiting for it, then A follows.  Up to 8
+      // row tiles, a weight box is read by the CTAs of its column tile at
+      // about the same time and not again in the layer: first out of L2.
+      // With more rows the larger activations push the box out between its
+      // readers, and the default policy is faster (measured at 2048 and
+      // 4096 rows).
+      const uint64_t wpol = m_tiles <= 8 ? policy_evict_first() : policy_evict_normal();
       int pre = 0;
       if (static_cast<int>(blockIdx.x) < units) {
         const Unit w = unit_of<BN>(p, blockIdx.x, m_tiles, kblocks);
         pre = w.kb1 - w.kb0 < C::STAGES ? w.kb1 - w.kb0 : C::STAGES;
         for (int i = 0; i < pre; ++i) {
           mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
-          tma_load_2d(smem + i * C::STAGE_BYTES + C::A_BYTES, &tmB, &full[i], (w.kb0 + i) * BK, w.n_blk * BN);
+          tma_load_2d_hint(smem + i * C::STAGE_BYTES + C::A_BYTES, &tmB, &full[i], (w.kb0 + i) * BK, w.n_blk * BN,
+                           wpol);
         }
       }
       griddep_wait();
@@ -734,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
             mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
             tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
-            tma_load_2d(sa + C::A_BYTES, &tmB, &full[stage], kb * BK, n0);
+            tma_load_2d_hint(sa + C::A_BYTES, &tmB, &full[stage], kb * BK, n0, wpol);
           }
           if (++stage == C::STAGES) {
             stage = 0;
@@ -960,11 +967,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       uint32_t pending = 0, armed_parity = 0;  // stages loaded and not yet seen released
       // The weights do not come from the previous kernel: the first ring
-      // fill of B is issued before waiting for it, then A follows.  A weight
-      // box is read by the two clusters of its column tile at about the same
-      // time and not again in the layer: first out of L2 (with the decode
-      // K/V stream also first out, the layer is 2% faster).
-      const uint64_t wpol = policy_evict_first();
+      // fill of B is issued before waiting for it, then A follows.  Up to 4
+      // pair row tiles (1024 rows), a weight box is read by the clusters of
+      // its column tile at about the same time and not again in the layer:
+      // first out of L2 (with the decode K/V stream also first out, the
+      // 512-row layer is 2% faster).  With more rows the activations push
+      // the box out between its readers, and the default policy is faster.
+      const uint64_t wpol = pm_tiles <= 4 ? policy_evict_first() : policy_evict_normal();
       int pre = 0;
       if (cluster < units) {
         const PairUnit w = pair_unit_of(p, cluster, pm_tiles, kblocks);
