@@ -89,6 +89,15 @@ def max_over_ranks(v: float, world: int) -> float:
 
 
 # ---------------------------------------------------------------- workload
+def launches_per_layer(dims, f8: bool) -> int:
+    """Kernels one hb_layer_forward launches (the chunk and decode attention
+    kernels are both launched whatever the batch holds)."""
+    if not f8:
+        return 8
+    fused = ((dims.n_q + 2 * dims.n_kv) * dims.d_head) % 256 == 0 and dims.d_head in (64, 128)
+    return 10 if fused else 11
+
+
 def make_workload(tau: int, n_dec: int):
     import workloads as wl
     if tau == 512 and n_dec == 32:
@@ -541,8 +550,10 @@ def run_hb(args, world, rank, local):
         "stages_ms": {k: round(float(v), 5) for k, v in zip(costs.STAGES, stage_ms)},
         "e2e": e2e,
         # per layer forward: row statistics, QKV, RoPE/KV append, chunk and decode
-        # attention, O, gate/up, down (E4M3: three more quantization kernels)
-        "gpu_launches": (11 if f8 else 8) * args.steps,
+        # attention, O, gate/up, down; E4M3: three more quantization kernels,
+        # and RoPE/KV append inside the QKV projection when its tiles hold
+        # whole heads (the library's rule: QKV columns % 256, d_head 64 or 128)
+        "gpu_launches": launches_per_layer(dims, f8) * args.steps,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

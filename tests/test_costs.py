@@ -66,3 +66,15 @@ def test_select_tau_takes_the_largest_budget_within_the_slo():
     assert bench.select_tau([(64, 1.0), (128, 1.0)], 10.0) == (128, None)
     # a non-monotone profile still returns the largest fitting budget
     assert bench.select_tau([(64, 1.0), (128, 3.0), (256, 2.0)], 2.5)[0] == 256
+
+
+def test_launch_count_follows_the_fused_qkv_rule():
+    """The bench's gpu_launches claim: 8 kernels per bf16 layer, 10 per E4M3
+    layer whose QKV tiles hold whole heads (RoPE/KV append fused), else 11."""
+    import bench
+    import workloads as wl
+    assert bench.launches_per_layer(wl.MISTRAL, False) == 8
+    assert bench.launches_per_layer(wl.MISTRAL, True) == 10      # 6144 QKV columns, d_head 128
+    assert bench.launches_per_layer(wl.YI34B, True) == 10        # 9216 columns
+    odd = wl.Dims(d_model=256, n_q=3, n_kv=1, d_head=64, d_ff=64)  # 320 columns: not whole 256-column tiles
+    assert bench.launches_per_layer(odd, True) == 11
