@@ -379,7 +379,10 @@ hb_status hb_fold_gamma(const void* w, const void* gamma, void* out, int32_t row
  *            accumulators of the QKV and gate/up GEMMs.  HB_WEIGHTS_E4M3:
  *            x, o, h and the SwiGLU output are quantized per token
  *            (hb_quantize_e4m3's rule, r still from the bf16 rows) and the
- *            projections run as hb_gemm_e4m3; d_ff % 16 == 0 required.
+ *            projections run as hb_gemm_e4m3; d_ff % 16 == 0 required.  With
+ *            E4M3 weights and (n_q + 2 n_kv) d_head % 256 == 0 the RoPE and
+ *            KV append run inside the QKV projection (same results; the
+ *            rope+kv stage is then empty).
  *   plan   : device plan; rope: table from hb_rope_table with max_pos rows
  *   x_in   : device bf16 [T][d_model]; x_out may alias x_in
  *   caches : updated in place with this iteration's K/V
