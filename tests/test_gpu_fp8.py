@@ -240,3 +240,31 @@ def test_e4m3_chunked_equals_unchunked_bitwise():
         assert torch.equal(out, ref), f"C={C}: outputs differ"
         assert torch.equal(k, kr) and torch.equal(v, vr), f"C={C}: KV differs"
     assert torch.isfinite(ref.float()).all()
+
+
+def test_fused_qkv_append_reports_a_bad_slot():
+    """With E4M3 weights (and QKV tiles of whole heads) the RoPE and KV append
+    run in the QKV projection's epilogue.  A slot outside the pool is skipped
+    and reported in the status word, as hb_kv_append does, and the other rows'
+    K still land in their slots."""
+    w = wl.tiny_layer(seed=0)
+    st, dims = w.state, w.dims
+    assert ((dims.n_q + 2 * dims.n_kv) * dims.d_head) % 256 == 0  # the fused path applies
+    max_pos = 512
+    gl = GpuLayer(w.weights[0], dims, st.k_pool, st.v_pool, max_pos, fmt="e4m3")
+    hp, _ = plan_both(st, 68, 64)
+    good = int(hp.slot_mapping[0])
+    hp.slot_mapping = np.array(hp.slot_mapping, dtype=np.int32, copy=True)
+    hp.slot_mapping[1] = 10**6
+    dp = hb.DevicePlan(hp)
+    xin = wd.bf16_tensor(w.x)
+    xout = torch.empty_like(xin)
+    ws = wd.workspace(hb.hb_layer_workspace_bytes(dims, hp.n_rows, hp.n_seqs, max_pos))
+    k_before = gl.k.clone()
+    hb.hb_layer_forward(gl.w, dims, dp, gl.rope, max_pos, xin, xout, gl.k, gl.v, max_pos, ws)
+    with pytest.raises(hb.HBError) as e:
+        hb.hb_check_status()
+    assert e.value.status == L.HB_ERR_DEVICE
+    hb.hb_check_status()  # cleared
+    pg, off = good // 16, good % 16
+    assert not torch.equal(gl.k[pg, :, off], k_before[pg, :, off])  # row 0's K was appended
