@@ -358,12 +358,12 @@ constexpr int kSlabBytes = 128 * 128;
 //   of its own half with one bulk copy.
 // Called by the 128 epilogue threads; `leader` is one of them.  Returns
 // false when a bounded wait expired.  This code runs once per CTA and
-// usually cold (the attention kernels before the o projection stream far
-// more than L2 holds), so its instruction fetches weigh as much as its
-// arithmetic: with E4M3 operands (the longer code with the scales) the
-// 32-column steps are not unrolled (E4M3 layer 206.1 -> 202.3 us, gate/up
-// epilogue), with bf16 they are (unrolling once cost 2 us per layer).  Both
-// measured on one GB300, 1500 steps each.
+// often cold, so its instruction fetches weigh as much as its arithmetic:
+// the 32-column steps of the residual path are not unrolled (bf16 layer
+// 233.0 -> 231.7 us), those of the SwiGLU and store paths only with E4M3
+// operands (their longer code with the scales: E4M3 layer 206.1 -> 202.3
+// us; with bf16, not unrolling them cost 2 us).  Measured on one GB300,
+// 1500 steps per variant.
 template <int BN, int EPI, bool F8>
 __device__ __forceinline__ bool epilogue_last(const Params& p, const CUtensorMap* tmC, const CUtensorMap* tmR,
                                               uint8_t* ring, uint64_t* ep_bar, volatile int* ep_flag, uint32_t t_base,
@@ -418,7 +418,7 @@ __device__ __forceinline__ bool epilogue_last(const Params& p, const CUtensorMap
 #pragma unroll 1
     for (int s = 0; s < ns; ++s) {
       uint8_t* slab = ring + s * kSlabBytes;
-#pragma unroll(F8 ? 1 : 2)
+#pragma unroll 1
       for (int h = 0; h < 2; ++h) {
         uint32_t r[32];
         const int cl = cl0 + s * 64 + h * 32;  // accumulator column within the tile
