@@ -300,6 +300,17 @@ def cores():
     return len(os.sched_getaffinity(0))
 
 
+def workload_config(w, weights, world, T, n_dec):
+    """The `config` of the bench line, the same for the GPU arm and the
+    reference arm (T rows per iteration, n_dec of them decodes)."""
+    dims = w.dims
+    return {"workload": WORKLOAD + ("_e4m3" if weights == "e4m3" else ""), "tau": w.tau, "weights": weights,
+            "chunk_tokens": T - n_dec, "decodes": n_dec, "rows": T, "d_model": dims.d_model,
+            "heads": f"{dims.n_q}q/{dims.n_kv}kv", "d_head": dims.d_head, "d_ff": dims.d_ff, "page": 16,
+            "parallelism": f"replicas{world}" if world > 1 else "single",
+            "l2": "inputs larger than L2 (436 MB weights + 308 MB KV per step), no flush"}
+
+
 # ---------------------------------------------------------------- reference arm
 def run_reference(args, world, rank):
     if rank != 0:
@@ -341,7 +352,7 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tau": w.tau, "rows_per_step": n_rows},
+        "config": workload_config(w, args.weights, world, w.tau, len(st.decodes)),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -535,10 +546,7 @@ def run_hb(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * t_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 projections, bf16 attention" if f8 else "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD + ("_e4m3" if f8 else ""), "tau": w.tau, "weights": args.weights, "chunk_tokens": c, "decodes": n_dec, "rows": T,
-                   "d_model": dims.d_model, "heads": f"{dims.n_q}q/{dims.n_kv}kv", "d_head": dims.d_head,
-                   "d_ff": dims.d_ff, "page": 16, "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": "inputs larger than L2 (436 MB weights + 308 MB KV per step), no flush"},
+        "config": workload_config(w, args.weights, world, T, n_dec),
         "roofline": {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_source,
                      "launch_ms": stage_ms[dom]},
