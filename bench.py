@@ -89,13 +89,12 @@ def max_over_ranks(v: float, world: int) -> float:
 
 
 # ---------------------------------------------------------------- workload
-def launches_per_layer(dims, f8: bool) -> int:
-    """Kernels one hb_layer_forward launches (the chunk and decode attention
-    kernels are both launched whatever the batch holds)."""
-    if not f8:
-        return 8
-    fused = ((dims.n_q + 2 * dims.n_kv) * dims.d_head) % 256 == 0 and dims.d_head in (64, 128)
-    return 10 if fused else 11
+def launches_per_layer(dims, f8: bool, n_rows: int) -> int:
+    """Kernels one hb_layer_forward launches, by the library's own rule
+    (hb_layer_kernel_count: the chunk and decode attention kernels are both
+    launched whatever the batch holds)."""
+    import chunked_prefill_hybrid_tau_gb300 as hb
+    return hb.hb_layer_kernel_count(dims, n_rows, 1 if f8 else 0)
 
 
 def make_workload(tau: int, n_dec: int):
@@ -560,8 +559,8 @@ def run_hb(args, world, rank, local):
         # per layer forward: row statistics, QKV, RoPE/KV append, chunk and decode
         # attention, O, gate/up, down; E4M3: three more quantization kernels,
         # and RoPE/KV append inside the QKV projection when its tiles hold
-        # whole heads (the library's rule: QKV columns % 256, d_head 64 or 128)
-        "gpu_launches": launches_per_layer(dims, f8) * args.steps,
+        # whole heads
+        "gpu_launches": launches_per_layer(dims, f8, T) * args.steps,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -384,6 +384,13 @@ def hb_layer_workspace_bytes(dims, max_rows, max_seqs, max_kv_len) -> int:
     return int(lib().hb_layer_workspace_bytes(C.byref(ds), int(max_rows), int(max_seqs), int(max_kv_len)))
 
 
+def hb_layer_kernel_count(dims, n_rows, fmt) -> int:
+    ds = dims_struct(dims)
+    n = C.c_int32()
+    _check(lib().hb_layer_kernel_count(C.byref(ds), int(n_rows), int(fmt), C.byref(n)), "hb_layer_kernel_count")
+    return int(n.value)
+
+
 @dataclasses.dataclass
 class LayerWeights:
     """Prepared device weights of one layer (prepare_layer_weights): bf16

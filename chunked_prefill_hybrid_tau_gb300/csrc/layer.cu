@@ -71,6 +71,29 @@ extern "C" size_t hb_layer_workspace_bytes(const hb_layer_dims* dims, int32_t ma
   return hb::layer_ws(*dims, max_rows, max_seqs, max_kv_len).total;
 }
 
+extern "C" hb_status hb_layer_kernel_count(const hb_layer_dims* dims, int32_t n_rows, int32_t format,
+                                           int32_t* count) {
+  using namespace hb;
+  clear_error();
+  hb_status st = check_dims(dims);
+  if (st != HB_OK) return st;
+  HB_REQUIRE(count && n_rows >= 0, "hb_layer_kernel_count: bad arguments");
+  HB_REQUIRE(format == HB_WEIGHTS_BF16 || format == HB_WEIGHTS_E4M3, "hb_layer_kernel_count: unknown format %d",
+             format);
+  // the same rules as hb_layer_forward: row statistics, QKV, RoPE/KV
+  // append, chunk and decode attention, O, gate/up, down; E4M3: three more
+  // quantization kernels, RoPE/KV append inside the QKV projection when
+  // its tiles hold whole heads
+  const int qkv_cols = (dims->n_q + 2 * dims->n_kv) * dims->d_head;
+  if (n_rows == 0)
+    *count = 0;
+  else if (format == HB_WEIGHTS_E4M3)
+    *count = gemm_rope_ok(qkv_cols, *dims) ? 10 : 11;
+  else
+    *count = 8;
+  return HB_OK;
+}
+
 extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_dims* dims, const hb_device_plan* plan,
                                       const void* rope, int32_t max_pos, const void* x_in, void* x_out, void* k_cache,
                                       void* v_cache, int32_t num_pages, int32_t max_kv_len, void* workspace,

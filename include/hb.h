@@ -427,6 +427,15 @@ hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_dims* dims,
                            void* k_cache, void* v_cache, int32_t num_pages, int32_t max_kv_len,
                            void* workspace, size_t ws_bytes, void* stream, const hb_profile* prof);
 
+/* hb_layer_kernel_count - how many kernels one hb_layer_forward call launches
+ * for n_rows packed rows with weights in `format` (host logic only, no
+ * device call; the chunk and decode attention kernels
+ * count whatever the batch holds, n_rows == 0 launches nothing).  bf16: 8;
+ * E4M3: 11, or 10 when the RoPE and KV append run inside the QKV
+ * projection.  *count written on HB_OK; HB_ERR_INVALID_ARG for a null
+ * pointer, bad dims, n_rows < 0 or an unknown format. */
+hb_status hb_layer_kernel_count(const hb_layer_dims* dims, int32_t n_rows, int32_t format, int32_t* count);
+
 /* ------------------------------------------------------------------------
  * hb_final_logits - final RMSNorm + untied LM head for selected rows (the
  * decode rows and the last chunk row of a model-level iteration):

@@ -69,12 +69,20 @@ def test_select_tau_takes_the_largest_budget_within_the_slo():
 
 
 def test_launch_count_follows_the_fused_qkv_rule():
-    """The bench's gpu_launches claim: 8 kernels per bf16 layer, 10 per E4M3
-    layer whose QKV tiles hold whole heads (RoPE/KV append fused), else 11."""
+    """The bench's gpu_launches claim, from the library's own rule: 8
+    kernels per bf16 layer; 10 per E4M3 layer whose QKV tiles hold whole
+    heads (RoPE/KV append fused), else 11; nothing for an empty batch."""
     import bench
     import workloads as wl
-    assert bench.launches_per_layer(wl.MISTRAL, False) == 8
-    assert bench.launches_per_layer(wl.MISTRAL, True) == 10      # 6144 QKV columns, d_head 128
-    assert bench.launches_per_layer(wl.YI34B, True) == 10        # 9216 columns
+    assert bench.launches_per_layer(wl.MISTRAL, False, 512) == 8
+    assert bench.launches_per_layer(wl.TINY, False, 68) == 8
+    assert bench.launches_per_layer(wl.MISTRAL, False, 0) == 0
+    assert bench.launches_per_layer(wl.MISTRAL, True, 512) == 10     # 6144 QKV columns, d_head 128
+    assert bench.launches_per_layer(wl.YI34B, True, 1024) == 10      # 9216 columns
     odd = wl.Dims(d_model=256, n_q=3, n_kv=1, d_head=64, d_ff=64)  # 320 columns: not whole 256-column tiles
-    assert bench.launches_per_layer(odd, True) == 11
+    assert bench.launches_per_layer(odd, True, 68) == 11
+    import chunked_prefill_hybrid_tau_gb300 as hb
+    with pytest.raises(hb.HBError):
+        hb.hb_layer_kernel_count(wl.MISTRAL, -1, 0)
+    with pytest.raises(hb.HBError):
+        hb.hb_layer_kernel_count(wl.MISTRAL, 512, 7)
