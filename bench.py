@@ -678,8 +678,9 @@ def select_tau(profile, slo_ms):
 def run_calibrate(args):
     """The scheduling method's tau calibration (the Sarathi-Serve reading notes'
     profiling step): measure the iteration time T(tau) of a --layers-deep
-    model (distinct random weights and KV pools per layer, every layer through
-    hb_layer_forward) over a range of token budgets, then take the largest
+    model (distinct random weights and KV pools per layer, the layers through
+    one hb_layers_forward call; the same layers as hb_layer_forward calls
+    are timed beside it) over a range of token budgets, then take the largest
     tau whose time fits the per-iteration SLO.  The batch at each tau is 64
     decodes with contexts uniform in [512, 8192] plus a chunk of tau - 64
     tokens.  Prints the profile and one summary line."""
@@ -707,9 +708,20 @@ def run_calibrate(args):
         x = x_all[:tau].clone()
         ds = hb.dims_struct(dims)
         wstructs = [lw.struct() for lw in layers]
+        warr = (type(wstructs[0]) * L)(*wstructs)
+        karr = (C.c_void_p * L)(*[k.data_ptr() for k, _ in pools])
+        varr = (C.c_void_p * L)(*[v.data_ptr() for _, v in pools])
 
-        def iteration():
+        def iteration(stacked):
             dp = runner.step(stream)
+            if stacked:  # the model's layers in one call (statistics carried between layers)
+                rc = lib.hb_layers_forward(warr, L, C.byref(ds), C.byref(dp), C.c_void_p(rope.data_ptr()), max_pos,
+                                           C.c_void_p(x.data_ptr()), C.c_void_p(x.data_ptr()), karr, varr,
+                                           int(pools[0][0].shape[0]), max_pos, C.c_void_p(ws.data_ptr()), ws.numel(),
+                                           C.c_void_p(stream.cuda_stream))
+                if rc != 0:
+                    raise RuntimeError(lib.hb_last_error().decode())
+                return
             for l in range(L):
                 k, v = pools[l]
                 rc = lib.hb_layer_forward(C.byref(wstructs[l]), C.byref(ds), C.byref(dp), C.c_void_p(rope.data_ptr()),
@@ -720,22 +732,27 @@ def run_calibrate(args):
                 if rc != 0:
                     raise RuntimeError(lib.hb_last_error().decode())
 
-        for _ in range(3):
-            iteration()
-        stream.synchronize()
-        n = max(5, min(args.steps, 20))
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        for _ in range(n):
-            iteration()
-        s1.record(stream)
-        stream.synchronize()
-        hb.hb_check_status(stream)
-        ms = s0.elapsed_time(s1) / n
+        def timed(stacked):
+            for _ in range(3):
+                iteration(stacked)
+            stream.synchronize()
+            n = max(5, min(args.steps, 20))
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            for _ in range(n):
+                iteration(stacked)
+            s1.record(stream)
+            stream.synchronize()
+            hb.hb_check_status(stream)
+            return s0.elapsed_time(s1) / n
+
+        ms = timed(True)
+        ms_calls = timed(False)
         T = runner.n_rows
         profile.append((tau, ms))
         print(json.dumps({"calibrate": "profile", "weights": fmt, "layers": L, "tau": tau, "rows": T,
-                          "iteration_ms": ms, "layer_ms": ms / L, "tokens_per_s": T / (ms / 1e3)}), flush=True)
+                          "iteration_ms": ms, "layer_ms": ms / L, "tokens_per_s": T / (ms / 1e3),
+                          "layer_calls_ms": ms_calls}), flush=True)
         del ws
     c_star = [r for r in run_sweep(args, [64], emit=False) if r["sweep"] == "c_star"][0]
     tau, knee = select_tau(profile, args.calibrate)

@@ -87,6 +87,9 @@ PROTOTYPES = {
     "hb_fold_gamma": (C.c_int, [vp, vp, vp, i32, i32, vp]),
     "hb_layer_workspace_bytes": (C.c_size_t, [C.POINTER(hb_layer_dims), i32, i32, i32]),
     "hb_layer_kernel_count": (C.c_int, [C.POINTER(hb_layer_dims), i32, i32, p_i32]),
+    "hb_layers_forward": (C.c_int, [C.POINTER(hb_layer_weights), i32, C.POINTER(hb_layer_dims),
+                                    C.POINTER(hb_device_plan), vp, i32, vp, vp, C.POINTER(vp), C.POINTER(vp), i32,
+                                    i32, vp, C.c_size_t, vp]),
     "hb_layer_forward": (C.c_int, [C.POINTER(hb_layer_weights), C.POINTER(hb_layer_dims),
                                    C.POINTER(hb_device_plan), vp, i32, vp, vp, vp, vp, i32, i32, vp, C.c_size_t, vp,
                                    C.POINTER(hb_profile)]),

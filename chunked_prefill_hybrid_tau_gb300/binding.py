@@ -431,6 +431,23 @@ def hb_layer_forward(w: LayerWeights, dims, dplan: DevicePlan, rope, max_pos, x_
                                   C.byref(prof) if prof is not None else None), "hb_layer_forward")
 
 
+def hb_layers_forward(ws_list, dims, dplan: DevicePlan, rope, max_pos, x_in, x_out, k_caches, v_caches, max_kv_len,
+                      workspace, stream=None):
+    """Layers back to back: ws_list[l] with k_caches[l], v_caches[l]."""
+    n = len(ws_list)
+    assert len(k_caches) == n and len(v_caches) == n
+    ds = dims_struct(dims)
+    ps = dplan.struct()
+    warr = (L.hb_layer_weights * max(n, 1))(*[w.struct() for w in ws_list])
+    karr = (C.c_void_p * max(n, 1))(*[k.data_ptr() for k in k_caches])
+    varr = (C.c_void_p * max(n, 1))(*[v.data_ptr() for v in v_caches])
+    num_pages = int(k_caches[0].shape[0]) if n else 1
+    _check(lib().hb_layers_forward(warr, n, C.byref(ds), C.byref(ps), _p(rope), int(max_pos), _p(x_in), _p(x_out),
+                                   karr, varr, num_pages, int(max_kv_len), _p(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+           "hb_layers_forward")
+
+
 def hb_final_logits(x, rows, g_f, w_lm, logits, workspace, eps, stream=None):
     T, d = x.shape
     vocab = w_lm.shape[0]

@@ -156,12 +156,14 @@ template <int DH>
 __global__ void kv_append_kernel(const __nv_bfloat16* __restrict__ qkv, const int* __restrict__ row_pos,
                                  const int* __restrict__ slots, const float2* __restrict__ rope, int max_pos, int n_q,
                                  int n_kv, __nv_bfloat16* __restrict__ q_out, __nv_bfloat16* __restrict__ kc,
-                                 __nv_bfloat16* __restrict__ vc, long long num_slots, int* status) {
+                                 __nv_bfloat16* __restrict__ vc, long long num_slots, int* status, int* zero,
+                                 int n_zero) {
   constexpr int HALF = DH / 2;
   constexpr int RC = HALF / 8;  // rotating threads per head
   constexpr int VC = DH / 8;    // copy threads per v head
   griddep_launch_dependents();
   griddep_wait();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_zero; i += gridDim.x * blockDim.x) zero[i] = 0;
   const int r = blockIdx.x;
   const int pos = row_pos[r];
   const int slot = slots[r];
@@ -266,7 +268,7 @@ hb_status row_sumsq_launch(const DeviceCtx& ctx, const void* x, float* ss, int r
 
 hb_status kv_append_launch(const DeviceCtx& ctx, const void* qkv, int T, const int* row_pos, const int* slots,
                            const void* rope, int max_pos, const hb_layer_dims& dm, void* q_out, void* k_cache,
-                           void* v_cache, int num_pages, cudaStream_t stream) {
+                           void* v_cache, int num_pages, cudaStream_t stream, int* zero, int n_zero) {
   if (T == 0) return HB_OK;
   const int per_row = (dm.n_q + dm.n_kv) * (dm.d_head / 16) + dm.n_kv * (dm.d_head / 8);
   const int threads = per_row < 1024 ? ((per_row + 31) / 32) * 32 : 1024;
@@ -278,9 +280,9 @@ hb_status kv_append_launch(const DeviceCtx& ctx, const void* qkv, int T, const i
   auto* rp = static_cast<const float2*>(rope);
   if (dm.d_head == 128)
     return launch_pdl(kv_append_kernel<128>, T, threads, 0, stream, "kv_append_kernel launch", in, row_pos, slots, rp,
-                      max_pos, dm.n_q, dm.n_kv, qo, kc, vc, num_slots, ctx.status);
+                      max_pos, dm.n_q, dm.n_kv, qo, kc, vc, num_slots, ctx.status, zero, n_zero);
   return launch_pdl(kv_append_kernel<64>, T, threads, 0, stream, "kv_append_kernel launch", in, row_pos, slots, rp,
-                    max_pos, dm.n_q, dm.n_kv, qo, kc, vc, num_slots, ctx.status);
+                    max_pos, dm.n_q, dm.n_kv, qo, kc, vc, num_slots, ctx.status, zero, n_zero);
 }
 
 hb_status check_dims(const hb_layer_dims* dm) {

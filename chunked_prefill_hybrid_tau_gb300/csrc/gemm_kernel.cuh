@@ -141,6 +141,27 @@ __device__ __forceinline__ void store_chunk(const Params& p, int row, int col, c
   }
 }
 
+// Sum of squares of 32 bf16 values held as 16 packed pairs, formed as
+// row_sumsq_kernel forms a 32-column part: an fma chain over each 8-value
+// vector, then (v0 + v1) + (v2 + v3).  Every producer of row statistics
+// uses this order, so a row's statistics have the same bits whichever
+// kernel wrote them.
+__device__ __forceinline__ float sumsq32(const uint32_t (&w)[16]) {
+  float v[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float a = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = unpack_bf16x2(w[4 * i + j]);
+      a = __fmaf_rn(f.x, f.x, a);
+      a = __fmaf_rn(f.y, f.y, a);
+    }
+    v[i] = a;
+  }
+  return __fadd_rn(__fadd_rn(v[0], v[1]), __fadd_rn(v[2], v[3]));
+}
+
 // RESIDUAL: C = R + acc for 32 columns, with the residual already loaded
 // (rv); writes the sum of squares of the 32 rounded outputs to ss_dst when
 // it is given.
@@ -157,16 +178,7 @@ __device__ __forceinline__ void residual_chunk(const Params& p, int row, int col
       w[4 * i + j] = pack_bf16x2(__fadd_rn(f.x, __uint_as_float(r[e])), __fadd_rn(f.y, __uint_as_float(r[e + 1])));
     }
   }
-  if (ss_dst) {
-    float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float2 f = unpack_bf16x2(w[i]);
-      ss = __fmaf_rn(f.x, f.x, ss);
-      ss = __fmaf_rn(f.y, f.y, ss);
-    }
-    *ss_dst = ss;
-  }
+  if (ss_dst) *ss_dst = sumsq32(w);
   uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) + static_cast<size_t>(row) * p.ldc + col);
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -431,25 +443,22 @@ __device__ __forceinline__ bool epilogue_last(const Params& p, const CUtensorMap
         }
         const int col = n_blk * BN + cl;
         if constexpr (F8) scale_cols(r, rowf, p.sb, col, p.N);
-        float ss = 0.f;
+        uint32_t w[16];
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           uint4* q = reinterpret_cast<uint4*>(slab + slab_off(rloc, h * 4 + c4));
           const uint4 rv = *q;
           const uint32_t rr[4] = {rv.x, rv.y, rv.z, rv.w};
-          uint32_t w[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const float2 f = unpack_bf16x2(rr[j]);
             const int e = 8 * c4 + 2 * j;
-            w[j] = pack_bf16x2(__fadd_rn(f.x, __uint_as_float(r[e])), __fadd_rn(f.y, __uint_as_float(r[e + 1])));
-            const float2 o = unpack_bf16x2(w[j]);
-            ss = __fmaf_rn(o.x, o.x, ss);
-            ss = __fmaf_rn(o.y, o.y, ss);
+            w[4 * c4 + j] =
+                pack_bf16x2(__fadd_rn(f.x, __uint_as_float(r[e])), __fadd_rn(f.y, __uint_as_float(r[e + 1])));
           }
-          *q = make_uint4(w[0], w[1], w[2], w[3]);
+          *q = make_uint4(w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2], w[4 * c4 + 3]);
         }
-        ss_sm[2 * s + h] = ss;
+        ss_sm[2 * s + h] = sumsq32(w);
       }
     }
     if (p.norm.ss_out != nullptr && row_ok) {

@@ -94,43 +94,57 @@ extern "C" hb_status hb_layer_kernel_count(const hb_layer_dims* dims, int32_t n_
   return HB_OK;
 }
 
-extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_dims* dims, const hb_device_plan* plan,
-                                      const void* rope, int32_t max_pos, const void* x_in, void* x_out, void* k_cache,
-                                      void* v_cache, int32_t num_pages, int32_t max_kv_len, void* workspace,
-                                      size_t ws_bytes, void* stream, const hb_profile* prof) {
-  using namespace hb;
-  clear_error();
-  hb_status st = check_dims(dims);
-  if (st != HB_OK) return st;
-  HB_REQUIRE(w && plan, "hb_layer_forward: null weights or plan");
-  HB_REQUIRE(w->w_qkv && w->w_o && w->w_gu && w->w_d, "hb_layer_forward: null weight");
-  HB_REQUIRE(w->format == HB_WEIGHTS_BF16 || w->format == HB_WEIGHTS_E4M3, "hb_layer_forward: unknown format %d",
+namespace hb {
+namespace {
+
+// Argument checks of one layer's weights.
+hb_status check_weights(const hb_layer_weights* w, const hb_layer_dims* dims) {
+  HB_REQUIRE(w, "layer forward: null weights");
+  HB_REQUIRE(w->w_qkv && w->w_o && w->w_gu && w->w_d, "layer forward: null weight");
+  HB_REQUIRE(w->format == HB_WEIGHTS_BF16 || w->format == HB_WEIGHTS_E4M3, "layer forward: unknown format %d",
              w->format);
   const bool f8 = w->format == HB_WEIGHTS_E4M3;
-  HB_REQUIRE(!f8 || (w->s_qkv && w->s_o && w->s_gu && w->s_d), "hb_layer_forward: E4M3 weights need scales");
+  HB_REQUIRE(!f8 || (w->s_qkv && w->s_o && w->s_gu && w->s_d), "layer forward: E4M3 weights need scales");
   HB_REQUIRE(!f8 || (aligned16(w->s_qkv) && aligned16(w->s_o) && aligned16(w->s_gu) && aligned16(w->s_d)),
-             "hb_layer_forward: E4M3 scales must be 16-byte aligned");
-  HB_REQUIRE(!f8 || dims->d_ff % 16 == 0, "hb_layer_forward: E4M3 weights need d_ff %% 16 == 0");
-  HB_REQUIRE(x_in && x_out && k_cache && v_cache && rope, "hb_layer_forward: null pointer");
-  HB_REQUIRE(plan->n_rows >= 0 && plan->n_seqs >= 0, "hb_layer_forward: bad plan sizes");
+             "layer forward: E4M3 scales must be 16-byte aligned");
+  HB_REQUIRE(!f8 || dims->d_ff % 16 == 0, "layer forward: E4M3 weights need d_ff %% 16 == 0");
+  return HB_OK;
+}
+
+// Argument checks shared by every layer of a call (dims already checked).
+hb_status check_call(const hb_layer_dims* dims, const hb_device_plan* plan, const void* rope, int max_pos,
+                     const void* x_in, const void* x_out, int num_pages, int max_kv_len, const void* workspace,
+                     size_t ws_bytes) {
+  HB_REQUIRE(plan, "layer forward: null plan");
+  HB_REQUIRE(x_in && x_out && rope, "layer forward: null pointer");
+  HB_REQUIRE(plan->n_rows >= 0 && plan->n_seqs >= 0, "layer forward: bad plan sizes");
   HB_REQUIRE(plan->n_rows == 0 || (plan->row_pos && plan->slot_mapping && plan->seq_q_start && plan->seq_kv_len &&
                                    plan->block_table),
-             "hb_layer_forward: null plan array");
-  HB_REQUIRE(num_pages > 0 && max_pos > 0 && max_kv_len > 0, "hb_layer_forward: bad sizes");
-  HB_REQUIRE(prof == nullptr || (prof->events && prof->n_events >= HB_LAYER_STAGES + 1),
-             "hb_layer_forward: profile needs %d events", HB_LAYER_STAGES + 1);
-  HB_REQUIRE(aligned16(x_in) && aligned16(x_out) && aligned16(rope), "hb_layer_forward: 16-byte alignment");
+             "layer forward: null plan array");
+  HB_REQUIRE(num_pages > 0 && max_pos > 0 && max_kv_len > 0, "layer forward: bad sizes");
+  HB_REQUIRE(aligned16(x_in) && aligned16(x_out) && aligned16(rope), "layer forward: 16-byte alignment");
+  if (plan->n_rows == 0) return HB_OK;
+  const size_t need = layer_ws(*dims, plan->n_rows, plan->n_seqs, max_kv_len).total;
+  HB_REQUIRE(workspace && ws_bytes >= need, "layer forward: workspace of %zu bytes needed, %zu given", need, ws_bytes);
+  HB_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, "layer forward: workspace 256-byte alignment");
+  return HB_OK;
+}
+
+// One layer (arguments checked, T > 0).  x_stats: the row statistics of
+// x_in are already in the workspace (the previous layer's down projection
+// wrote them), so the statistics kernel is left out; stats_next: the down
+// projection also writes the statistics of x_out, for the next layer.
+// Both are formed in the same order, so the results do not depend on which
+// kernel produced them.
+hb_status run_layer(const DeviceCtx& ctx, const hb_layer_weights* w, const hb_layer_dims* dims,
+                    const hb_device_plan* plan, const void* rope, int max_pos, const void* x_in, void* x_out,
+                    void* k_cache, void* v_cache, int num_pages, int max_kv_len, void* workspace, cudaStream_t s,
+                    const hb_profile* prof, bool x_stats, bool stats_next) {
+  hb_status st = HB_OK;
+  const bool f8 = w->format == HB_WEIGHTS_E4M3;
   const int T = plan->n_rows;
-  if (T == 0) return HB_OK;
   const hb_layer_dims& dm = *dims;
   const LayerWs lw = layer_ws(dm, T, plan->n_seqs, max_kv_len);
-  HB_REQUIRE(workspace && ws_bytes >= lw.total, "hb_layer_forward: workspace of %zu bytes needed, %zu given",
-             lw.total, ws_bytes);
-  HB_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, "hb_layer_forward: workspace 256-byte alignment");
-  DeviceCtx ctx;
-  st = device_context(&ctx);
-  if (st != HB_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* ss_x = reinterpret_cast<float*>(ws + lw.ss_x);
   float* ss_h = reinterpret_cast<float*>(ws + lw.ss_h);
@@ -175,18 +189,21 @@ extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_
   rope_qkv.max_pos = max_pos;
   rope_qkv.num_slots = static_cast<long long>(num_pages) * 16;
   const int qkv_epi = fuse_rope ? kEpiRope : HB_EPI_STORE;
-  GemmNorm norm_x, norm_h_out, norm_h_in;
+  GemmNorm norm_x, norm_h_out, norm_h_in, norm_x_next;
   norm_x.ss_in = ss_x;
   norm_h_out.ss_out = ss_h;
   norm_h_in.ss_in = ss_h;
-  for (GemmNorm* nm : {&norm_x, &norm_h_out, &norm_h_in}) {
+  norm_x_next.ss_out = ss_x;  // the next layer's input statistics (read by this layer's QKV long before)
+  for (GemmNorm* nm : {&norm_x, &norm_h_out, &norm_h_in, &norm_x_next}) {
     nm->parts = d / 32;
     nm->inv_d = 1.0f / d;
     nm->eps = dm.rms_eps;
   }
   // split-K workspaces of the o and down projections: fp32 partial tiles
   // and arrival counters, and the attention counters after them: zeroed by
-  // the layer's first kernel (row statistics or the quantization of x)
+  // the quantization of x (E4M3) or by the RoPE/KV append (bf16), both
+  // ahead of every kernel that uses them and behind every kernel of the
+  // previous layer
   const int n_flags = gemm_split_flags(T, d);
   const int n_zero = static_cast<int>((lw.attn - lw.flags + attention_counter_bytes(dm, plan->n_seqs)) / 4);
   GemmSplit split_o, split_d;
@@ -221,23 +238,83 @@ extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_
                           &norm_h_in);
     if (st != HB_OK) return st;
     HB_STEP(7, quant_rows_launch(ctx, a, aq, sa, T, fp, nullptr, nullptr, 0, s));
-    st = gemm_e4m3_launch(ctx, aq, fp, sa, w->w_d, w->s_d, x_out, d, h, T, d, dm.d_ff, HB_EPI_RESIDUAL, s, nullptr,
-                          &split_d);
+    st = gemm_e4m3_launch(ctx, aq, fp, sa, w->w_d, w->s_d, x_out, d, h, T, d, dm.d_ff, HB_EPI_RESIDUAL, s,
+                          stats_next ? &norm_x_next : nullptr, &split_d);
     if (st != HB_OK) return st;
     return mark(HB_LAYER_STAGES);
   }
-  HB_STEP(0, row_sumsq_launch(ctx, x_in, ss_x, T, d, split_o.flags, n_zero, s));
+  HB_STEP(0, x_stats ? HB_OK : row_sumsq_launch(ctx, x_in, ss_x, T, d, nullptr, 0, s));
   HB_STEP(1, gemm_launch(ctx, x_in, d, w->w_qkv, qkv, qkv_cols, nullptr, T, qkv_cols, d, HB_EPI_STORE, s, &norm_x));
   HB_STEP(2, kv_append_launch(ctx, qkv, T, plan->row_pos, plan->slot_mapping, rope, max_pos, dm, q, k_cache, v_cache,
-                              num_pages, s));
+                              num_pages, s, split_o.flags, n_zero));
   HB_STEP(3, attention_launch(ctx, q, k_cache, v_cache, num_pages, *plan, dm, max_kv_len, o, aws,
                               lw.total - lw.attn, s, true));
   HB_STEP(4, gemm_launch(ctx, o, hd, w->w_o, h, d, x_in, T, d, hd, HB_EPI_RESIDUAL, s, &norm_h_out, &split_o));
   HB_STEP(5, HB_OK);  // rmsnorm2: statistics came from the o projection, scaling goes to gate/up
   HB_STEP(6, gemm_launch(ctx, h, d, w->w_gu, a, fp, nullptr, T, 2 * fp, d, HB_EPI_SWIGLU, s, &norm_h_in));
-  HB_STEP(7, gemm_launch(ctx, a, fp, w->w_d, x_out, d, h, T, d, dm.d_ff, HB_EPI_RESIDUAL, s, nullptr, &split_d));
+  HB_STEP(7, gemm_launch(ctx, a, fp, w->w_d, x_out, d, h, T, d, dm.d_ff, HB_EPI_RESIDUAL, s,
+                         stats_next ? &norm_x_next : nullptr, &split_d));
 #undef HB_STEP
   return mark(HB_LAYER_STAGES);
+}
+
+
+}  // namespace
+}  // namespace hb
+
+extern "C" hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_dims* dims, const hb_device_plan* plan,
+                                      const void* rope, int32_t max_pos, const void* x_in, void* x_out, void* k_cache,
+                                      void* v_cache, int32_t num_pages, int32_t max_kv_len, void* workspace,
+                                      size_t ws_bytes, void* stream, const hb_profile* prof) {
+  using namespace hb;
+  clear_error();
+  hb_status st = check_dims(dims);
+  if (st != HB_OK) return st;
+  st = check_weights(w, dims);
+  if (st != HB_OK) return st;
+  st = check_call(dims, plan, rope, max_pos, x_in, x_out, num_pages, max_kv_len, workspace, ws_bytes);
+  if (st != HB_OK) return st;
+  HB_REQUIRE(k_cache && v_cache, "hb_layer_forward: null KV cache");
+  HB_REQUIRE(prof == nullptr || (prof->events && prof->n_events >= HB_LAYER_STAGES + 1),
+             "hb_layer_forward: profile needs %d events", HB_LAYER_STAGES + 1);
+  if (plan->n_rows == 0) return HB_OK;
+  DeviceCtx ctx;
+  st = device_context(&ctx);
+  if (st != HB_OK) return st;
+  return run_layer(ctx, w, dims, plan, rope, max_pos, x_in, x_out, k_cache, v_cache, num_pages, max_kv_len, workspace,
+                   static_cast<cudaStream_t>(stream), prof, false, false);
+}
+
+extern "C" hb_status hb_layers_forward(const hb_layer_weights* w, int32_t n_layers, const hb_layer_dims* dims,
+                                       const hb_device_plan* plan, const void* rope, int32_t max_pos, const void* x_in,
+                                       void* x_out, void* const* k_caches, void* const* v_caches, int32_t num_pages,
+                                       int32_t max_kv_len, void* workspace, size_t ws_bytes, void* stream) {
+  using namespace hb;
+  clear_error();
+  hb_status st = check_dims(dims);
+  if (st != HB_OK) return st;
+  HB_REQUIRE(w && k_caches && v_caches && n_layers >= 0, "hb_layers_forward: null array or negative layer count");
+  for (int l = 0; l < n_layers; ++l) {
+    st = check_weights(w + l, dims);
+    if (st != HB_OK) return st;
+    HB_REQUIRE(k_caches[l] && v_caches[l], "hb_layers_forward: null KV cache of layer %d", l);
+  }
+  st = check_call(dims, plan, rope, max_pos, x_in, x_out, num_pages, max_kv_len, workspace, ws_bytes);
+  if (st != HB_OK) return st;
+  if (plan->n_rows == 0 || n_layers == 0) return HB_OK;
+  DeviceCtx ctx;
+  st = device_context(&ctx);
+  if (st != HB_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int l = 0; l < n_layers; ++l) {
+    // a bf16 layer takes its input statistics from the layer before it
+    const bool next_bf16 = l + 1 < n_layers && w[l + 1].format == HB_WEIGHTS_BF16;
+    const bool x_stats = l > 0 && w[l].format == HB_WEIGHTS_BF16;
+    st = run_layer(ctx, w + l, dims, plan, rope, max_pos, l == 0 ? x_in : x_out, x_out, k_caches[l], v_caches[l],
+                   num_pages, max_kv_len, workspace, s, nullptr, x_stats, next_bf16);
+    if (st != HB_OK) return st;
+  }
+  return HB_OK;
 }
 
 extern "C" hb_status hb_final_logits(const void* x, int32_t T, const int32_t* rows, int32_t n_sel, const void* g_f,

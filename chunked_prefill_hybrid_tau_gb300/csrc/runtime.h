@@ -86,9 +86,11 @@ hb_status check_dims(const hb_layer_dims* dims);
 // Launchers (arguments already checked; asynchronous on `stream`).
 hb_status rmsnorm_launch(const DeviceCtx& ctx, const void* x, const int* rows, const void* gamma, void* y,
                          int n_rows, int d, float eps, int n_src, cudaStream_t stream);
+// zero / n_zero: ints cleared after the kernel's wait for its inputs (the
+// layer's split-K and attention counters; nullptr, 0 for none).
 hb_status kv_append_launch(const DeviceCtx& ctx, const void* qkv, int T, const int* row_pos, const int* slots,
                            const void* rope, int max_pos, const hb_layer_dims& dims, void* q_out, void* k_cache,
-                           void* v_cache, int num_pages, cudaStream_t stream);
+                           void* v_cache, int num_pages, cudaStream_t stream, int* zero = nullptr, int n_zero = 0);
 hb_status gemm_check(const void* A, const void* B, void* C, const void* R, int M, int N, int K, int epi);
 
 // RMSNorm folded into the projections.  Row statistics are 32-column partial

@@ -427,6 +427,27 @@ hb_status hb_layer_forward(const hb_layer_weights* w, const hb_layer_dims* dims,
                            void* k_cache, void* v_cache, int32_t num_pages, int32_t max_kv_len,
                            void* workspace, size_t ws_bytes, void* stream, const hb_profile* prof);
 
+/* ------------------------------------------------------------------------
+ * hb_layers_forward - the layer stack of one hybrid iteration: n_layers
+ * decoder layers back to back over the same packed batch, each layer's
+ * output the next one's input (the per-layer "run_iteration(B)" step of the
+ * scheduling loop, Sarathi-Serve reading notes section 3.4, repeated down
+ * the model).  Layer l uses w[l] and the KV pools k_caches[l], v_caches[l]
+ * (host arrays of n_layers device pointers); layer 0 reads x_in, every
+ * layer writes x_out (x_out may alias x_in); one workspace serves all
+ * layers (hb_layer_workspace_bytes).  The results are those of n_layers
+ * hb_layer_forward calls, bit for bit: a bf16 layer after the first takes
+ * the row statistics of its input from the previous layer's down
+ * projection, which writes them in the same order as the statistics
+ * kernel, and that kernel is left out (one launch less per layer).
+ * Errors as hb_layer_forward; nothing is launched when any layer's
+ * arguments are invalid.
+ * ---------------------------------------------------------------------- */
+hb_status hb_layers_forward(const hb_layer_weights* w, int32_t n_layers, const hb_layer_dims* dims,
+                            const hb_device_plan* plan, const void* rope, int32_t max_pos, const void* x_in,
+                            void* x_out, void* const* k_caches, void* const* v_caches, int32_t num_pages,
+                            int32_t max_kv_len, void* workspace, size_t ws_bytes, void* stream);
+
 /* hb_layer_kernel_count - how many kernels one hb_layer_forward call launches
  * for n_rows packed rows with weights in `format` (host logic only, no
  * device call; the chunk and decode attention kernels

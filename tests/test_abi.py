@@ -82,3 +82,33 @@ def test_idle_iteration_is_a_no_op(lib):
     st = lib.hb_layer_forward(C.byref(w), C.byref(ds), C.byref(plan), fake, 64, fake, fake, fake, fake, 8, 64,
                               None, 0, None, None)
     assert st == L.HB_ERR_INVALID_ARG and b"null plan array" in lib.hb_last_error()
+
+
+def test_layer_stack_checks_every_layer_before_launching(lib):
+    """hb_layers_forward validates all layers' arguments before any device
+    work: an idle iteration is a no-op, and a bad later layer is an argument
+    error (no GPU needed for either)."""
+    import workloads as wl
+    ds = B.dims_struct(wl.TINY)
+    fake = C.c_void_p(4096)  # never dereferenced
+    good = L.hb_layer_weights(fake, fake, fake, fake, None, None, None, None, L.HB_WEIGHTS_BF16)
+    e4m3_no_scales = L.hb_layer_weights(fake, fake, fake, fake, None, None, None, None, L.HB_WEIGHTS_E4M3)
+    plan = L.hb_device_plan(0, 0, 1, None, None, None, None, None, 0, 0, 0)
+    ks = (C.c_void_p * 3)(4096, 4096, 4096)
+    vs = (C.c_void_p * 3)(4096, 4096, 4096)
+
+    def call(ws, n, k=ks, v=vs):
+        return lib.hb_layers_forward(ws, n, C.byref(ds), C.byref(plan), fake, 64, fake, fake, k, v, 8, 64, None, 0,
+                                     None)
+
+    st = call((L.hb_layer_weights * 3)(good, good, good), 3)
+    assert st == L.HB_OK, lib.hb_last_error()
+    assert call((L.hb_layer_weights * 3)(good, good, good), 0) == L.HB_OK
+    assert call((L.hb_layer_weights * 3)(good, good, e4m3_no_scales), 3) == L.HB_ERR_INVALID_ARG
+    assert b"scales" in lib.hb_last_error()
+    v_null = (C.c_void_p * 3)(4096, None, 4096)
+    assert call((L.hb_layer_weights * 3)(good, good, good), 3, v=v_null) == L.HB_ERR_INVALID_ARG
+    assert b"layer 1" in lib.hb_last_error()
+    assert call((L.hb_layer_weights * 3)(good, good, good), -1) == L.HB_ERR_INVALID_ARG
+    assert lib.hb_layers_forward(None, 1, C.byref(ds), C.byref(plan), fake, 64, fake, fake, ks, vs, 8, 64, None, 0,
+                                 None) == L.HB_ERR_INVALID_ARG

@@ -1,6 +1,7 @@
 """Model-level parity: the 32-layer Mistral-7B-shaped model with its LM head
-(tau = 2048) and the 60-layer Yi-34B-shaped model (tau = 1024), all layers
-through hb_layer_forward and the logits through hb_final_logits (GPU).
+(tau = 2048, layer by layer through hb_layer_forward) and the 60-layer
+Yi-34B-shaped model (tau = 1024, the whole stack in one hb_layers_forward
+call), the logits through hb_final_logits (GPU).
 
 The oracle follows sampled decode rows through every layer from the original
 inputs: a decode row's output depends only on its own hidden state and its
@@ -69,13 +70,17 @@ def run_model(dims, tau, dec_ctx, prompt_len, sample, vocab, seed, full_layers=(
     idx = torch.tensor(sample_pages, device="cuda")
     host_kv = [(wd.to_numpy(k[idx]), wd.to_numpy(v[idx])) for k, v in pools]
     full = {}
-    for l in range(dims.n_layers):
-        k, v = pools[l]
-        if l in full_layers:
-            full[l] = [wd.to_numpy(x), wd.to_numpy(k), wd.to_numpy(v)]
-        hb.hb_layer_forward(layers[l], dims, dp, rope, max_kv + 1, x, x, k, v, max_kv, ws)
-        if l in full_layers:
-            full[l].append(wd.to_numpy(x))
+    if full_layers:
+        for l in range(dims.n_layers):
+            k, v = pools[l]
+            if l in full_layers:
+                full[l] = [wd.to_numpy(x), wd.to_numpy(k), wd.to_numpy(v)]
+            hb.hb_layer_forward(layers[l], dims, dp, rope, max_kv + 1, x, x, k, v, max_kv, ws)
+            if l in full_layers:
+                full[l].append(wd.to_numpy(x))
+    else:  # the whole stack in one call
+        hb.hb_layers_forward(layers, dims, dp, rope, max_kv + 1, x, x, [k for k, _ in pools], [v for _, v in pools],
+                             max_kv, ws)
     hb.hb_check_status()
     rows = torch.tensor(list(range(n_dec)) + [T - 1], dtype=torch.int32, device="cuda")
     logits = None
