@@ -207,8 +207,8 @@ __device__ __forceinline__ void scale_cols(uint32_t (&r)[32], float rowf, const 
 // columns; here it arrives on the tile's counter and waits (bounded) for the
 // partner's arrival, after which the partner's partial of its own columns is
 // in place.  Own + partner is commutative, so either half's sum has the same
-// bits.  The counters must be zero at launch (the layer's first kernel
-// clears them); both halves of a tile run in the same round of the
+// bits.  The counters must be zero at launch (the layer clears them in a
+// kernel ahead of its projections); both halves of a tile run in the same round of the
 // persistent grid (consecutive units on an even number of clusters).
 __device__ __forceinline__ bool split_exchange(const Params& p, int stile, bool leader, volatile int* ep_flag,
                                                volatile int* abort_flag) {

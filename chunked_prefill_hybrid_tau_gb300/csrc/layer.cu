@@ -55,7 +55,7 @@ LayerWs layer_ws(const hb_layer_dims& dm, int T, int S, int max_kv_len) {
   w.q8_a = off; off += align256(t * ffn_pad(dm));
   w.s8 = off;   off += 4 * align256(t * 4);
   // split-K counters right before the attention workspace, whose counters
-  // come first: the layer's first kernel zeroes both in one range
+  // come first: one kernel of the layer zeroes both in one range
   w.flags = off;  off += align256(static_cast<size_t>(2) * gemm_split_flags(T, dm.d_model) * 4);
   w.attn = off; off += align256(attention_workspace_bytes(dm, S, max_kv_len));
   w.total = off;

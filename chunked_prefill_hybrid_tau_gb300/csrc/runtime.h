@@ -108,7 +108,7 @@ struct GemmNorm {
 
 // Split-K workspace for RESIDUAL projections (fp32 partial tiles and arrival
 // counters; the counters must be zero at launch and are not cleared by the
-// kernel: the layer's first kernel zeroes them).  Used when
+// kernel: a kernel ahead of the projections zeroes them).  Used when
 // gemm_split_k(N, K, epi) holds, which depends on the shape only.
 struct GemmSplit {
   float* part = nullptr;
@@ -174,7 +174,8 @@ size_t attention_workspace_bytes(const hb_layer_dims& dims, int max_seqs, int ma
 // attention kernels start (work and combine counters).
 size_t attention_counter_bytes(const hb_layer_dims& dims, int n_seqs);
 // counters_zeroed: the caller has zeroed the counters on the stream (the
-// layer does it in its first kernel), else they are cleared here.
+// layer does it in a kernel ahead of the attention), else they are cleared
+// here.
 hb_status attention_launch(const DeviceCtx& ctx, const void* q, const void* k_cache, const void* v_cache,
                            int num_pages, const hb_device_plan& plan, const hb_layer_dims& dims, int max_kv_len,
                            void* out, void* ws, size_t ws_bytes, cudaStream_t stream, bool counters_zeroed);
