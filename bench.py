@@ -415,10 +415,15 @@ def run_hb(args, world, rank, local):
     t_clock0 = time.perf_counter()
     barrier(world)
     torch.cuda.synchronize(dev)
+    launches0 = hb.hb_kernel_launches()
     start.record(stream)
     for _ in range(args.steps):
         layer(runner.step(stream), x_dev, out_dev)
     end.record(stream)
+    launches = hb.hb_kernel_launches() - launches0  # this library's kernels in the timed region
+    if launches != launches_per_layer(dims, f8, runner.n_rows) * args.steps:
+        print(f"warning: {launches} kernels launched in the timed region, the library's rule says "
+              f"{launches_per_layer(dims, f8, runner.n_rows) * args.steps}", file=sys.stderr)
     torch.cuda.synchronize(dev)
     barrier(world)
     hb.hb_check_status(stream)
@@ -556,11 +561,11 @@ def run_hb(args, world, rank, local):
                                                                       s_bar)},
         "stages_ms": {k: round(float(v), 5) for k, v in zip(costs.STAGES, stage_ms)},
         "e2e": e2e,
-        # per layer forward: row statistics, QKV, RoPE/KV append, chunk and decode
-        # attention, O, gate/up, down; E4M3: three more quantization kernels,
-        # and RoPE/KV append inside the QKV projection when its tiles hold
-        # whole heads
-        "gpu_launches": launches_per_layer(dims, f8, T) * args.steps,
+        # counted by the library (per layer forward: row statistics, QKV, RoPE/KV
+        # append, chunk and decode attention, O, gate/up, down; E4M3: three more
+        # quantization kernels, RoPE/KV append inside the QKV projection when
+        # its tiles hold whole heads), checked against its rule below
+        "gpu_launches": launches,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

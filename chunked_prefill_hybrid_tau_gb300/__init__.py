@@ -8,15 +8,15 @@ and a thin ctypes binding whose functions carry the C names.
 """
 from .binding import (DevicePlan, HBError, HostPlan, LayerWeights, Scheduler, dims_struct, hb_attention,
                       hb_attention_workspace_bytes, hb_check_status, hb_device_info, hb_final_logits, hb_fold_gamma,
-                      hb_gemm, hb_gemm_e4m3, hb_interleave_gate_up, hb_kv_append, hb_layer_forward,
-                      hb_layer_kernel_count, hb_layer_workspace_bytes, hb_layers_forward, hb_plan_batch,
-                      hb_quantize_e4m3, hb_rmsnorm, hb_rope_table, hb_selftest_wait_timeout, hb_version, lib,
-                      prepare_layer_weights)
+                      hb_gemm, hb_gemm_e4m3, hb_interleave_gate_up, hb_kernel_launches, hb_kv_append,
+                      hb_layer_forward, hb_layer_kernel_count, hb_layer_workspace_bytes, hb_layers_forward,
+                      hb_plan_batch, hb_quantize_e4m3, hb_rmsnorm, hb_rope_table, hb_selftest_wait_timeout,
+                      hb_version, lib, prepare_layer_weights)
 
 __all__ = [
     "DevicePlan", "HBError", "HostPlan", "LayerWeights", "Scheduler", "dims_struct", "hb_attention",
     "hb_attention_workspace_bytes", "hb_check_status", "hb_device_info", "hb_final_logits", "hb_fold_gamma",
-    "hb_gemm", "hb_gemm_e4m3", "hb_interleave_gate_up", "hb_kv_append", "hb_layer_forward", "hb_layer_kernel_count",
-    "hb_layer_workspace_bytes", "hb_layers_forward", "hb_plan_batch", "hb_quantize_e4m3", "hb_rmsnorm",
-    "hb_rope_table", "hb_selftest_wait_timeout", "hb_version", "lib", "prepare_layer_weights",
+    "hb_gemm", "hb_gemm_e4m3", "hb_interleave_gate_up", "hb_kernel_launches", "hb_kv_append", "hb_layer_forward",
+    "hb_layer_kernel_count", "hb_layer_workspace_bytes", "hb_layers_forward", "hb_plan_batch", "hb_quantize_e4m3",
+    "hb_rmsnorm", "hb_rope_table", "hb_selftest_wait_timeout", "hb_version", "lib", "prepare_layer_weights",
 ]

@@ -96,6 +96,7 @@ PROTOTYPES = {
     "hb_final_logits": (C.c_int, [vp, i32, vp, i32, vp, vp, i32, i32, C.c_float, vp, vp, C.c_size_t, vp]),
     "hb_check_status": (C.c_int, [vp]),
     "hb_device_info": (C.c_int, [p_i32, p_i32]),
+    "hb_kernel_launches": (C.c_uint64, []),
     "hb_selftest_wait_timeout": (C.c_int, [i32, vp]),
 }
 

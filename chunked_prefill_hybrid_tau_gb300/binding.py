@@ -62,6 +62,10 @@ def hb_device_info():
     return int(n.value), bool(s.value)
 
 
+def hb_kernel_launches() -> int:
+    return int(lib().hb_kernel_launches())
+
+
 def hb_check_status(stream=None):
     _check(lib().hb_check_status(_stream(stream)), "hb_check_status")
 

@@ -150,9 +150,21 @@ hb_status encode_tmap_kv_pages(CUtensorMap* map, const void* pool, uint64_t rows
   return HB_OK;
 }
 
-hb_status launch_status(const char* what) { return cuda_status(cudaGetLastError(), what); }
+// Kernels launched by this library in this process (all devices and host
+// threads).
+static std::atomic<uint64_t> g_launches{0};
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+hb_status launch_status(const char* what) {
+  const hb_status st = cuda_status(cudaGetLastError(), what);
+  if (st == HB_OK) count_launch();
+  return st;
+}
 
 }  // namespace hb
+
+extern "C" uint64_t hb_kernel_launches(void) { return hb::g_launches.load(std::memory_order_relaxed); }
 
 extern "C" hb_status hb_check_status(void* stream) {
   hb::clear_error();

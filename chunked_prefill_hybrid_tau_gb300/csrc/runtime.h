@@ -22,7 +22,10 @@ struct DeviceCtx {
 hb_status device_context(DeviceCtx* ctx);
 
 hb_status cuda_status(cudaError_t e, const char* what);
+// After a <<<...>>> launch: its error, and the launch counted when accepted.
 hb_status launch_status(const char* what);
+// Counts one accepted kernel launch (hb_kernel_launches reads the total).
+void count_launch();
 
 // 2D tensor map of bf16 (elem_bytes 2), byte (elem_bytes 1: E4M3 codes) or
 // fp32 (elem_bytes 4) elements: `outer` rows of `inner` elements, rows
@@ -66,7 +69,9 @@ hb_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_status(cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...), what);
+  const hb_status st = cuda_status(cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...), what);
+  if (st == HB_OK) count_launch();
+  return st;
 }
 
 hb_status encode_tmap_q3d(CUtensorMap* map, const void* q, int T, int n_q, int d_head);

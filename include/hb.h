@@ -480,6 +480,12 @@ hb_status hb_check_status(void* stream);
 /* Number of SMs of the current device and whether it is sm_103 (1/0). */
 hb_status hb_device_info(int32_t* num_sms, int32_t* is_sm103);
 
+/* Kernels this library has launched in this process so far, over every
+ * device and host thread (a launch counts once the CUDA runtime accepts
+ * it).  Read it before and after a region to count that region's kernels;
+ * needs no device. */
+uint64_t hb_kernel_launches(void);
+
 /* ------------------------------------------------------------------------
  * hb_selftest_wait_timeout - exercise the failure path of the bounded
  * device waits without faulting the GPU.  The pages define no such

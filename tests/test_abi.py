@@ -112,3 +112,13 @@ def test_layer_stack_checks_every_layer_before_launching(lib):
     assert call((L.hb_layer_weights * 3)(good, good, good), -1) == L.HB_ERR_INVALID_ARG
     assert lib.hb_layers_forward(None, 1, C.byref(ds), C.byref(plan), fake, 64, fake, fake, ks, vs, 8, 64, None, 0,
                                  None) == L.HB_ERR_INVALID_ARG
+
+
+def test_launch_counter_needs_no_device(lib):
+    """hb_kernel_launches is readable without a GPU, and calls that fail
+    their argument checks launch nothing."""
+    n0 = lib.hb_kernel_launches()
+    assert lib.hb_gemm(None, None, None, None, 128, 128, 128, 0, None) == L.HB_ERR_INVALID_ARG
+    assert lib.hb_selftest_wait_timeout(0, None) == L.HB_ERR_INVALID_ARG
+    assert lib.hb_kernel_launches() == n0
+    assert B.hb_kernel_launches() == n0

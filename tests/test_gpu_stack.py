@@ -42,17 +42,24 @@ def stack_vs_calls(dims, dec_ctx, prompt_len, done, tau, formats, seed):
     layers = [wd.layer_weights_random(dims, seed * 100 + l, fmt=f) for l, f in enumerate(formats)]
     pools = [(wd.randn_bf16(shape, gen), wd.randn_bf16(shape, gen)) for _ in formats]
 
-    # one call per layer, in place
+    # one call per layer, in place; each launches the kernels the library's rule says
     x1 = x.clone()
     p1 = [(k.clone(), v.clone()) for k, v in pools]
+    per_layer = [hb.hb_layer_kernel_count(dims, T, 1 if f == "e4m3" else 0) for f in formats]
     for l, lw in enumerate(layers):
+        n0 = hb.hb_kernel_launches()
         hb.hb_layer_forward(lw, dims, dp, rope, max_kv + 1, x1, x1, p1[l][0], p1[l][1], max_kv, ws)
+        assert hb.hb_kernel_launches() - n0 == per_layer[l], f"layer {l}"
     hb.hb_check_status()
-    # the stack, out of place (layer 0 reads x, every layer writes x2)
+    # the stack, out of place (layer 0 reads x, every layer writes x2): a bf16
+    # layer after the first launches no statistics kernel
     x2 = torch.full_like(x, float("nan"))
     p2 = [(k.clone(), v.clone()) for k, v in pools]
+    n0 = hb.hb_kernel_launches()
     hb.hb_layers_forward(layers, dims, dp, rope, max_kv + 1, x, x2, [k for k, _ in p2], [v for _, v in p2], max_kv,
                          ws)
+    carried = sum(1 for l, f in enumerate(formats) if l > 0 and f == "bf16")
+    assert hb.hb_kernel_launches() - n0 == sum(per_layer) - carried
     hb.hb_check_status()
     assert torch.isfinite(x1.float()).all()
     assert torch.equal(x1, x2), f"outputs differ (max {float((x1.float() - x2.float()).abs().max())})"
