@@ -90,3 +90,12 @@ def test_stack_equals_layer_calls_mixed_formats():
     rng = np.random.default_rng(4)
     dec_ctx = rng.integers(512, 4097, size=32)
     stack_vs_calls(wl.MISTRAL, dec_ctx, 4096, 1024, 512, ["bf16", "e4m3", "bf16", "e4m3"], seed=13)
+
+
+def test_stack_equals_layer_calls_unfused_e4m3():
+    """3 q heads and 1 kv head of 64 dims: 320 QKV columns, not whole
+    256-column tiles, so E4M3 layers run the separate RoPE/KV append
+    (11 kernels) and bf16 layers between them take carried statistics."""
+    import dataclasses
+    dims = dataclasses.replace(wl.TINY, n_q=3, n_kv=1, d_ff=256)
+    stack_vs_calls(dims, [40, 90, 300], 256, 64, 67, ["e4m3", "bf16", "e4m3", "bf16"], seed=14)
